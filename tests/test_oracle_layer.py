@@ -1,0 +1,247 @@
+"""Pins of the oracle's layer steps against definitions computed another way:
+brute-force subset search for top-k, a library sort for the permutation,
+and small-integer weights whose expert FFN reduces to exact integer matmuls
+plus library sigmoid and brute-force rounding."""
+import itertools
+from collections import Counter
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit, softmax
+
+import oracle
+import synth
+
+
+def bf16_bits(v):
+    return torch.tensor(np.asarray(v, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_vals(u16):
+    return torch.from_numpy(np.asarray(u16, dtype=np.uint16).view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def test_bf16_helpers_agree_with_torch():
+    u = np.arange(0, 65536, 7, dtype=np.uint32).astype(np.uint16)
+    a, b = oracle.bf16_to_f64(u), bf16_vals(u)
+    fin = np.isfinite(b)
+    assert np.array_equal(a[fin], b[fin])
+
+
+def _keys_independent(x16, w16, lb, cb, score_func):
+    logits = bf16_vals(x16) @ bf16_vals(w16).T
+    if lb is not None:
+        logits = logits + lb.astype(np.float64)
+    s = expit(logits) if score_func == 0 else softmax(logits, axis=1)
+    return s, s + (0 if cb is None else cb.astype(np.float64))
+
+
+def _brute_topk(key, k):
+    """Smallest sorted index tuple among the k-subsets S with
+    min(key[S]) >= max(key[not S]) (the defining property of a top-k set)."""
+    E = key.size
+    best = None
+    for S in itertools.combinations(range(E), k):
+        rest = [e for e in range(E) if e not in S]
+        if rest and min(key[list(S)]) < max(key[rest]):
+            continue
+        if best is None or S < best:
+            best = S
+    return best
+
+
+@pytest.mark.parametrize("score_func", [0, 1])
+@pytest.mark.parametrize("k", [1, 2, 3, 8])
+def test_route_matches_brute_force_with_ties(score_func, k):
+    rng = np.random.default_rng(10 + k + 7 * score_func)
+    T, H, E = 6, 64, 8 if k < 8 else 10
+    x = bf16_bits(rng.normal(0, 1, (T, H)))
+    w = rng.normal(0, 0.1, (E, H))
+    w[3] = w[1]                       # experts 1 and 3 tie on every token
+    w[E - 1] = w[0]                   # and 0 with E-1
+    w = bf16_bits(w)
+    lb = rng.normal(0, 0.3, E).astype(np.float32)
+    lb[3], lb[E - 1] = lb[1], lb[0]
+    cb = np.zeros(E, dtype=np.float32)
+    cb[5] = 0.25                      # a correction bias that changes selection only
+    r = oracle.route(x, w, k, score_func, lb, cb)
+    s, key = _keys_independent(x, w, lb, cb, score_func)
+    for t in range(T):
+        expect = _brute_topk(key[t], k)
+        assert tuple(sorted(r.ids[t])) == expect
+        # selection order: key descending, equal keys by index
+        order = sorted(r.ids[t], key=lambda e: (-key[t, e], e))
+        assert list(r.ids[t]) == order
+        g = s[t, r.ids[t]] / s[t, r.ids[t]].sum()
+        np.testing.assert_allclose(r.gates[t], g, rtol=1e-14)
+        assert abs(r.gates[t].sum() - 1) < 1e-14
+        assert len(set(r.ids[t])) == k
+
+
+def test_route_all_equal_scores_pick_lowest_indices():
+    T, H, E, k = 3, 32, 12, 8
+    x = bf16_bits(np.ones((T, H)))
+    w = bf16_bits(np.zeros((E, H)))
+    r = oracle.route(x, w, k)
+    assert (r.ids == np.arange(k)).all()
+    np.testing.assert_allclose(r.gates, 1.0 / k)
+    assert (r.margin == 0).all()
+
+
+def test_dispatch_matches_sorted_definition():
+    rng = np.random.default_rng(11)
+    T, E, k = 50, 12, 4
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    counts, offsets, perm = oracle.dispatch(ids, E)
+    c = Counter(ids.ravel().tolist())
+    assert [c.get(e, 0) for e in range(E)] == counts.tolist()
+    assert offsets[0] == 0 and offsets[-1] == T * k and (np.diff(offsets) == counts).all()
+    triples = sorted((int(ids[t, j]), t, j) for t in range(T) for j in range(k))
+    for row, (e, t, j) in enumerate(triples):
+        assert perm[t * k + j] == row
+    assert sorted(perm.tolist()) == list(range(T * k))
+
+
+# ---- expert FFN special case: weights +-m * 2^p, activations small integers
+def _pack_codes(codes):
+    codes = np.asarray(codes, dtype=np.uint8)
+    return (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+
+
+def _pm_weight(rng, rows, K, mag_code, scale_byte):
+    """Random sign matrix S (+-1) and its MXFP4 encoding with E2M1 magnitude
+    code ``mag_code`` and one E8M0 scale byte for every block."""
+    S = rng.choice([-1.0, 1.0], (rows, K))
+    codes = np.where(S > 0, mag_code, mag_code | 8)
+    return S, _pack_codes(codes), np.full((rows, K // 32), scale_byte, dtype=np.uint8)
+
+
+E2M1 = {2: 1.0, 3: 1.5, 4: 2.0}
+
+
+def _e4m3_nearest(v):
+    """Brute-force nearest e4m3 code (ties to even code) by search over the
+    table of all finite values decoded by torch."""
+    tab = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    codes = np.array([c for c in range(256) if np.isfinite(tab[c])])
+    out = np.empty(v.shape, dtype=np.uint8)
+    for i, x in np.ndenumerate(v):
+        x = min(max(x, -448.0), 448.0)
+        d = np.abs(tab[codes] - x)
+        m = d.min()
+        cand = codes[d == m]
+        if len(cand) > 1:
+            even = cand[(cand & 1) == 0]
+            cand = even if len(even) else cand
+            # equal distance to +0/-0 only at x == 0: keep the sign of x
+            if len(cand) > 1:
+                cand = cand[[(c >> 7) == int(np.signbit(x)) for c in cand]]
+        out[i] = cand[0]
+    return out, tab
+
+
+def _q2_brute(h):
+    """1 x 128 requantisation by search: smallest e with amax <= 448 * 2^e."""
+    n, I = h.shape
+    q = np.empty((n, I), dtype=np.uint8)
+    s = np.empty((n, I // 128), dtype=np.uint8)
+    deq = np.empty_like(h)
+    for r in range(n):
+        for b in range(I // 128):
+            blk = h[r, b * 128:(b + 1) * 128]
+            amax = np.abs(blk).max()
+            e = 0
+            if amax > 0:
+                e = -140
+                while not (amax <= 448.0 * 2.0 ** e):
+                    e += 1
+            codes, tab = _e4m3_nearest(blk / 2.0 ** e)
+            q[r, b * 128:(b + 1) * 128] = codes
+            s[r, b] = e + 127
+            deq[r, b * 128:(b + 1) * 128] = tab[codes] * 2.0 ** e
+    return q, s, deq
+
+
+@pytest.mark.parametrize("E,k", [(1, 1), (2, 2), (3, 2)])
+def test_expert_ffn_small_integer_case(E, k):
+    """x in {-3..3}: Q1 is exact.  W13/W2 are +-m*2^p: gate/up are exact
+    integer matmuls.  SwiGLU by scipy's expit, Q2 by brute force, down-proj and
+    combine in fp64.  Different gate and up sign matrices pin the row order;
+    non-square matrices pin the orientation of every operand."""
+    rng = np.random.default_rng(20 + E)
+    T, H, I = 5, 256, 256
+    x = rng.integers(-3, 4, (T, H)).astype(np.float64)
+    x[:, 0] = 3
+    x16 = bf16_bits(x)
+    wr = bf16_bits(rng.normal(0, 0.05, (E, H)))
+    W13_list, W2_list = [], []
+    w13_q = np.empty((E, 2 * I, H // 2), np.uint8)
+    w13_s = np.empty((E, 2 * I, H // 32), np.uint8)
+    w2_q = np.empty((E, H, I // 2), np.uint8)
+    w2_s = np.empty((E, H, I // 32), np.uint8)
+    for e in range(E):
+        mc, sb = [(2, 127), (3, 125), (4, 126)][e]
+        S13, w13_q[e], w13_s[e] = _pm_weight(rng, 2 * I, H, mc, sb)
+        S2, w2_q[e], w2_s[e] = _pm_weight(rng, H, I, [3, 2, 4][e], [129, 127, 124][e])
+        W13_list.append(S13 * E2M1[mc] * 2.0 ** (sb - 127))
+        W2_list.append(S2 * E2M1[[3, 2, 4][e]] * 2.0 ** ([129, 127, 124][e] - 127))
+    f = oracle.forward(x16, wr, w13_q, w13_s, w2_q, w2_s, k)
+    # independent routing
+    s = expit(bf16_vals(x16) @ bf16_vals(wr).T)
+    ids = np.argsort(-s, axis=1, kind="stable")[:, :k]
+    assert np.array_equal(f.route.ids, ids)
+    # Q1 exact: the decoded activations equal x
+    assert np.array_equal(oracle.act_dequant(f.aq, f.as_), x)
+    y = np.zeros((T, H))
+    for t in range(T):
+        sel = s[t, ids[t]]
+        for j, e in enumerate(ids[t]):
+            gu = x[t:t + 1] @ W13_list[e].T
+            g, u = gu[:, :I], gu[:, I:]
+            hval = g * expit(g) * u
+            q, sc, deq = _q2_brute(hval)
+            np.testing.assert_allclose(f.h[t, j], hval[0], rtol=1e-13, atol=1e-300)
+            assert np.array_equal(f.hq[t, j], q[0]) and np.array_equal(f.hs[t, j], sc[0])
+            y[t] += sel[j] / sel.sum() * (deq @ W2_list[e].T)[0]
+    np.testing.assert_allclose(f.y64, y, rtol=1e-12, atol=1e-9 * np.abs(y).max())
+    assert np.array_equal(f.y, oracle.f64_to_bf16(f.y64))
+
+
+def test_forward_token_subset_matches_full():
+    inp = synth.make_inputs("toy")
+    full = oracle.forward(inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, 8,
+                          logit_bias=inp.logit_bias, sel_bias=inp.sel_bias)
+    sub = oracle.forward(inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, 8,
+                         logit_bias=inp.logit_bias, sel_bias=inp.sel_bias, tokens=[5, 17, 63])
+    assert np.array_equal(sub.y, full.y[[5, 17, 63]])
+    assert np.array_equal(sub.perm, full.perm)
+
+
+def test_page_byte_accounting(golden):
+    """Expert sizes printed on the teardown page pin 3*H*I parameters per
+    expert and 4.25 bits per MXFP4 weight."""
+    g = {r[0]: float(r[1]) for r in golden("page_accounting.txt")}
+    I = int(g["intermediate"])
+    for hid, key in [("flash_hidden", "flash_expert_params_millions"), ("pro_hidden", "pro_expert_params_millions")]:
+        params = 3 * int(g[hid]) * I
+        assert round(params / 1e6, 1) == g[key]
+        assert synth.expert_weight_bytes(int(g[hid]), I) * 8 == params * g["bits_per_weight"]
+    assert round(g["flash_expert_weights_billions"] * 1e9 * g["bits_per_weight"] / 8 / 1e9, 1) == g["flash_expert_gb"]
+
+
+def test_generator_mxfp4_matches_oracle_quantiser():
+    w = synth.expert_f32(3, 7, 2, 32, 512, 0.02)
+    p, s = synth.mxfp4_experts(3, 7, 2, 32, 512, 0.02)
+    po, so = oracle.mxfp4_quant(w.reshape(-1, 512).astype(np.float64))
+    assert np.array_equal(po.reshape(p.shape), p) and np.array_equal(so.reshape(s.shape), s)
+
+
+def test_generator_is_deterministic_and_seeded():
+    a = synth.make_inputs("toy")
+    b = synth.make_inputs("toy")
+    assert np.array_equal(a.x, b.x) and np.array_equal(a.w13_q, b.w13_q) and np.array_equal(a.w2_s, b.w2_s)
+    x = bf16_vals(a.x)
+    assert abs(x.mean()) < 0.02 and abs(x.std() - 1) < 0.02
+    c = synth.make_inputs(synth.Config("s1", 64, 512, 16, 256, 8, 1, "none"))
+    assert not np.array_equal(a.x, c.x)
