@@ -1,0 +1,349 @@
+"""Benchmark of the routed MXFP4 / e4m3 MoE layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+One step = one forward of the whole layer (router, top-k, dispatch with
+activation quantisation, gate/up grouped GEMM with SwiGLU and
+re-quantisation, down grouped GEMM, combine) over one batch of T synthetic
+tokens already resident in HBM.  Prints one JSON line.  Default workload:
+the Flash-shaped decode layer (T=64, H=4096, E=256 top-8, I=2048).
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer on
+its own GPU (the layer does not shard on one box): a barrier and a max over
+ranks bracket the timed region, and ``value`` is the tokens of all ranks
+divided by that time.
+
+``--impl reference`` times the CPU oracle (fp64 restatement of the layer) on
+the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and % of roofline (HBM GB/s decode, tensor TFLOP/s prefill) on 1 B300"
+DEFAULT_CONFIG = "flash-decode"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def workload_desc(cfg):
+    return {"workload": cfg.name, "desc": cfg.desc, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "top_k": cfg.k,
+            "seed": cfg.seed, "routing_bias": cfg.bias, "score": "sigmoid" if cfg.score_func == 0 else "softmax"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ["mx_gemm.cu", "ptx.cuh", "moe_internal.cuh"]:
+        with open(os.path.join(ROOT, "fp8_mxfp4_expert_bf16_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Polls the SM clock and throttle reasons through NVML while running."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, index):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        self._mark = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception:
+            self.nv = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            if self._mark and self.nv is not None:
+                try:
+                    self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                    r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                    for bit, name in self.REASONS.items():
+                        if r & bit:
+                            self.reasons.add(name)
+                except Exception:
+                    pass
+            time.sleep(0.005)
+
+    def __enter__(self):
+        self.t = threading.Thread(target=self._run, daemon=True)
+        self.t.start()
+        return self
+
+    def mark(self, on):
+        self._mark = on
+
+    def __exit__(self, *a):
+        self._stop.set()
+        self.t.join()
+
+    def summary(self):
+        if self.nv is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_sample(inp, budget_s=12.0, max_tokens=None):
+    """Time the CPU oracle token by token on the workload (routing of the
+    whole batch included in every call) until the time budget is spent."""
+    import oracle
+    c = inp.cfg
+    rng = np.random.default_rng(12345)
+    order = rng.permutation(c.T)
+    t0 = time.perf_counter()
+    done = 0
+    for t in order:
+        oracle.forward(inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, c.k, c.score_func,
+                       inp.logit_bias, inp.sel_bias, tokens=[int(t)])
+        done += 1
+        if time.perf_counter() - t0 >= budget_s or (max_tokens and done >= max_tokens):
+            break
+    el = time.perf_counter() - t0
+    return done, el
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+    except Exception:
+        n = 1
+    return max(n, os.cpu_count() or 1)
+
+
+def run_reference(args, cfg):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    inp = synth.make_inputs(cfg)
+    tokens = 0
+    elapsed = 0.0
+    for _ in range(args.warmup):
+        oracle_sample(inp, budget_s=args.ref_budget / max(args.steps, 1), max_tokens=1)
+    per = []
+    for _ in range(args.steps):
+        n, el = oracle_sample(inp, budget_s=args.ref_budget / max(args.steps, 1))
+        tokens += n
+        elapsed += el
+        per.append(el)
+    value = tokens / elapsed
+    cores = cpu_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * elapsed / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_desc(cfg),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{tokens} tokens of the {cfg.name} batch, one oracle call per token "
+                                   f"(routing of all {cfg.T} tokens + that token's {cfg.k} expert FFNs, fp64)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, cfg):
+    import torch
+    import fp8_mxfp4_expert_bf16_b300 as moe
+
+    ws, rank, local = dist_env()
+    dist = ws > 1
+    if dist:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+    device = local
+    torch.cuda.set_device(device)
+    inp = synth.make_inputs(cfg)
+    c = cfg
+    layer = moe.MoELayer(c.H, c.I, c.E, c.k, c.T, c.score_func, device=device)
+    layer.load_weights(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
+    x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).to(f"cuda:{device}")
+    y = torch.empty_like(x)
+    stream = torch.cuda.Stream(device)
+    P = peaks()
+
+    def barrier():
+        torch.cuda.synchronize(device)
+        if dist:
+            tdist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            layer.forward(x, y, stream)
+    layer.check_device_error()
+
+    # routing statistics of this batch (for the algorithmic byte / flop counts)
+    counts, _ = layer.expert_counts()
+    active = int((counts > 0).sum())
+    rows = int(counts.sum())
+    ebytes13 = 2 * c.I * c.H // 2 + 2 * c.I * c.H // 32
+    ebytes2 = c.H * c.I // 2 + c.H * c.I // 32
+    g1_bytes = active * ebytes13
+    g2_bytes = active * ebytes2
+    g1_flops = 2.0 * rows * (2 * c.I) * c.H
+    g2_flops = 2.0 * rows * c.H * c.I
+    decode = c.T * c.k <= 4 * c.E   # few rows per expert: weight streaming binds
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    layer.set_profiling(True)
+    with ClockSampler(device) as clk:
+        barrier()
+        clk.mark(True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                layer.forward(x, y, stream)
+            ev1.record(stream)
+        barrier()
+        clk.mark(False)
+    ms_total = ev0.elapsed_time(ev1)
+    stage = layer.stage_times()       # averages over the last <= 64 timed forwards
+    layer.set_profiling(False)
+    launches = layer.launch_count() * args.steps
+    layer.check_device_error()
+
+    t_local = torch.tensor([ms_total], dtype=torch.float64, device=f"cuda:{device}")
+    if dist:
+        tdist.all_reduce(t_local, op=tdist.ReduceOp.MAX)
+    ms_max = float(t_local.item())
+    value = ws * c.T * args.steps / (ms_max / 1000.0)
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    xh = torch.from_numpy(inp.x.view(np.int16)).pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    for _ in range(3):
+        layer.forward_host(xh, yh, stream)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        layer.forward_host(xh, yh, stream)
+    el = time.perf_counter() - t0
+    t_e2e = torch.tensor([el], dtype=torch.float64, device=f"cuda:{device}")
+    if dist:
+        tdist.all_reduce(t_e2e, op=tdist.ReduceOp.MAX)
+    e2e_value = ws * c.T * args.steps / float(t_e2e.item())
+
+    g1_ms = stage["gemm1_gate_up"]
+    g2_ms = stage["gemm2_down"]
+    if decode:
+        ach = g1_bytes / (g1_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "k_mx_gemm<0> (gate/up grouped GEMM)", "achieved": ach,
+                "peak": P["hbm_gbs"], "unit": "GB/s", "frac": ach / P["hbm_gbs"],
+                "peak_source": f"{P['source']} HBM copy bandwidth",
+                "algorithmic_bytes_per_launch": g1_bytes,
+                "traffic": ncu_traffic(cfg.name, "gemm1"),
+                "down_gemm": {"achieved": g2_bytes / (g2_ms / 1e3) / 1e9, "bytes_per_launch": g2_bytes},
+                "layer_weight_gbs": (g1_bytes + g2_bytes) / (ms_max / args.steps / 1e3) / 1e9}
+    else:
+        pk = 2.0 * P["bf16_tflops"]
+        ach = g1_flops / (g1_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": "k_mx_gemm<0> (gate/up grouped GEMM)", "achieved": ach, "peak": pk,
+                "unit": "TFLOP/s", "frac": ach / pk,
+                "peak_source": f"{P['source']} bf16 burst x 2 (nominal fp8/bf16 ratio; block-scaled fp8 peak not measured)",
+                "algorithmic_flops_per_launch": g1_flops, "traffic": ncu_traffic(cfg.name, "gemm1"),
+                "down_gemm": {"achieved": g2_flops / (g2_ms / 1e3) / 1e12},
+                "layer_tflops": (g1_flops + g2_flops) / (ms_max / args.steps / 1e3) / 1e12}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n, el = oracle_sample(inp, budget_s=args.ref_budget)
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{n} tokens of the {cfg.name} batch, one oracle call per token "
+                         f"(routing of all {cfg.T} tokens + that token's {cfg.k} expert FFNs, fp64)"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e2m1 (fp32 accumulate)",
+            "data": "synthetic", "config": dict(workload_desc(cfg), parallelism=f"replicas{ws}",
+                                               l2="inputs larger than L2: every step streams the active experts' "
+                                                  "weights from HBM"),
+            "roofline": roof,
+            "stage_ms": stage,
+            "routing": {"active_experts": active, "rows": rows, "max_count": int(counts.max()),
+                        "min_count": int(counts.min())},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": c.T * c.H * 2,
+                    "d2h_bytes_per_step": c.T * c.H * 2},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        tdist.barrier()
+        tdist.destroy_process_group()
+    layer.close()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    cfg = synth.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_gpu(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

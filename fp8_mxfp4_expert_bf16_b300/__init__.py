@@ -1,0 +1,239 @@
+"""Routed MoE feed-forward layer with MXFP4 experts and e4m3 activations on B300.
+
+Thin Python binding over the C ABI of ``libmoe_mx.so`` (declared in
+``include/moe_mx.h``): argument marshalling only, every step of the layer
+runs in the library's CUDA kernels.  PyTorch supplies device memory and
+streams.  There is no CPU fallback: if the library is missing or cannot be
+loaded, importing the layer class raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+
+from .build import LIB as _LIB_PATH, build as _build
+
+__all__ = ["MoELayer", "MoEError", "lib", "declared_symbols", "STAGES"]
+
+_HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_mx.h")
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_CUDA", 4: "MOE_ERR_OOM",
+          5: "MOE_ERR_NOT_LOADED", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_UNSUPPORTED", 8: "MOE_ERR_DEVICE"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("num_experts", ctypes.c_int),
+                ("top_k", ctypes.c_int), ("max_tokens", ctypes.c_int), ("score_func", ctypes.c_int),
+                ("device", ctypes.c_int)]
+
+
+_lib = None
+
+
+def declared_symbols() -> list[str]:
+    """Every function the C header declares."""
+    with open(_HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:moe_status|int|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
+
+
+def lib(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libmoe_mx.so (building it first if asked and needed)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build() if build_if_missing else _LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"libmoe_mx.so not built ({path}); run python -m fp8_mxfp4_expert_bf16_b300.build")
+    L = ctypes.CDLL(path)
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
+    sig = {
+        "moe_init": (S, [ctypes.POINTER(_Config), ctypes.POINTER(P)]),
+        "moe_destroy": (S, [P]),
+        "moe_load_weights": (S, [P, P, P, P, P, P, P, P]),
+        "moe_forward": (S, [P, P, I, P, P]),
+        "moe_forward_host": (S, [P, P, I, P, P]),
+        "moe_get_logits": (S, [P, P]),
+        "moe_get_routing": (S, [P, P, P]),
+        "moe_get_expert_counts": (S, [P, P, P]),
+        "moe_get_permutation": (S, [P, P]),
+        "moe_get_act_quant": (S, [P, P, P]),
+        "moe_get_inter_quant": (S, [P, P, P]),
+        "moe_get_expert_out": (S, [P, P]),
+        "moe_set_profiling": (S, [P, I]),
+        "moe_get_stage_times": (S, [P, P, I]),
+        "moe_stage_count": (I, []),
+        "moe_stage_name": (ctypes.c_char_p, [I]),
+        "moe_check_device_error": (S, [P]),
+        "moe_last_launch_count": (I, [P]),
+        "moe_last_error": (ctypes.c_char_p, [P]),
+        "moe_status_string": (ctypes.c_char_p, [I]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def _stages():
+    L = lib()
+    return [L.moe_stage_name(i).decode() for i in range(L.moe_stage_count())]
+
+
+STAGES = None
+
+
+def _ptr(a) -> int | None:
+    """Address of a numpy array or a torch tensor (host or device); None -> NULL."""
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        assert a.flags["C_CONTIGUOUS"], "arrays must be C-contiguous"
+        return a.ctypes.data
+    assert a.is_contiguous(), "tensors must be contiguous"
+    return a.data_ptr()
+
+
+class MoELayer:
+    """One routed MoE layer on one GPU.
+
+    Shapes: H hidden, I expert middle width, E experts, k top-k.  Weights in
+    the packed MXFP4 layout of ``moe_load_weights`` (see the C header).
+    """
+
+    def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, max_tokens: int,
+                 score_func: int = 0, device: int = 0):
+        import torch  # noqa: F401  (device memory and streams)
+        self.L = lib()
+        self.H, self.I, self.E, self.k, self.max_tokens = hidden, inter, num_experts, top_k, max_tokens
+        self.device = device
+        cfg = _Config(hidden, inter, num_experts, top_k, max_tokens, score_func, device)
+        h = ctypes.c_void_p()
+        st = self.L.moe_init(ctypes.byref(cfg), ctypes.byref(h))
+        if st != 0:
+            raise MoEError(st, self.L.moe_last_error(None).decode())
+        self.h = h
+        self.last_T = None
+
+    # ------------------------------------------------------------ plumbing
+    def _check(self, st: int):
+        if st != 0:
+            raise MoEError(st, self.L.moe_last_error(self.h).decode())
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.L.moe_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _stream(stream):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+    # ------------------------------------------------------------ API
+    def load_weights(self, router_w, logit_bias, sel_bias, w13_q, w13_s, w2_q, w2_s):
+        """Copy the weights (numpy arrays or torch tensors, host or device)."""
+        H, I, E = self.H, self.I, self.E
+        for a, shape in [(router_w, (E, H)), (w13_q, (E, 2 * I, H // 2)), (w13_s, (E, 2 * I, H // 32)),
+                         (w2_q, (E, H, I // 2)), (w2_s, (E, H, I // 32))]:
+            assert tuple(a.shape) == shape, (tuple(a.shape), shape)
+        for b in (logit_bias, sel_bias):
+            assert b is None or tuple(b.shape) == (E,)
+        self._check(self.L.moe_load_weights(self.h, _ptr(router_w), _ptr(logit_bias), _ptr(sel_bias),
+                                            _ptr(w13_q), _ptr(w13_s), _ptr(w2_q), _ptr(w2_s)))
+
+    def forward(self, x, y=None, stream=None):
+        """x: cuda bf16 [T, H] -> y: cuda bf16 [T, H] (enqueued on the stream, no sync)."""
+        import torch
+        assert x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.shape[1] == self.H
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty_like(x)
+        self._check(self.L.moe_forward(self.h, _ptr(x), T, _ptr(y), self._stream(stream)))
+        self.last_T = T
+        return y
+
+    def forward_host(self, x_host, y_host=None, stream=None):
+        """Host bf16 bits (numpy uint16 or a CPU tensor) in and out; copies and
+        synchronisation happen inside the library call."""
+        T = x_host.shape[0]
+        if y_host is None:
+            y_host = np.empty((T, self.H), dtype=np.uint16)
+        self._check(self.L.moe_forward_host(self.h, _ptr(x_host), T, _ptr(y_host), self._stream(stream)))
+        self.last_T = T
+        return y_host
+
+    def set_profiling(self, on: bool = True):
+        self._check(self.L.moe_set_profiling(self.h, int(on)))
+
+    def stage_times(self) -> dict:
+        n = self.L.moe_stage_count()
+        ms = np.zeros(n, dtype=np.float32)
+        self._check(self.L.moe_get_stage_times(self.h, _ptr(ms), n))
+        return {self.L.moe_stage_name(i).decode(): float(ms[i]) for i in range(n)}
+
+    def check_device_error(self):
+        self._check(self.L.moe_check_device_error(self.h))
+
+    def launch_count(self) -> int:
+        return self.L.moe_last_launch_count(self.h)
+
+    # ------------------------------------------------------------ getters
+    def logits(self):
+        out = np.empty((self.last_T, self.E), dtype=np.float32)
+        self._check(self.L.moe_get_logits(self.h, _ptr(out)))
+        return out
+
+    def routing(self):
+        ids = np.empty((self.last_T, self.k), dtype=np.int32)
+        gates = np.empty((self.last_T, self.k), dtype=np.float32)
+        self._check(self.L.moe_get_routing(self.h, _ptr(ids), _ptr(gates)))
+        return ids, gates
+
+    def expert_counts(self):
+        counts = np.empty(self.E, dtype=np.int32)
+        offsets = np.empty(self.E + 1, dtype=np.int32)
+        self._check(self.L.moe_get_expert_counts(self.h, _ptr(counts), _ptr(offsets)))
+        return counts, offsets
+
+    def permutation(self):
+        perm = np.empty(self.last_T * self.k, dtype=np.int32)
+        self._check(self.L.moe_get_permutation(self.h, _ptr(perm)))
+        return perm
+
+    def act_quant(self):
+        q = np.empty((self.last_T, self.H), dtype=np.uint8)
+        s = np.empty((self.last_T, self.H // 128), dtype=np.uint8)
+        self._check(self.L.moe_get_act_quant(self.h, _ptr(q), _ptr(s)))
+        return q, s
+
+    def inter_quant(self):
+        n = self.last_T * self.k
+        q = np.empty((n, self.I), dtype=np.uint8)
+        s = np.empty((n, self.I // 128), dtype=np.uint8)
+        self._check(self.L.moe_get_inter_quant(self.h, _ptr(q), _ptr(s)))
+        return q, s
+
+    def expert_out(self):
+        out = np.empty((self.last_T * self.k, self.H), dtype=np.float32)
+        self._check(self.L.moe_get_expert_out(self.h, _ptr(out)))
+        return out

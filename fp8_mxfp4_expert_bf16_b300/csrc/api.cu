@@ -1,0 +1,524 @@
+// C ABI of the routed MXFP4 MoE layer: argument checks, device workspace,
+// TMA tensor maps, weight loading, the stream-ordered forward and the debug
+// getters.  See include/moe_mx.h for the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/moe_mx.h"
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+static const char* kStageNames[] = {"router", "topk", "dispatch", "gemm1_gate_up", "gemm2_down", "combine"};
+constexpr int kNumStages = 6;
+constexpr int kProfSlots = 64;   // forwards whose stage events are kept
+
+struct moe_handle {
+    moe_config cfg{};
+    DevState s{};
+    bool loaded = false;
+    int last_T = -1;
+    int last_launches = 0;
+    bool profiling = false;
+    cudaEvent_t ev[kProfSlots][kNumStages + 1] = {};
+    bool ev_valid = false;
+    int prof_count = 0;      // forwards recorded since profiling was enabled / last read
+    std::vector<void*> allocs;
+    uint16_t* xbuf = nullptr;   // staging for moe_forward_host
+    uint16_t* ybuf = nullptr;
+    // owned weight buffers
+    void* w_alloc[7] = {};
+    std::string err;
+};
+
+static thread_local std::string g_err;
+
+static moe_status fail(moe_handle* h, moe_status st, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (h) h->err = buf;
+    else g_err = buf;
+    return st;
+}
+
+#define CUDA_TRY(h, call)                                                                            \
+    do {                                                                                             \
+        cudaError_t e_ = (call);                                                                     \
+        if (e_ != cudaSuccess)                                                                       \
+            return fail((h), e_ == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA, "%s: %s (%s:%d)", \
+                        #call, cudaGetErrorString(e_), __FILE__, __LINE__);                          \
+    } while (0)
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D tensor map over a row-major [rows][inner] tensor.
+static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t rows,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows)
+{
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(m, dt, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename T>
+static moe_status dalloc(moe_handle* h, T** p, size_t bytes)
+{
+    void* q = nullptr;
+    cudaError_t e = cudaMalloc(&q, bytes < 256 ? 256 : bytes);
+    if (e != cudaSuccess)
+        return fail(h, MOE_ERR_OOM, "cudaMalloc(%zu bytes): %s", bytes, cudaGetErrorString(e));
+    h->allocs.push_back(q);
+    *p = static_cast<T*>(q);
+    return MOE_OK;
+}
+
+static moe_status getter_prologue(moe_handle* h)
+{
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "handle is NULL");
+    if (h->last_T < 0) return fail(h, MOE_ERR_NOT_LOADED, "no forward has run since the weights were loaded");
+    return moe_check_device_error(h);
+}
+
+template <typename Fn>
+static moe_status with_tmp(moe_handle* h, size_t bytes, void* host_out, Fn&& fill)
+{
+    if (!host_out || bytes == 0) return MOE_OK;
+    void* d = nullptr;
+    CUDA_TRY(h, cudaMalloc(&d, bytes));
+    cudaError_t e = fill(d);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(host_out, d, bytes, cudaMemcpyDeviceToHost);
+    cudaFree(d);
+    if (e != cudaSuccess) return fail(h, MOE_ERR_CUDA, "getter: %s", cudaGetErrorString(e));
+    return MOE_OK;
+}
+
+
+extern "C" {
+
+const char* moe_status_string(moe_status s)
+{
+    switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_SHAPE: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_OOM: return "out of device memory";
+    case MOE_ERR_NOT_LOADED: return "weights not loaded / no forward yet";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_UNSUPPORTED: return "unsupported device";
+    case MOE_ERR_DEVICE: return "device-side error";
+    }
+    return "unknown status";
+}
+
+const char* moe_last_error(moe_handle* h) { return h ? h->err.c_str() : g_err.c_str(); }
+
+int moe_stage_count(void) { return kNumStages; }
+const char* moe_stage_name(int i) { return (i >= 0 && i < kNumStages) ? kStageNames[i] : ""; }
+
+moe_status moe_destroy(moe_handle* h)
+{
+    if (!h) return MOE_OK;
+    cudaSetDevice(h->cfg.device);
+    for (void* p : h->allocs) cudaFree(p);
+    for (void* p : h->w_alloc)
+        if (p) cudaFree(p);
+    if (h->ev_valid)
+        for (auto& slot : h->ev)
+            for (auto& e : slot) cudaEventDestroy(e);
+    delete h;
+    return MOE_OK;
+}
+
+moe_status moe_init(const moe_config* cfg, moe_handle** out)
+{
+    if (!out) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_init: out is NULL");
+    *out = nullptr;
+    if (!cfg) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_init: cfg is NULL");
+    const moe_config c = *cfg;
+    if (c.hidden < 128 || c.hidden > 16384 || c.hidden % 128)
+        return fail(nullptr, MOE_ERR_SHAPE, "hidden=%d: must be a multiple of 128 in [128, 16384]", c.hidden);
+    if (c.inter < 128 || c.inter > 16384 || c.inter % 128)
+        return fail(nullptr, MOE_ERR_SHAPE, "inter=%d: must be a multiple of 128 in [128, 16384]", c.inter);
+    if (c.num_experts < 1 || c.num_experts > kMaxExperts)
+        return fail(nullptr, MOE_ERR_SHAPE, "num_experts=%d: must be in [1, %d]", c.num_experts, kMaxExperts);
+    if (c.top_k < 1 || c.top_k > kMaxTopK || c.top_k > c.num_experts)
+        return fail(nullptr, MOE_ERR_SHAPE, "top_k=%d: must be in [1, min(E, 8)]", c.top_k);
+    if (c.max_tokens < 1 || c.max_tokens > (1 << 20))
+        return fail(nullptr, MOE_ERR_SHAPE, "max_tokens=%d: must be in [1, 2^20]", c.max_tokens);
+    if (c.score_func != MOE_SCORE_SIGMOID && c.score_func != MOE_SCORE_SOFTMAX)
+        return fail(nullptr, MOE_ERR_INVALID_ARG, "score_func=%d", c.score_func);
+    if (cudaSetDevice(c.device) != cudaSuccess)
+        return fail(nullptr, MOE_ERR_CUDA, "cudaSetDevice(%d) failed", c.device);
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, c.device) != cudaSuccess)
+        return fail(nullptr, MOE_ERR_CUDA, "cudaGetDeviceProperties failed");
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(nullptr, MOE_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                    c.device, prop.major, prop.minor);
+    if (!get_encode()) return fail(nullptr, MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+
+    moe_handle* h = new moe_handle;
+    h->cfg = c;
+    DevState& s = h->s;
+    s.H = c.hidden;
+    s.I = c.inter;
+    s.E = c.num_experts;
+    s.K = c.top_k;
+    s.Tm = c.max_tokens;
+    s.score_func = c.score_func;
+    s.KB1 = s.H / 128;
+    s.KB2 = s.I / 128;
+    s.NT1 = s.I / 128;
+    s.BN2 = (s.H % 256 == 0) ? 256 : 128;
+    s.NT2 = s.H / s.BN2;
+    s.MTmax = (s.Tm * s.K + kBM - 1) / kBM + s.E;
+    s.Rmax = s.MTmax * kBM;
+    s.nchunk_max = (s.Tm + kChunk - 1) / kChunk;
+    s.num_sms = prop.multiProcessorCount;
+
+    moe_status st;
+#define ALLOC(ptr, bytes)                                      \
+    if ((st = dalloc(h, &(ptr), (bytes))) != MOE_OK) {         \
+        std::string m = h->err;                                \
+        moe_destroy(h);                                        \
+        return fail(nullptr, st, "%s", m.c_str());             \
+    }
+    ALLOC(s.logits, sizeof(float) * s.Tm * s.E);
+    ALLOC(s.ids, sizeof(int32_t) * s.Tm * s.K);
+    ALLOC(s.gates, sizeof(float) * s.Tm * s.K);
+    ALLOC(s.chunk_hist, sizeof(int32_t) * s.nchunk_max * s.E);
+    ALLOC(s.chunk_base, sizeof(int32_t) * s.nchunk_max * s.E);
+    ALLOC(s.counts, sizeof(int32_t) * s.E);
+    ALLOC(s.offsets, sizeof(int32_t) * (s.E + 1));
+    ALLOC(s.mtile_off, sizeof(int32_t) * (s.E + 1));
+    ALLOC(s.mtile_expert, sizeof(int32_t) * s.MTmax);
+    ALLOC(s.mtile_rows, sizeof(int32_t) * s.MTmax);
+    ALLOC(s.n_mtiles, sizeof(int32_t) * 4);
+    ALLOC(s.prow, sizeof(int32_t) * s.Tm * s.K);
+    ALLOC(s.aq, (size_t)s.Rmax * s.H);
+    ALLOC(s.asf, sizeof(uint32_t) * (size_t)s.MTmax * s.KB1 * 128);
+    ALLOC(s.hq, (size_t)s.Rmax * s.I);
+    ALLOC(s.hsf, sizeof(uint32_t) * (size_t)s.MTmax * s.KB2 * 128);
+    ALLOC(s.obuf, sizeof(float) * (size_t)s.Rmax * s.H);
+    ALLOC(s.err, sizeof(int32_t) * 4);
+    ALLOC(h->xbuf, sizeof(uint16_t) * (size_t)s.Tm * s.H);
+    ALLOC(h->ybuf, sizeof(uint16_t) * (size_t)s.Tm * s.H);
+#undef ALLOC
+    // padding rows of the activation / SwiGLU buffers are never written by a
+    // forward; zero them once so every tile reads finite values
+    bool ok = cudaMemset(s.aq, 0, (size_t)s.Rmax * s.H) == cudaSuccess &&
+              cudaMemset(s.asf, 0, sizeof(uint32_t) * (size_t)s.MTmax * s.KB1 * 128) == cudaSuccess &&
+              cudaMemset(s.hq, 0, (size_t)s.Rmax * s.I) == cudaSuccess &&
+              cudaMemset(s.hsf, 0, sizeof(uint32_t) * (size_t)s.MTmax * s.KB2 * 128) == cudaSuccess &&
+              cudaMemset(s.err, 0, sizeof(int32_t) * 4) == cudaSuccess &&
+              cudaMemset(s.n_mtiles, 0, sizeof(int32_t) * 4) == cudaSuccess;
+    const uint32_t boxes[kNumABox] = {32, 64, 128};
+    for (int i = 0; ok && i < kNumABox; ++i) {
+        ok = make_map(&s.tm_aq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.aq, s.H, s.Rmax, s.H, 128, boxes[i]) &&
+             make_map(&s.tm_hq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, s.I, s.Rmax, s.I, 128, boxes[i]);
+    }
+    if (ok) ok = gemm_set_attributes() == cudaSuccess;
+    if (ok) ok = cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) {
+        moe_destroy(h);
+        return fail(nullptr, MOE_ERR_CUDA, "moe_init: workspace setup failed: %s",
+                    cudaGetErrorString(cudaGetLastError()));
+    }
+    *out = h;
+    return MOE_OK;
+}
+
+moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float* logit_bias, const float* sel_bias,
+                            const uint8_t* w13_q, const uint8_t* w13_s, const uint8_t* w2_q, const uint8_t* w2_s)
+{
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_load_weights: handle is NULL");
+    if (!router_w || !w13_q || !w13_s || !w2_q || !w2_s)
+        return fail(h, MOE_ERR_INVALID_ARG, "moe_load_weights: a required weight pointer is NULL");
+    DevState& s = h->s;
+    CUDA_TRY(h, cudaSetDevice(h->cfg.device));
+    h->loaded = false;
+    for (void*& p : h->w_alloc)
+        if (p) {
+            cudaFree(p);
+            p = nullptr;
+        }
+    const size_t E = s.E, H = s.H, I = s.I;
+    const size_t n_wr = E * H * 2, n_13q = E * 2 * I * H / 2, n_13s = E * 2 * I * H / 32, n_2q = E * H * I / 2,
+                 n_2s = E * H * I / 32;
+    void *d_wr, *d_b, *d_13q, *d_2q, *d_sf13, *d_sf2, *d_tmp;
+    CUDA_TRY(h, cudaMalloc(&d_wr, n_wr));
+    h->w_alloc[0] = d_wr;
+    CUDA_TRY(h, cudaMalloc(&d_b, 2 * E * sizeof(float)));
+    h->w_alloc[1] = d_b;
+    CUDA_TRY(h, cudaMalloc(&d_13q, n_13q));
+    h->w_alloc[2] = d_13q;
+    CUDA_TRY(h, cudaMalloc(&d_2q, n_2q));
+    h->w_alloc[3] = d_2q;
+    CUDA_TRY(h, cudaMalloc(&d_sf13, n_13s));
+    h->w_alloc[4] = d_sf13;
+    CUDA_TRY(h, cudaMalloc(&d_sf2, n_2s));
+    h->w_alloc[5] = d_sf2;
+    CUDA_TRY(h, cudaMalloc(&d_tmp, (n_13s > n_2s ? n_13s : n_2s) + 256));
+    h->w_alloc[6] = d_tmp;
+    float* d_lb = static_cast<float*>(d_b);
+    float* d_cb = d_lb + E;
+    CUDA_TRY(h, cudaMemcpy(d_wr, router_w, n_wr, cudaMemcpyDefault));
+    CUDA_TRY(h, cudaMemset(d_b, 0, 2 * E * sizeof(float)));
+    if (logit_bias) CUDA_TRY(h, cudaMemcpy(d_lb, logit_bias, E * sizeof(float), cudaMemcpyDefault));
+    if (sel_bias) CUDA_TRY(h, cudaMemcpy(d_cb, sel_bias, E * sizeof(float), cudaMemcpyDefault));
+    CUDA_TRY(h, cudaMemcpy(d_13q, w13_q, n_13q, cudaMemcpyDefault));
+    CUDA_TRY(h, cudaMemcpy(d_2q, w2_q, n_2q, cudaMemcpyDefault));
+
+    int32_t* flag = s.err + 3;
+    CUDA_TRY(h, cudaMemset(flag, 0, sizeof(int32_t)));
+    // w13 scales: [E][2I][H/32] -> chunks [E][H/128][I/128][gate, up][512 B]
+    CUDA_TRY(h, cudaMemcpy(d_tmp, w13_s, n_13s, cudaMemcpyDefault));
+    CUDA_TRY(h, launch_check_e8m0(static_cast<uint8_t*>(d_tmp), n_13s, flag, 0));
+    CUDA_TRY(h, launch_repack_sf(static_cast<uint8_t*>(d_tmp), static_cast<uint8_t*>(d_sf13), s.E, s.KB1, s.NT1, 2,
+                                 2 * s.I, s.H / 32, 0, s.I / 128, 0));
+    CUDA_TRY(h, cudaDeviceSynchronize());
+    // w2 scales: [E][H][I/32] -> chunks [E][I/128][H/BN2][BN2/128][512 B]
+    CUDA_TRY(h, cudaMemcpy(d_tmp, w2_s, n_2s, cudaMemcpyDefault));
+    CUDA_TRY(h, launch_check_e8m0(static_cast<uint8_t*>(d_tmp), n_2s, flag, 0));
+    CUDA_TRY(h, launch_repack_sf(static_cast<uint8_t*>(d_tmp), static_cast<uint8_t*>(d_sf2), s.E, s.KB2, s.NT2,
+                                 s.BN2 / 128, s.H, s.I / 32, 1, s.I / 128, 0));
+    CUDA_TRY(h, cudaDeviceSynchronize());
+    int32_t nan_found = 0;
+    CUDA_TRY(h, cudaMemcpy(&nan_found, flag, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    cudaFree(d_tmp);
+    h->w_alloc[6] = nullptr;
+    if (nan_found) {
+        CUDA_TRY(h, cudaMemset(flag, 0, sizeof(int32_t)));
+        return fail(h, MOE_ERR_INVALID_ARG, "moe_load_weights: an expert scale byte is 0xFF (E8M0 NaN)");
+    }
+    if (!make_map(&s.tm_w13, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, d_13q, H, E * 2 * I, H / 2, 128, 128) ||
+        !make_map(&s.tm_w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, d_2q, I, E * H, I / 2, 128, 128))
+        return fail(h, MOE_ERR_CUDA, "moe_load_weights: cuTensorMapEncodeTiled failed for the expert weights");
+    s.wr = static_cast<const uint16_t*>(d_wr);
+    s.lb = d_lb;
+    s.cb = d_cb;
+    s.w13q = static_cast<const uint8_t*>(d_13q);
+    s.w2q = static_cast<const uint8_t*>(d_2q);
+    s.sfb13 = static_cast<const uint8_t*>(d_sf13);
+    s.sfb2 = static_cast<const uint8_t*>(d_sf2);
+    h->loaded = true;
+    h->last_T = -1;
+    return MOE_OK;
+}
+
+moe_status moe_set_profiling(moe_handle* h, int enable)
+{
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "handle is NULL");
+    CUDA_TRY(h, cudaSetDevice(h->cfg.device));
+    if (enable && !h->ev_valid) {
+        for (auto& slot : h->ev)
+            for (auto& e : slot) CUDA_TRY(h, cudaEventCreate(&e));
+        h->ev_valid = true;
+    }
+    h->profiling = enable != 0;
+    h->prof_count = 0;
+    return MOE_OK;
+}
+
+moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, void* stream)
+{
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_forward: handle is NULL");
+    if (!h->loaded) return fail(h, MOE_ERR_NOT_LOADED, "moe_forward: weights not loaded");
+    if (T < 0 || T > h->s.Tm)
+        return fail(h, MOE_ERR_SHAPE, "moe_forward: T=%d outside [0, max_tokens=%d]", T, h->s.Tm);
+    if (T == 0) return MOE_OK;
+    if (!x || !y) return fail(h, MOE_ERR_INVALID_ARG, "moe_forward: x or y is NULL");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u)
+        return fail(h, MOE_ERR_INVALID_ARG, "moe_forward: x and y must be 16-byte aligned");
+    const size_t bytes = (size_t)T * h->s.H * 2;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
+    if (xa < ya + bytes && ya < xa + bytes) return fail(h, MOE_ERR_INVALID_ARG, "moe_forward: x and y overlap");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const DevState& s = h->s;
+    CUDA_TRY(h, cudaSetDevice(h->cfg.device));
+    const bool prof = h->profiling && h->ev_valid;
+    cudaEvent_t* ev = h->ev[h->prof_count % kProfSlots];
+    int n = 0;
+    if (prof) CUDA_TRY(h, cudaEventRecord(ev[0], st));
+    CUDA_TRY(h, launch_router(s, x, T, st));
+    ++n;
+    if (prof) CUDA_TRY(h, cudaEventRecord(ev[1], st));
+    CUDA_TRY(h, launch_topk(s, T, st));
+    ++n;
+    if (prof) CUDA_TRY(h, cudaEventRecord(ev[2], st));
+    CUDA_TRY(h, launch_dispatch(s, x, T, st, &n));
+    if (prof) CUDA_TRY(h, cudaEventRecord(ev[3], st));
+    CUDA_TRY(h, launch_gemm1(s, st));
+    ++n;
+    if (prof) CUDA_TRY(h, cudaEventRecord(ev[4], st));
+    CUDA_TRY(h, launch_gemm2(s, st));
+    ++n;
+    if (prof) CUDA_TRY(h, cudaEventRecord(ev[5], st));
+    CUDA_TRY(h, launch_combine(s, y, T, st));
+    ++n;
+    if (prof) CUDA_TRY(h, cudaEventRecord(ev[6], st));
+    h->last_T = T;
+    h->last_launches = n;
+    if (prof) ++h->prof_count;
+    return MOE_OK;
+}
+
+moe_status moe_forward_host(moe_handle* h, const uint16_t* x_host, int T, uint16_t* y_host, void* stream)
+{
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_forward_host: handle is NULL");
+    if (!h->loaded) return fail(h, MOE_ERR_NOT_LOADED, "moe_forward_host: weights not loaded");
+    if (T < 0 || T > h->s.Tm)
+        return fail(h, MOE_ERR_SHAPE, "moe_forward_host: T=%d outside [0, max_tokens=%d]", T, h->s.Tm);
+    if (T == 0) return MOE_OK;
+    if (!x_host || !y_host) return fail(h, MOE_ERR_INVALID_ARG, "moe_forward_host: x or y is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t bytes = (size_t)T * h->s.H * 2;
+    CUDA_TRY(h, cudaSetDevice(h->cfg.device));
+    CUDA_TRY(h, cudaMemcpyAsync(h->xbuf, x_host, bytes, cudaMemcpyHostToDevice, st));
+    moe_status r = moe_forward(h, h->xbuf, T, h->ybuf, stream);
+    if (r != MOE_OK) return r;
+    CUDA_TRY(h, cudaMemcpyAsync(y_host, h->ybuf, bytes, cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(h, cudaStreamSynchronize(st));
+    return MOE_OK;
+}
+
+int moe_last_launch_count(moe_handle* h) { return h ? h->last_launches : 0; }
+
+moe_status moe_check_device_error(moe_handle* h)
+{
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "handle is NULL");
+    CUDA_TRY(h, cudaSetDevice(h->cfg.device));
+    CUDA_TRY(h, cudaDeviceSynchronize());
+    int32_t w[3] = {0, 0, 0};
+    CUDA_TRY(h, cudaMemcpy(w, h->s.err, sizeof w, cudaMemcpyDeviceToHost));
+    if (w[0] == 0) return MOE_OK;
+    CUDA_TRY(h, cudaMemset(h->s.err, 0, 3 * sizeof(int32_t)));
+    if (w[0] == kDevErrTimeout)
+        return fail(h, MOE_ERR_TIMEOUT, "a kernel wait timed out (site %d, block %d)", w[1], w[2]);
+    return fail(h, MOE_ERR_DEVICE, "device error code %d (site %d)", w[0], w[1]);
+}
+
+moe_status moe_get_logits(moe_handle* h, float* logits)
+{
+    moe_status r = getter_prologue(h);
+    if (r != MOE_OK) return r;
+    if (logits)
+        CUDA_TRY(h, cudaMemcpy(logits, h->s.logits, sizeof(float) * h->last_T * h->s.E, cudaMemcpyDeviceToHost));
+    return MOE_OK;
+}
+
+moe_status moe_get_routing(moe_handle* h, int32_t* ids, float* gates)
+{
+    moe_status r = getter_prologue(h);
+    if (r != MOE_OK) return r;
+    const size_t n = (size_t)h->last_T * h->s.K;
+    if (ids) CUDA_TRY(h, cudaMemcpy(ids, h->s.ids, sizeof(int32_t) * n, cudaMemcpyDeviceToHost));
+    if (gates) CUDA_TRY(h, cudaMemcpy(gates, h->s.gates, sizeof(float) * n, cudaMemcpyDeviceToHost));
+    return MOE_OK;
+}
+
+moe_status moe_get_expert_counts(moe_handle* h, int32_t* counts, int32_t* offsets)
+{
+    moe_status r = getter_prologue(h);
+    if (r != MOE_OK) return r;
+    if (counts) CUDA_TRY(h, cudaMemcpy(counts, h->s.counts, sizeof(int32_t) * h->s.E, cudaMemcpyDeviceToHost));
+    if (offsets)
+        CUDA_TRY(h, cudaMemcpy(offsets, h->s.offsets, sizeof(int32_t) * (h->s.E + 1), cudaMemcpyDeviceToHost));
+    return MOE_OK;
+}
+
+moe_status moe_get_permutation(moe_handle* h, int32_t* perm)
+{
+    moe_status r = getter_prologue(h);
+    if (r != MOE_OK) return r;
+    const int T = h->last_T;
+    return with_tmp(h, sizeof(int32_t) * T * h->s.K, perm,
+                    [&](void* d) { return launch_unpad_perm(h->s, T, static_cast<int32_t*>(d), 0); });
+}
+
+static moe_status get_quant(moe_handle* h, int which, uint8_t* q, uint8_t* sc)
+{
+    moe_status r = getter_prologue(h);
+    if (r != MOE_OK) return r;
+    const int T = h->last_T;
+    const size_t rows = which == 0 ? (size_t)T : (size_t)T * h->s.K;
+    const size_t width = which == 0 ? h->s.H : h->s.I;
+    const size_t qb = rows * width, sb = rows * (width / 128);
+    uint8_t *dq = nullptr, *ds = nullptr;
+    CUDA_TRY(h, cudaMalloc(&dq, qb + sb + 256));
+    ds = dq + qb;
+    cudaError_t e = launch_gather_rows_u8(h->s, T, which, dq, ds, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess && q) e = cudaMemcpy(q, dq, qb, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && sc) e = cudaMemcpy(sc, ds, sb, cudaMemcpyDeviceToHost);
+    cudaFree(dq);
+    if (e != cudaSuccess) return fail(h, MOE_ERR_CUDA, "getter: %s", cudaGetErrorString(e));
+    return MOE_OK;
+}
+
+moe_status moe_get_act_quant(moe_handle* h, uint8_t* q, uint8_t* scale) { return get_quant(h, 0, q, scale); }
+moe_status moe_get_inter_quant(moe_handle* h, uint8_t* q, uint8_t* scale) { return get_quant(h, 1, q, scale); }
+
+moe_status moe_get_expert_out(moe_handle* h, float* out)
+{
+    moe_status r = getter_prologue(h);
+    if (r != MOE_OK) return r;
+    const int T = h->last_T;
+    return with_tmp(h, sizeof(float) * (size_t)T * h->s.K * h->s.H, out,
+                    [&](void* d) { return launch_gather_obuf(h->s, T, static_cast<float*>(d), 0); });
+}
+
+moe_status moe_get_stage_times(moe_handle* h, float* ms, int n)
+{
+    if (!h || !ms) return fail(h, MOE_ERR_INVALID_ARG, "moe_get_stage_times: NULL argument");
+    if (!h->profiling || !h->ev_valid || h->prof_count == 0)
+        return fail(h, MOE_ERR_NOT_LOADED, "moe_get_stage_times: profiling off or no forward recorded");
+    const int cnt = h->prof_count < kProfSlots ? h->prof_count : kProfSlots;
+    const int last = (h->prof_count - 1) % kProfSlots;
+    CUDA_TRY(h, cudaEventSynchronize(h->ev[last][kNumStages]));
+    for (int i = 0; i < n && i < kNumStages; ++i) {
+        double sum = 0.0;
+        for (int k = 0; k < cnt; ++k) {
+            const int slot = (h->prof_count - 1 - k) % kProfSlots;
+            float t = 0.f;
+            CUDA_TRY(h, cudaEventElapsedTime(&t, h->ev[slot][i], h->ev[slot][i + 1]));
+            sum += t;
+        }
+        ms[i] = (float)(sum / cnt);
+    }
+    h->prof_count = 0;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// Internal state shared by the host orchestration and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr int kBM = 128;            // rows per grouped-GEMM tile (tokens of one expert)
+constexpr int kBK = 128;            // K elements per pipeline stage
+constexpr int kChunk = 256;         // tokens per dispatch chunk
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 8;
+constexpr int kNumABox = 3;         // activation tile maps with 32 / 64 / 128 rows
+
+// Error word codes written by kernels (first writer wins).
+constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrBounds = 2;
+
+struct DevState {
+    int H, I, E, K, Tm, score_func;
+    int KB1, KB2;        // H/128, I/128: K-blocks of the two grouped GEMMs
+    int NT1, NT2, BN2;   // n-tiles: G1 (I/128, 256 columns = gate 128 + up 128), G2 (H/BN2)
+    int MTmax;           // max 128-row m-tiles: ceil(Tm*K/128) + E
+    int Rmax;            // MTmax * 128 padded rows
+    int nchunk_max;      // ceil(Tm / kChunk)
+
+    // weights (owned)
+    const uint16_t* wr = nullptr;   // [E][H] bf16
+    const float* lb = nullptr;      // [E]
+    const float* cb = nullptr;      // [E]
+    const uint8_t* w13q = nullptr;  // [E][2I][H/2]
+    const uint8_t* w2q = nullptr;   // [E][H][I/2]
+    const uint8_t* sfb13 = nullptr; // [E][KB1][NT1][2][512]  scale chunks in tcgen05.cp order
+    const uint8_t* sfb2 = nullptr;  // [E][KB2][NT2][BN2/128][512]
+
+    // workspace
+    float* logits;        // [Tm][E]
+    int32_t* ids;         // [Tm][K]
+    float* gates;         // [Tm][K]
+    int32_t* chunk_hist;  // [nchunk_max][E]
+    int32_t* chunk_base;  // [nchunk_max][E]
+    int32_t* counts;      // [E]
+    int32_t* offsets;     // [E+1] unpadded exclusive scan
+    int32_t* mtile_off;   // [E+1] exclusive scan of ceil(count/128)
+    int32_t* mtile_expert;// [MTmax]
+    int32_t* mtile_rows;  // [MTmax] valid rows of each m-tile (1..128)
+    int32_t* n_mtiles;    // [1]
+    int32_t* prow;        // [Tm*K] padded row of each (token, slot)
+    uint8_t* aq;          // [Rmax][H]   e4m3 activations, expert-contiguous padded rows
+    uint32_t* asf;        // [MTmax][KB1][128] scale words in tcgen05.cp order
+    uint8_t* hq;          // [Rmax][I]   e4m3 SwiGLU output
+    uint32_t* hsf;        // [MTmax][KB2][128]
+    float* obuf;          // [Rmax][H]   expert outputs (fp32)
+    int32_t* err;         // [4] error word, where, aux
+
+    // tensor maps (host copies, passed by value to the GEMM kernels)
+    CUtensorMap tm_aq[kNumABox], tm_hq[kNumABox], tm_w13, tm_w2;
+    int num_sms;
+};
+
+// Word index of row r of m-tile mt, K-block kb, in a scale-factor buffer laid
+// out for tcgen05.cp .32x128b.warpx4: per (mt, kb) 128 words, row r at word
+// (r % 32) * 4 + r / 32; each word holds the 4 E8M0 bytes of the four
+// 32-wide K sub-blocks.
+__host__ __device__ __forceinline__ size_t sf_word_index(int mt, int kb, int KB, int r)
+{
+    return ((size_t)mt * KB + kb) * 128 + (size_t)(r & 31) * 4 + (r >> 5);
+}
+
+// launchers (route.cu)
+cudaError_t launch_router(const DevState& s, const uint16_t* x, int T, cudaStream_t st);
+cudaError_t launch_topk(const DevState& s, int T, cudaStream_t st);
+cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStream_t st, int* nlaunch);
+cudaError_t launch_combine(const DevState& s, uint16_t* y, int T, cudaStream_t st);
+// load-time helpers (route.cu)
+cudaError_t launch_repack_sf(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
+                             int K32, int mode, int I128, cudaStream_t st);
+cudaError_t launch_check_e8m0(const uint8_t* p, size_t n, int32_t* flag, cudaStream_t st);
+// getter helpers (route.cu)
+cudaError_t launch_unpad_perm(const DevState& s, int T, int32_t* out, cudaStream_t st);
+cudaError_t launch_gather_rows_u8(const DevState& s, int T, int which, uint8_t* q, uint8_t* sc, cudaStream_t st);
+cudaError_t launch_gather_obuf(const DevState& s, int T, float* out, cudaStream_t st);
+// grouped GEMMs (mx_gemm.cu)
+cudaError_t launch_gemm1(const DevState& s, cudaStream_t st);
+cudaError_t launch_gemm2(const DevState& s, cudaStream_t st);
+cudaError_t gemm_set_attributes();
+
+}  // namespace moe

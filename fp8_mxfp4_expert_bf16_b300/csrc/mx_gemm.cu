@@ -1,0 +1,371 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05), with
+// MXFP4 weights consumed natively by the block-scaled MMA and e4m3
+// activations with power-of-two (E8M0) block scales.
+//
+// Layer definition: "MiMo V2.6 Pro and Flash architecture teardown", section
+// "How Big Is Each Expert?" (gate, up and down projections around a
+// 2,048-wide middle) and section "Why Are the V2.6 Files Half the Size of
+// V2.5?" (MXFP4: E2M1 pairs per byte, one E8M0 scale per 32 values); vLLM
+// recipe "XiaomiMiMo/MiMo-V2.6-Pro-RL", "Overview" (computed as block-wise
+// FP8 e4m3).
+//
+// One persistent CTA per SM walks a static list of (m-tile, n-tile) tiles.
+// An m-tile is 128 consecutive padded rows of one expert; an n-tile is 256
+// weight rows (gate 128 + up 128 of one 128-wide slice of the expert's
+// middle for the gate/up GEMM; 256 output features for the down GEMM).
+// Warp roles:
+//   warp 0      TMA producer: per 128-wide K step, the activation tile
+//               (128 B rows, 128-byte swizzle), the weight tile (E2M1 codes
+//               expanded by TMA into 16-byte groups, the operand format of
+//               kind::mxf8f6f4) and both scale-factor chunks;
+//   warp 1      TMEM owner and MMA issuer: copies the scale chunks into
+//               TMEM (tcgen05.cp) and issues 4 block-scaled 128x256x32 MMAs
+//               per stage into one fp32 accumulator in TMEM;
+//   warps 2-5   epilogue: TMEM -> registers; gate/up: h = silu(g) * u and
+//               re-quantisation of h to e4m3 per 1 x 128 block; down: fp32
+//               rows to the expert-output buffer.
+// All waits are bounded in time; a wait that gives up writes an error word,
+// raises a CTA-wide abort flag, and the CTA drains its copies / MMAs and
+// frees TMEM before exiting.
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * 128;                                      // 16 KB activation tile
+constexpr int kBHalfBytes = 128 * 128;                                  // 16 KB: 128 weight rows in smem
+// A 128 x 128 E2M1 box occupies 16 KB of shared memory (each 8 bytes of
+// packed codes followed by an 8-byte gap) but completes only the 8 KB it
+// reads from global memory on the barrier's transaction count.
+constexpr uint32_t kBHalfTxBytes = 128 * 64;
+constexpr int kBBytes = 2 * kBHalfBytes;                                // 32 KB
+constexpr int kSFAOff = kABytes + kBBytes;                              // 512 B
+constexpr int kSFBOff = kSFAOff + 512;                                  // up to 1 KB
+constexpr int kStageStride = ((kSFBOff + 1024 + 1023) / 1024) * 1024;   // 51200
+constexpr int kBarOff = kStages * kStageStride;
+constexpr int kSmemBytes = kBarOff + 256 + 1024;                        // barriers + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0;      // accumulator: 256 fp32 columns
+constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), SFB at +8 (8 cols)
+
+struct GemmArgs {
+    const uint8_t* sfb;          // weight scale chunks [E][KB][NT][halves][512 B]
+    const uint32_t* sfa;         // activation scale words [MT][KB][128]
+    const int32_t* mtile_expert;
+    const int32_t* mtile_rows;
+    const int32_t* n_mtiles;
+    int KB;                      // K / 128
+    int NT;                      // n-tiles per m-tile
+    int halves;                  // n-tile width / 128 (2, or 1 for a 128-wide down GEMM tile)
+    int w_rows;                  // weight rows per expert (2I or H)
+    int half1_off;               // row offset of the second half inside an expert (I, or 128)
+    int half_stride;             // row step between consecutive n-tiles (128 for gate/up, 256/128 for down)
+    // gate/up epilogue
+    uint8_t* hq;                 // [R][I] e4m3
+    uint32_t* hsf;               // [MT][I/128][128]
+    int I;
+    // down epilogue
+    float* obuf;                 // [R][H]
+    int H;
+    int32_t* err;
+};
+
+struct SmemCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full;
+    uint64_t acc_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void raise_error(SmemCtl* ctl, int32_t* err, int where)
+{
+    if (atomicCAS(err, 0, kDevErrTimeout) == 0) {
+        err[1] = where;
+        err[2] = blockIdx.x;
+    }
+    *(volatile int*)&ctl->abort = 1;
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+// smallest integer e with amax <= 448 * 2^e (clamped to [-127, 127]; 0 for
+// an all-zero block), exactly from the binary exponent of amax
+__device__ __forceinline__ int act_block_exponent(float amax)
+{
+    if (!(amax > 0.f)) return 0;
+    int p;
+    const float f = frexpf(amax, &p);
+    const int e = (f <= 0.875f) ? p - 9 : p - 8;
+    return max(-127, min(127, e));
+}
+
+template <int kMode>   // 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows
+__global__ void __launch_bounds__(192, 1)
+    k_mx_gemm(const __grid_constant__ CUtensorMap tmA32, const __grid_constant__ CUtensorMap tmA64,
+              const __grid_constant__ CUtensorMap tmA128, const __grid_constant__ CUtensorMap tmW, const GemmArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kBarOff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        mbar_init(smem_u32(&ctl->acc_full), 1);
+        mbar_init(smem_u32(&ctl->acc_empty), 4);
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA32);
+        tma_prefetch_desc(&tmA64);
+        tma_prefetch_desc(&tmA128);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const volatile int* abrt = &ctl->abort;
+
+    const int NT = args.NT, KB = args.KB;
+    const int total = (*args.n_mtiles) * NT;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            uint32_t last_phase[kStages];
+            bool issued[kStages];
+            for (int s = 0; s < kStages; ++s) issued[s] = false, last_phase[s] = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const int mt = tile / NT, nt = tile - (tile / NT) * NT;
+                const int e = args.mtile_expert[mt];
+                const int rows = args.mtile_rows[mt];
+                const CUtensorMap* tA = rows <= 32 ? &tmA32 : (rows <= 64 ? &tmA64 : &tmA128);
+                const uint32_t a_bytes = (rows <= 32 ? 32u : (rows <= 64 ? 64u : 128u)) * 128u;
+                const uint32_t tx = a_bytes + args.halves * (kBHalfTxBytes + 512) + 512;
+                const int wrow0 = e * args.w_rows + nt * args.half_stride;
+                const int wrow1 = wrow0 + args.half1_off;
+                const uint8_t* sfb = args.sfb + (((size_t)e * KB) * NT + nt) * args.halves * 512;
+                const size_t sfb_kstep = (size_t)NT * args.halves * 512;
+                const uint32_t* sfa = args.sfa + (size_t)mt * KB * 128;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                    if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abrt)) {
+                        raise_error(ctl, args.err, 1);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + s * kStageStride;
+                    const uint32_t fb = smem_u32(&ctl->full[s]);
+                    mbar_arrive_expect_tx(fb, tx);
+                    tma_load_2d(smem_u32(st), tA, fb, kb * kBK, mt * kBM);
+                    tma_load_2d(smem_u32(st + kABytes), &tmW, fb, kb * kBK, wrow0);
+                    if (args.halves == 2) tma_load_2d(smem_u32(st + kABytes + kBHalfBytes), &tmW, fb, kb * kBK, wrow1);
+                    bulk_load(smem_u32(st + kSFAOff), sfa + (size_t)kb * 128, 512, fb);
+                    bulk_load(smem_u32(st + kSFBOff), sfb + kb * sfb_kstep, args.halves * 512, fb);
+                    issued[s] = true;
+                    last_phase[s] = ph;
+                }
+            }
+            // wait for every copy this thread started before the CTA may exit
+            int zero = 0;
+            for (int s = 0; s < kStages; ++s)
+                if (issued[s] && !mbar_wait(smem_u32(&ctl->full[s]), last_phase[s], &zero))
+                    raise_error(ctl, args.err, 2);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            const uint32_t idesc = idesc_mxf8f6f4(128, 128 * args.halves, kTypeE4M3, kTypeE2M1);
+            int it = 0, tcount = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
+                if (tcount > 0 && !mbar_wait(smem_u32(&ctl->acc_empty), (uint32_t)(tcount - 1) & 1u, abrt)) {
+                    raise_error(ctl, args.err, 3);
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                    if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abrt)) {
+                        raise_error(ctl, args.err, 4);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(smem + s * kStageStride);
+                    const uint32_t sfa_t = tmem + kSFCol + 16u * s;
+                    const uint32_t sfb_t = sfa_t + 8u;
+                    tmem_cp_32x128b_warpx4(sfa_t, desc_sf_chunk(st + kSFAOff));
+                    tmem_cp_32x128b_warpx4(sfb_t, desc_sf_chunk(st + kSFBOff));
+                    if (args.halves == 2) tmem_cp_32x128b_warpx4(sfb_t + 4u, desc_sf_chunk(st + kSFBOff + 512));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad = desc_kmajor_sw128(st + 32u * k);
+                        const uint64_t bd = desc_kmajor_sw128(st + kABytes + 32u * k);
+                        mma_mxf8f6f4(tmem + kAccCol, ad, bd, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
+                                     (kb | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&ctl->empty[s]));
+                }
+                if (ok) tc_commit(smem_u32(&ctl->acc_full));
+            }
+            // all MMAs of this thread complete before TMEM is released
+            int zero = 0;
+            tc_commit(smem_u32(&ctl->drain));
+            if (!mbar_wait(smem_u32(&ctl->drain), 0u, &zero)) raise_error(ctl, args.err, 5);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;                       // this warp's TMEM lane quarter
+        const int row = q * 32 + lane;
+        const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+        int tcount = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tcount) {
+            const int mt = tile / NT, nt = tile - (tile / NT) * NT;
+            const int rows = args.mtile_rows[mt];
+            if (!mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)tcount & 1u, abrt)) {
+                raise_error(ctl, args.err, 6);
+                break;
+            }
+            tc_fence_after();
+            if (kMode == 0) {
+                float h[128];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(tl + kAccCol + 16u * c, g);
+                    tmem_ld16(tl + kAccCol + 128u + 16u * c, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float gf = __uint_as_float(g[j]), uf = __uint_as_float(u[j]);
+                        h[16 * c + j] = gf / (1.0f + expf(-gf)) * uf;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty));
+                if (row < rows) {
+                    float amax = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 128; ++j) amax = fmaxf(amax, fabsf(h[j]));
+                    const int ex = act_block_exponent(amax);
+                    const float inv = __int_as_float((127 - ex) << 23);
+                    uint4* dst = reinterpret_cast<uint4*>(args.hq + (size_t)(mt * kBM + row) * args.I + nt * 128);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        uint4 w;
+                        w.x = e4m3x4(h[16 * v + 0] * inv, h[16 * v + 1] * inv, h[16 * v + 2] * inv, h[16 * v + 3] * inv);
+                        w.y = e4m3x4(h[16 * v + 4] * inv, h[16 * v + 5] * inv, h[16 * v + 6] * inv, h[16 * v + 7] * inv);
+                        w.z = e4m3x4(h[16 * v + 8] * inv, h[16 * v + 9] * inv, h[16 * v + 10] * inv, h[16 * v + 11] * inv);
+                        w.w = e4m3x4(h[16 * v + 12] * inv, h[16 * v + 13] * inv, h[16 * v + 14] * inv, h[16 * v + 15] * inv);
+                        dst[v] = w;
+                    }
+                    args.hsf[sf_word_index(mt, nt, args.I / 128, row)] = (uint32_t)(ex + 127) * 0x01010101u;
+                }
+            } else {
+                const int ncols = 128 * args.halves;
+                float* dst = args.obuf + (size_t)(mt * kBM + row) * args.H + (size_t)nt * ncols;
+                for (int c = 0; c < ncols / 16; ++c) {
+                    uint32_t v[16];
+                    tmem_ld16(tl + kAccCol + 16u * c, v);
+                    tmem_ld_wait();
+                    if (row < rows) {
+                        float4* d4 = reinterpret_cast<float4*>(dst + 16 * c);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty));
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+cudaError_t gemm_set_attributes()
+{
+    cudaError_t e = cudaFuncSetAttribute(k_mx_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_mx_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
+{
+    GemmArgs a{};
+    a.sfb = s.sfb13;
+    a.sfa = s.asf;
+    a.mtile_expert = s.mtile_expert;
+    a.mtile_rows = s.mtile_rows;
+    a.n_mtiles = s.n_mtiles;
+    a.KB = s.KB1;
+    a.NT = s.NT1;
+    a.halves = 2;
+    a.w_rows = 2 * s.I;
+    a.half1_off = s.I;
+    a.half_stride = 128;
+    a.hq = s.hq;
+    a.hsf = s.hsf;
+    a.I = s.I;
+    a.err = s.err;
+    k_mx_gemm<0><<<s.num_sms, 192, kSmemBytes, st>>>(s.tm_aq[0], s.tm_aq[1], s.tm_aq[2], s.tm_w13, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
+{
+    GemmArgs a{};
+    a.sfb = s.sfb2;
+    a.sfa = s.hsf;
+    a.mtile_expert = s.mtile_expert;
+    a.mtile_rows = s.mtile_rows;
+    a.n_mtiles = s.n_mtiles;
+    a.KB = s.KB2;
+    a.NT = s.NT2;
+    a.halves = s.BN2 / 128;
+    a.w_rows = s.H;
+    a.half1_off = 128;
+    a.half_stride = s.BN2;
+    a.obuf = s.obuf;
+    a.H = s.H;
+    a.err = s.err;
+    k_mx_gemm<1><<<s.num_sms, 192, kSmemBytes, st>>>(s.tm_hq[0], s.tm_hq[1], s.tm_hq[2], s.tm_w2, a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

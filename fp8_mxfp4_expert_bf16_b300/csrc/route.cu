@@ -1,0 +1,515 @@
+// Router, top-k gate, token->expert dispatch with activation quantisation,
+// gate-weighted combine, and the small load-time / debug kernels.
+//
+// The layer follows the web pages on MiMo-V2.6: "MiMo V2.6 Pro and Flash
+// architecture teardown", section "How Big Is Each Expert?" (sigmoid router
+// with a per-expert correction bias, 8 experts per token) and section "Why
+// Are the V2.6 Files Half the Size of V2.5?" (bf16 router); vLLM recipe
+// "XiaomiMiMo/MiMo-V2.6-Pro-RL", "Overview" (block-wise e4m3 compute).
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <climits>
+#include <cstdint>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------------------ router
+// logits[t][e] = sum_h x[t][h] * Wr[e][h] + logit_bias[e]: bf16 products are
+// exact in fp32, accumulation in fp32.  One warp per (expert, 16 tokens);
+// lanes stride over h in 8-element (16-byte) vectors, then a warp reduction.
+constexpr int kRouterTok = 16;
+
+__global__ void __launch_bounds__(256) k_router_simt(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
+                                                     const float* __restrict__ lb, float* __restrict__ logits, int T,
+                                                     int H, int E)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + warp;
+    const int t0 = blockIdx.y * kRouterTok;
+    if (e >= E) return;
+    float acc[kRouterTok];
+#pragma unroll
+    for (int i = 0; i < kRouterTok; ++i) acc[i] = 0.f;
+    const uint16_t* w = wr + (size_t)e * H;
+    for (int h = lane * 8; h < H; h += 256) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(w + h);
+        const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
+                             bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+#pragma unroll
+        for (int i = 0; i < kRouterTok; ++i) {
+            const int t = t0 + i;
+            if (t < T) {
+                const uint4 xv = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h);
+                acc[i] = fmaf(bf16_lo(xv.x), wf[0], acc[i]);
+                acc[i] = fmaf(bf16_hi(xv.x), wf[1], acc[i]);
+                acc[i] = fmaf(bf16_lo(xv.y), wf[2], acc[i]);
+                acc[i] = fmaf(bf16_hi(xv.y), wf[3], acc[i]);
+                acc[i] = fmaf(bf16_lo(xv.z), wf[4], acc[i]);
+                acc[i] = fmaf(bf16_hi(xv.z), wf[5], acc[i]);
+                acc[i] = fmaf(bf16_lo(xv.w), wf[6], acc[i]);
+                acc[i] = fmaf(bf16_hi(xv.w), wf[7], acc[i]);
+            }
+        }
+    }
+    const float bias = lb[e];
+#pragma unroll
+    for (int i = 0; i < kRouterTok; ++i) {
+        const float v = warp_sum(acc[i]);
+        if (lane == i && t0 + i < T) logits[(size_t)(t0 + i) * E + e] = v + bias;
+    }
+}
+
+cudaError_t launch_router(const DevState& s, const uint16_t* x, int T, cudaStream_t st)
+{
+    dim3 grid((s.E + 7) / 8, (T + kRouterTok - 1) / kRouterTok);
+    k_router_simt<<<grid, 256, 0, st>>>(x, s.wr, s.lb, s.logits, T, s.H, s.E);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ top-k
+// One warp per token.  Scores s = sigmoid(l) (or softmax over experts), keys
+// = s + correction bias; k rounds of a warp arg-max over (key desc, index
+// asc); gates = selected scores / their sum (summed in selection order).
+__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, const float* __restrict__ cb,
+                                              int32_t* __restrict__ ids, float* __restrict__ gates, int T, int E,
+                                              int K, int score_func)
+{
+    constexpr int kMaxV = kMaxExperts / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    const float* l = logits + (size_t)t * E;
+    float sc[kMaxV], key[kMaxV];
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i) {
+        const int e = lane + 32 * i;
+        sc[i] = (e < E) ? l[e] : -INFINITY;
+    }
+    if (score_func == 0) {
+#pragma unroll
+        for (int i = 0; i < kMaxV; ++i) sc[i] = 1.0f / (1.0f + expf(-sc[i]));
+    } else {
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kMaxV; ++i) m = fmaxf(m, sc[i]);
+        m = warp_max(m);
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < kMaxV; ++i) {
+            sc[i] = (lane + 32 * i < E) ? expf(sc[i] - m) : 0.f;
+            sum += sc[i];
+        }
+        sum = warp_sum(sum);
+#pragma unroll
+        for (int i = 0; i < kMaxV; ++i) sc[i] = sc[i] / sum;
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i) {
+        const int e = lane + 32 * i;
+        const float kv = (e < E) ? sc[i] + cb[e] : -INFINITY;
+        key[i] = isnan(kv) ? -INFINITY : kv;   // a NaN score ranks last, so every slot gets a valid expert
+    }
+    uint32_t taken = 0;
+    int my_id = 0;
+    float my_s = 0.f, ssum = 0.f;
+    for (int j = 0; j < K; ++j) {
+        float bk = -INFINITY, bs = 0.f;
+        int be = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < kMaxV; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && (key[i] > bk || (key[i] == bk && e < be))) {
+                bk = key[i];
+                be = e;
+                bs = sc[i];
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+            if (ok > bk || (ok == bk && oe < be)) {
+                bk = ok;
+                be = oe;
+                bs = os;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == j) {
+            my_id = be;
+            my_s = bs;
+        }
+        ssum += bs;
+    }
+    if (lane < K) {
+        ids[(size_t)t * K + lane] = my_id;
+        gates[(size_t)t * K + lane] = my_s / ssum;
+    }
+}
+
+cudaError_t launch_topk(const DevState& s, int T, cudaStream_t st)
+{
+    k_topk<<<(T + 7) / 8, 256, 0, st>>>(s.logits, s.cb, s.ids, s.gates, T, s.E, s.K, s.score_func);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dispatch
+// (1) per 256-token chunk, the expert histogram of its (token, slot) pairs.
+__global__ void __launch_bounds__(kChunk) k_chunk_hist(const int32_t* __restrict__ ids, int32_t* __restrict__ chunk_hist,
+                                                       int T, int E, int K, int32_t* err)
+{
+    __shared__ int hist[kMaxExperts];
+    for (int e = threadIdx.x; e < E; e += kChunk) hist[e] = 0;
+    __syncthreads();
+    const int t = blockIdx.x * kChunk + threadIdx.x;
+    if (t < T) {
+        for (int j = 0; j < K; ++j) {
+            int e = ids[(size_t)t * K + j];
+            if (e < 0 || e >= E) {   // cannot happen for ids from k_topk; keep every index in bounds anyway
+                atomicCAS(err, 0, kDevErrBounds);
+                e = min(max(e, 0), E - 1);
+            }
+            atomicAdd(&hist[e], 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kChunk) chunk_hist[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += n;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int w = (lane < NT / 32) ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += n;
+        }
+        if (lane < NT / 32) warp_tot[lane] = w;
+    }
+    __syncthreads();
+    const int base = (warp > 0) ? warp_tot[warp - 1] : 0;
+    __syncthreads();
+    return base + inc - v;
+}
+
+// (2) one block: per-expert running sums over chunks (chunk base offsets),
+// expert counts, exclusive scans (offsets, m-tile offsets) and the m-tile
+// list (expert and valid rows of every 128-row tile).
+__global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict__ chunk_hist,
+                                                      int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
+                                                      int32_t* __restrict__ offsets, int32_t* __restrict__ mtile_off,
+                                                      int32_t* __restrict__ mtile_expert,
+                                                      int32_t* __restrict__ mtile_rows, int32_t* __restrict__ n_mtiles,
+                                                      int nchunk, int E)
+{
+    __shared__ int warp_tot[32];
+    const int e = threadIdx.x;
+    int run = 0;
+    if (e < E) {
+        for (int c = 0; c < nchunk; ++c) {
+            const int v = chunk_hist[(size_t)c * E + e];
+            chunk_base[(size_t)c * E + e] = run;
+            run += v;
+        }
+        counts[e] = run;
+    }
+    const int mt = (run + kBM - 1) / kBM;
+    const int ex_cnt = block_exclusive_scan<kMaxExperts>(run, warp_tot);
+    const int ex_mt = block_exclusive_scan<kMaxExperts>(mt, warp_tot);
+    if (e < E) {
+        offsets[e] = ex_cnt;
+        mtile_off[e] = ex_mt;
+        for (int m = 0; m < mt; ++m) {
+            mtile_expert[ex_mt + m] = e;
+            mtile_rows[ex_mt + m] = min(kBM, run - kBM * m);
+        }
+        if (e == E - 1) {
+            offsets[E] = ex_cnt + run;
+            mtile_off[E] = ex_mt + mt;
+            *n_mtiles = ex_mt + mt;
+        }
+    }
+}
+
+// (3) per chunk: stable rank of every (token, slot) among the chunk's tokens
+// routed to the same expert (popcount of a per-expert token bitmask), its
+// padded row = 128 * mtile_off[e] + chunk base + rank, then the 1 x 128 e4m3
+// quantisation of each token's row written to all k of its rows.
+//
+// Quantisation of one block of 128 values: amax; the smallest integer e with
+// amax <= 448 * 2^e (from amax = f * 2^p, f in [0.5,1): e = p-9 if f <= 0.875
+// else p-8), clamped to [-127, 127], zero block -> 0; codes e4m3(v * 2^-e)
+// with round-to-nearest-even and saturation; the scale byte e + 127.
+__device__ __forceinline__ int act_block_exponent(float amax)
+{
+    if (!(amax > 0.f)) return 0;
+    int p;
+    const float f = frexpf(amax, &p);
+    int e = (f <= 0.875f) ? p - 9 : p - 8;
+    return max(-127, min(127, e));
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ float pow2_neg(int e) { return __int_as_float((127 - e) << 23); }
+
+__global__ void __launch_bounds__(kChunk) k_scatter_quant(const uint16_t* __restrict__ x, const int32_t* __restrict__ ids,
+                                                          const int32_t* __restrict__ chunk_base,
+                                                          const int32_t* __restrict__ mtile_off,
+                                                          int32_t* __restrict__ prow, uint8_t* __restrict__ aq,
+                                                          uint32_t* __restrict__ asf, int T, int H, int E, int K)
+{
+    __shared__ uint32_t mask[kMaxExperts][kChunk / 32];
+    __shared__ int rows_s[kChunk][kMaxTopK];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < E * (kChunk / 32); i += kChunk) (&mask[0][0])[i] = 0u;
+    __syncthreads();
+    const int t = blockIdx.x * kChunk + tid;
+    if (t < T)
+        for (int j = 0; j < K; ++j) atomicOr(&mask[min(max(ids[(size_t)t * K + j], 0), E - 1)][tid >> 5], 1u << lane);
+    __syncthreads();
+    if (t < T) {
+        for (int j = 0; j < K; ++j) {
+            const int e = min(max(ids[(size_t)t * K + j], 0), E - 1);
+            int rank = __popc(mask[e][tid >> 5] & ((1u << lane) - 1u));
+            for (int w = 0; w < (tid >> 5); ++w) rank += __popc(mask[e][w]);
+            const int row = mtile_off[e] * kBM + chunk_base[(size_t)blockIdx.x * E + e] + rank;
+            prow[(size_t)t * K + j] = row;
+            rows_s[tid][j] = row;
+        }
+    }
+    __syncthreads();
+    const int KB = H / 128;
+    for (int i = warp; i < kChunk; i += kChunk / 32) {
+        const int tt = blockIdx.x * kChunk + i;
+        if (tt >= T) break;
+        const uint16_t* xr = x + (size_t)tt * H;
+        for (int b = 0; b < KB; ++b) {
+            const uint2 v = *reinterpret_cast<const uint2*>(xr + b * 128 + lane * 4);
+            const float f0 = bf16_lo(v.x), f1 = bf16_hi(v.x), f2 = bf16_lo(v.y), f3 = bf16_hi(v.y);
+            const float amax = warp_max(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+            const int ex = act_block_exponent(amax);
+            const float inv = pow2_neg(ex);
+            const uint32_t word = e4m3x4(f0 * inv, f1 * inv, f2 * inv, f3 * inv);
+            for (int j = 0; j < K; ++j)
+                *reinterpret_cast<uint32_t*>(aq + (size_t)rows_s[i][j] * H + b * 128 + lane * 4) = word;
+            if (lane < K) {
+                const int row = rows_s[i][lane];
+                asf[sf_word_index(row >> 7, b, KB, row & 127)] = (uint32_t)(ex + 127) * 0x01010101u;
+            }
+        }
+    }
+}
+
+cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStream_t st, int* nlaunch)
+{
+    const int nchunk = (T + kChunk - 1) / kChunk;
+    k_chunk_hist<<<nchunk, kChunk, 0, st>>>(s.ids, s.chunk_hist, T, s.E, s.K, s.err);
+    k_scan<<<1, kMaxExperts, 0, st>>>(s.chunk_hist, s.chunk_base, s.counts, s.offsets, s.mtile_off, s.mtile_expert,
+                                      s.mtile_rows, s.n_mtiles, nchunk, s.E);
+    k_scatter_quant<<<nchunk, kChunk, 0, st>>>(x, s.ids, s.chunk_base, s.mtile_off, s.prow, s.aq, s.asf, T, s.H, s.E,
+                                               s.K);
+    *nlaunch += 3;
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ combine
+// y[t] = bf16_rne( sum_j gate[t][j] * o[row(t, j)] ), fp32 fused multiply-adds
+// in slot order.
+__global__ void __launch_bounds__(256) k_combine(const float* __restrict__ obuf, const int32_t* __restrict__ prow,
+                                                 const float* __restrict__ gates, uint16_t* __restrict__ y, int H,
+                                                 int K)
+{
+    __shared__ int rows[kMaxTopK];
+    __shared__ float g[kMaxTopK];
+    const int t = blockIdx.x;
+    if (threadIdx.x < K) {
+        rows[threadIdx.x] = prow[(size_t)t * K + threadIdx.x];
+        g[threadIdx.x] = gates[(size_t)t * K + threadIdx.x];
+    }
+    __syncthreads();
+    const int H4 = H / 4;
+    for (int h4 = threadIdx.x; h4 < H4; h4 += blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < K; ++j) {
+            const float4 o = reinterpret_cast<const float4*>(obuf + (size_t)rows[j] * H)[h4];
+            acc.x = fmaf(g[j], o.x, acc.x);
+            acc.y = fmaf(g[j], o.y, acc.y);
+            acc.z = fmaf(g[j], o.z, acc.z);
+            acc.w = fmaf(g[j], o.w, acc.w);
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 out;
+        out.x = *reinterpret_cast<const uint32_t*>(&lo);
+        out.y = *reinterpret_cast<const uint32_t*>(&hi);
+        reinterpret_cast<uint2*>(y + (size_t)t * H)[h4] = out;
+    }
+}
+
+cudaError_t launch_combine(const DevState& s, uint16_t* y, int T, cudaStream_t st)
+{
+    k_combine<<<T, 256, 0, st>>>(s.obuf, s.prow, s.gates, y, s.H, s.K);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ load time
+// Canonical scale bytes [E][rows_total][K32] -> 32-bit words in tcgen05.cp
+// chunk order [E][KB][NT][halves][128 words]; chunk (nt, half) holds the 128
+// weight rows of row block rb = half * I128 + nt (mode 0: gate/up halves of a
+// fused gate-up tile) or rb = nt * halves + half (mode 1: consecutive rows).
+__global__ void k_repack_sf(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst, int E, int KB, int NT,
+                            int halves, int rows_total, int K32, int mode, int I128)
+{
+    const size_t n = (size_t)E * KB * NT * halves * 128;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i % 128);
+        size_t q = i / 128;
+        const int hf = (int)(q % halves);
+        q /= halves;
+        const int nt = (int)(q % NT);
+        q /= NT;
+        const int kb = (int)(q % KB);
+        const int e = (int)(q / KB);
+        const int rb = (mode == 0) ? hf * I128 + nt : nt * halves + hf;
+        const int row = rb * 128 + r;
+        const uint8_t* s = src + ((size_t)e * rows_total + row) * K32 + kb * 4;
+        const uint32_t w = (uint32_t)s[0] | ((uint32_t)s[1] << 8) | ((uint32_t)s[2] << 16) | ((uint32_t)s[3] << 24);
+        const size_t chunk = (((size_t)e * KB + kb) * NT + nt) * halves + hf;
+        dst[chunk * 128 + (r & 31) * 4 + (r >> 5)] = w;
+    }
+}
+
+cudaError_t launch_repack_sf(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
+                             int K32, int mode, int I128, cudaStream_t st)
+{
+    k_repack_sf<<<1184, 256, 0, st>>>(src, reinterpret_cast<uint32_t*>(dst), E, KB, NT, halves, rows_total, K32, mode,
+                                      I128);
+    return cudaGetLastError();
+}
+
+__global__ void k_check_e8m0(const uint8_t* __restrict__ p, size_t n, int32_t* flag)
+{
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        if (p[i] == 0xFFu) {
+            atomicOr(flag, 1);
+            return;
+        }
+}
+
+cudaError_t launch_check_e8m0(const uint8_t* p, size_t n, int32_t* flag, cudaStream_t st)
+{
+    k_check_e8m0<<<1184, 256, 0, st>>>(p, n, flag);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ getters
+__global__ void k_unpad_perm(const int32_t* __restrict__ prow, const int32_t* __restrict__ ids,
+                             const int32_t* __restrict__ offsets, const int32_t* __restrict__ mtile_off,
+                             int32_t* __restrict__ out, int n)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int e = ids[i];
+    out[i] = offsets[e] + (prow[i] - mtile_off[e] * kBM);
+}
+
+cudaError_t launch_unpad_perm(const DevState& s, int T, int32_t* out, cudaStream_t st)
+{
+    const int n = T * s.K;
+    k_unpad_perm<<<(n + 255) / 256, 256, 0, st>>>(s.prow, s.ids, s.offsets, s.mtile_off, out, n);
+    return cudaGetLastError();
+}
+
+__device__ __forceinline__ int padded_row_of(const int32_t* offsets, const int32_t* mtile_off, int E, int r)
+{
+    int lo = 0, hi = E - 1;   // last e with offsets[e] <= r and a non-empty range
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (offsets[mid] <= r) lo = mid;
+        else hi = mid - 1;
+    }
+    return mtile_off[lo] * kBM + (r - offsets[lo]);
+}
+
+// which = 0: activation codes of token t (its slot-0 row); which = 1: SwiGLU
+// codes of canonical row r.  One block per output row.
+__global__ void k_gather_q(const uint8_t* __restrict__ src, const uint32_t* __restrict__ sf, const int32_t* prow,
+                           const int32_t* offsets, const int32_t* mtile_off, int E, int K, int width, int which,
+                           uint8_t* __restrict__ q, uint8_t* __restrict__ sc)
+{
+    const int r = blockIdx.x;
+    const int prw = (which == 0) ? prow[(size_t)r * K] : padded_row_of(offsets, mtile_off, E, r);
+    const int KB = width / 128;
+    for (int i = threadIdx.x; i < width; i += blockDim.x)
+        if (q) q[(size_t)r * width + i] = src[(size_t)prw * width + i];
+    for (int kb = threadIdx.x; kb < KB; kb += blockDim.x)
+        if (sc) sc[(size_t)r * KB + kb] = (uint8_t)(sf[sf_word_index(prw >> 7, kb, KB, prw & 127)] & 0xFFu);
+}
+
+cudaError_t launch_gather_rows_u8(const DevState& s, int T, int which, uint8_t* q, uint8_t* sc, cudaStream_t st)
+{
+    const int rows = (which == 0) ? T : T * s.K;
+    if (rows == 0) return cudaSuccess;
+    if (which == 0)
+        k_gather_q<<<rows, 256, 0, st>>>(s.aq, s.asf, s.prow, s.offsets, s.mtile_off, s.E, s.K, s.H, 0, q, sc);
+    else
+        k_gather_q<<<rows, 256, 0, st>>>(s.hq, s.hsf, s.prow, s.offsets, s.mtile_off, s.E, s.K, s.I, 1, q, sc);
+    return cudaGetLastError();
+}
+
+__global__ void k_gather_obuf(const float* __restrict__ obuf, const int32_t* offsets, const int32_t* mtile_off, int E,
+                              int H, float* __restrict__ out)
+{
+    const int r = blockIdx.x;
+    const int prw = padded_row_of(offsets, mtile_off, E, r);
+    for (int i = threadIdx.x; i < H; i += blockDim.x) out[(size_t)r * H + i] = obuf[(size_t)prw * H + i];
+}
+
+cudaError_t launch_gather_obuf(const DevState& s, int T, float* out, cudaStream_t st)
+{
+    const int rows = T * s.K;
+    if (rows == 0) return cudaSuccess;
+    k_gather_obuf<<<rows, 256, 0, st>>>(s.obuf, s.offsets, s.mtile_off, s.E, s.H, out);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,165 @@
+/*
+ * moe_mx.h — C ABI of a single-GPU (sm_103a) routed Mixture-of-Experts
+ * feed-forward layer whose expert weights are stored as MXFP4 and computed
+ * against block-scaled FP8 (e4m3) activations.
+ *
+ * What the layer computes (web pages on MiMo-V2.6):
+ *  - "MiMo V2.6 Pro and Flash architecture teardown" (kgptalkie), section
+ *    "How Big Is Each Expert?": a router scores the experts with a sigmoid
+ *    plus a per-expert correction bias, 8 experts per token, each expert a
+ *    gate / up / down projection around a 2,048-wide middle; section "How Is
+ *    the Backbone Built?": no shared expert; section "Why Are the V2.6 Files
+ *    Half the Size of V2.5?": experts in MXFP4 (two E2M1 values per byte, one
+ *    E8M0 scale per 32 values), router weights in BF16.
+ *  - vLLM recipe "XiaomiMiMo/MiMo-V2.6-Pro-RL", section "Overview": 384
+ *    routed experts, top-8; weights stored as mxfp4 and computed as
+ *    block-wise FP8 e4m3.
+ *  - devupai "MiMo-V2.6-Flash", section "Self-Hosting": a dynamic
+ *    activation scheme.
+ *
+ * Per token t (H = hidden, I = expert width, E = experts, k = top-k):
+ *   logits = x[t] . Wr^T + logit_bias                      (fp32)
+ *   s = sigmoid(logits) (or softmax),  key = s + sel_bias
+ *   ids = top-k of key (descending, ties to the lower index)
+ *   gates = s[ids] / sum(s[ids])
+ *   a = e4m3 quantisation of x[t], one power-of-two scale per 1 x 128 block
+ *   for each selected expert e:
+ *       [g | u] = a . W13[e]^T      (W13 [2I][H]: gate rows, then up rows)
+ *       h = silu(g) * u,  re-quantised to e4m3 per 1 x 128 block
+ *       o = h . W2[e]^T             (W2 [H][I])
+ *   y[t] = bf16( sum_j gates[j] * o_j )   (fp32 accumulation)
+ *
+ * Conventions for every entry point:
+ *  - Returns a moe_status; MOE_OK is 0.  On failure moe_last_error() gives a
+ *    one-line reason (a handle-less failure is reported through the NULL
+ *    handle, moe_last_error(NULL)).
+ *  - "device" pointers are CUDA device memory of the handle's device;
+ *    "host" pointers are ordinary (pageable or pinned) host memory.  Where
+ *    either is accepted this is said.
+ *  - The caller keeps ownership of every buffer it passes; the library keeps
+ *    ownership of its weights copy and its workspace until moe_destroy.
+ *  - bf16 values are passed as 16-bit patterns (uint16_t).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *  - A handle is not thread-safe: calls on one handle must not overlap.
+ */
+#ifndef MOE_MX_H
+#define MOE_MX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* NULL pointer, bad enum, bad value (e.g. a NaN E8M0 byte) */
+    MOE_ERR_SHAPE = 2,        /* a dimension outside the supported set */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+    MOE_ERR_OOM = 4,          /* device allocation failed */
+    MOE_ERR_NOT_LOADED = 5,   /* forward before moe_load_weights, or getter before forward */
+    MOE_ERR_TIMEOUT = 6,      /* a kernel's bounded wait gave up (reported by a later call) */
+    MOE_ERR_UNSUPPORTED = 7,  /* device is not sm_103 / feature not built */
+    MOE_ERR_DEVICE = 8        /* a kernel reported an internal consistency error */
+} moe_status;
+
+typedef struct moe_handle moe_handle;
+
+enum { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SOFTMAX = 1 };
+
+typedef struct {
+    int hidden;       /* H: multiple of 128, 128..16384 */
+    int inter;        /* I: multiple of 128, 128..16384 */
+    int num_experts;  /* E: 1..512 */
+    int top_k;        /* k: 1..min(E, 8) */
+    int max_tokens;   /* workspace is sized for 0 <= T <= max_tokens (>= 1) */
+    int score_func;   /* MOE_SCORE_SIGMOID (the pages' router) or MOE_SCORE_SOFTMAX */
+    int device;       /* CUDA device ordinal; the device must be sm_103 */
+} moe_config;
+
+/* Create a handle: checks the configuration and the device, allocates the
+ * workspace for max_tokens tokens on cfg->device.  *out receives the handle
+ * (NULL on failure). */
+moe_status moe_init(const moe_config* cfg, moe_handle** out);
+
+/* Free everything the handle owns.  NULL is accepted (no-op). */
+moe_status moe_destroy(moe_handle* h);
+
+/* Copy the layer's weights into the handle (host or device pointers; the
+ * copy is synchronous and the caller's buffers may be freed afterwards).
+ *   router_w   bf16 [E][H]
+ *   logit_bias fp32 [E], added to the router logits; NULL = zeros
+ *   sel_bias   fp32 [E], the correction bias added to the scores for
+ *              selection only; NULL = zeros
+ *   w13_q      u8 [E][2I][H/2]  packed E2M1, element 2i in the low nibble;
+ *              rows [0, I) are the gate projection, [I, 2I) the up projection
+ *   w13_s      u8 [E][2I][H/32] E8M0 scale per 32 consecutive inputs
+ *   w2_q       u8 [E][H][I/2]   down projection, packed E2M1
+ *   w2_s       u8 [E][H][I/32]
+ * A scale byte 0xFF (E8M0 NaN) fails with MOE_ERR_INVALID_ARG and leaves the
+ * handle without weights. */
+moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float* logit_bias,
+                            const float* sel_bias, const uint8_t* w13_q, const uint8_t* w13_s,
+                            const uint8_t* w2_q, const uint8_t* w2_s);
+
+/* y = layer(x) for T tokens: x bf16 [T][H] and y bf16 [T][H] are device
+ * pointers (x and y must not overlap).  Enqueued on `stream`; returns without
+ * waiting for the GPU and without reading anything back, so it can be
+ * captured in a CUDA graph.  T = 0 is a no-op.  T > max_tokens fails with
+ * MOE_ERR_SHAPE.  A device-side timeout of an earlier call is reported by
+ * the next call that synchronises (moe_check_device_error or a getter). */
+moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, void* stream);
+
+/* Same layer with host buffers: copies x (host, [T][H] bf16) to the device,
+ * runs moe_forward on `stream`, copies y back to y_host and waits for the
+ * stream.  Pinned host memory gives the fastest copies. */
+moe_status moe_forward_host(moe_handle* h, const uint16_t* x_host, int T, uint16_t* y_host, void* stream);
+
+/* Debug getters for the last forward (they synchronise the device and copy
+ * to HOST memory; T and k are those of that forward):
+ *   logits   fp32 [T][E]
+ *   ids      int32 [T][k] selected experts in selection order
+ *   gates    fp32 [T][k]
+ *   counts   int32 [E], offsets int32 [E+1] (exclusive scan of counts)
+ *   perm     int32 [T*k]: perm[t*k+j] = row of (token t, slot j) in the
+ *            expert-contiguous order, token-ascending within an expert
+ *   act q    u8 [T][H] e4m3 codes of x, scale u8 [T][H/128] E8M0 bytes
+ *   inter q  u8 [T*k][I] e4m3 codes of silu(g)*u in perm order,
+ *            scale u8 [T*k][I/128]
+ *   expert_out fp32 [T*k][H]: o of every (token, slot) row in perm order
+ * Any output pointer may be NULL to skip it. */
+moe_status moe_get_logits(moe_handle* h, float* logits);
+moe_status moe_get_routing(moe_handle* h, int32_t* ids, float* gates);
+moe_status moe_get_expert_counts(moe_handle* h, int32_t* counts, int32_t* offsets);
+moe_status moe_get_permutation(moe_handle* h, int32_t* perm);
+moe_status moe_get_act_quant(moe_handle* h, uint8_t* q, uint8_t* scale);
+moe_status moe_get_inter_quant(moe_handle* h, uint8_t* q, uint8_t* scale);
+moe_status moe_get_expert_out(moe_handle* h, float* out);
+
+/* Per-stage timing of subsequent forwards: CUDA events recorded between the
+ * stages on the forward's stream, kept for the 64 most recent forwards.
+ * moe_get_stage_times waits for the last recorded forward and writes, for
+ * each of min(n, moe_stage_count()) stages, its average milliseconds over
+ * the forwards recorded since profiling was enabled or the times were last
+ * read (at most the last 64); then it starts a new recording window. */
+moe_status moe_set_profiling(moe_handle* h, int enable);
+moe_status moe_get_stage_times(moe_handle* h, float* ms, int n);
+int moe_stage_count(void);
+const char* moe_stage_name(int i);
+
+/* Synchronise the device and report (then clear) an error word written by a
+ * kernel (MOE_ERR_TIMEOUT from a bounded wait, MOE_ERR_DEVICE otherwise). */
+moe_status moe_check_device_error(moe_handle* h);
+
+/* Number of kernels the last forward launched. */
+int moe_last_launch_count(moe_handle* h);
+
+const char* moe_last_error(moe_handle* h);
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_MX_H */

@@ -310,6 +310,7 @@ class Forward:
     hq: np.ndarray          # u8 [n, k, I] Q2 codes per (token, slot)
     hs: np.ndarray          # u8 [n, k, I/128]
     h: np.ndarray           # f64 [n, k, I] pre-quantisation SwiGLU output
+    o: np.ndarray           # f64 [n, k, H] expert outputs before the gate weighting
     y64: np.ndarray         # f64 [n, H] gate-weighted sum before rounding
     y: np.ndarray           # u16 [n, H] bf16 output
 
@@ -346,4 +347,4 @@ def forward(x_bf16, router_w_bf16, w13_q, w13_s, w2_q, w2_s, k: int,
         o[rows, slots] = o_e
     g = r.gates[toks]
     y64 = np.einsum("nk,nkh->nh", g, o)
-    return Forward(r, counts, offsets, perm, toks, aq, as_, hq, hs, h, y64, f64_to_bf16(y64))
+    return Forward(r, counts, offsets, perm, toks, aq, as_, hq, hs, h, o, y64, f64_to_bf16(y64))

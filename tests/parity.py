@@ -1,0 +1,165 @@
+"""Parity checks of the CUDA layer against the CPU oracle on the same seeded
+inputs.  Bars (written here, used by the GPU tests):
+
+  * routing ids, expert counts/offsets, permutation, Q1 codes and scales:
+    bit-exact.  Tokens whose oracle margin between the k-th and (k+1)-th
+    key is below TAU_KEY * max|key| may legitimately route either way (the
+    GPU accumulates logits in fp32, the oracle in fp64): for those the GPU's
+    choice must be a valid top-k of the oracle keys within that tolerance,
+    and they are left out of the output comparison.
+  * gates: |gpu - oracle| <= 1e-5 (fp32 sigmoid / division vs fp64).
+  * Q2 (e4m3 SwiGLU codes): equal scale bytes and codes at most one step
+    apart; at most 1e-3 of the codes may differ at all (the GPU's fp32
+    gate/up sums and the oracle's fp64 sums round differently only near an
+    e4m3 rounding boundary).
+  * y: relative L2 error <= 1e-3 and max |error| <= 2e-2 * RMS(y_oracle)
+    against the oracle's bf16-rounded output.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+TAU_KEY = 1e-5
+GATE_TOL = 1e-5
+Y_REL_L2 = 1e-3
+Y_MAX_ABS_RMS = 2e-2
+Q2_MISMATCH_FRAC = 1e-3
+
+
+def bf16_f64(u16):
+    return oracle.bf16_to_f64(np.asarray(u16, dtype=np.uint16))
+
+
+def e4m3_ordinal(codes):
+    c = np.asarray(codes, dtype=np.int64)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def run_layer(layer, inp, T=None):
+    import torch
+    x_np = inp.x if T is None else inp.x[:T]
+    x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).cuda()
+    y = layer.forward(x)
+    torch.cuda.synchronize()
+    layer.check_device_error()
+    return y.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def make_layer(inp, max_tokens=None, score_func=None):
+    import fp8_mxfp4_expert_bf16_b300 as moe
+    c = inp.cfg
+    layer = moe.MoELayer(c.H, c.I, c.E, c.k, max_tokens or inp.x.shape[0],
+                         c.score_func if score_func is None else score_func)
+    layer.load_weights(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
+    return layer
+
+
+def check_routing(r, ids_g, gates_g, k):
+    """Returns the boolean mask of tokens whose routing is unique."""
+    T = ids_g.shape[0]
+    kmax = np.abs(r.keys).max(axis=1)
+    unique = r.margin > TAU_KEY * kmax
+    same = (ids_g == r.ids).all(axis=1)
+    bad = np.nonzero(unique & ~same)[0]
+    assert bad.size == 0, f"routing differs on tokens with a clear margin: {bad[:10]}"
+    for t in np.nonzero(~same)[0]:
+        kth = np.sort(r.keys[t])[::-1][k - 1]
+        tol = TAU_KEY * kmax[t]
+        assert len(set(ids_g[t].tolist())) == k
+        assert (r.keys[t, ids_g[t]] >= kth - tol).all(), f"token {t}: invalid near-tie selection"
+    np.testing.assert_allclose(gates_g[same], r.gates[same], atol=GATE_TOL, rtol=0)
+    return same
+
+
+def check_dispatch(layer, f, ids_g, same_all):
+    counts, offsets = layer.expert_counts()
+    perm = layer.permutation()
+    if same_all:
+        assert np.array_equal(counts, f.counts)
+        assert np.array_equal(offsets, f.offsets)
+        assert np.array_equal(perm, f.perm)
+    else:
+        # routing legitimately differs on near-tie tokens: the dispatch must be
+        # exactly the histogram / stable sort of the GPU's own ids
+        flat = ids_g.reshape(-1).astype(np.int64)
+        assert np.array_equal(counts, np.bincount(flat, minlength=layer.E))
+        assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
+        expect = np.empty_like(perm)
+        expect[np.argsort(flat, kind="stable")] = np.arange(flat.size)
+        assert np.array_equal(perm, expect)
+    return perm
+
+
+def check_y(y_g, y_o, tokens_mask=None):
+    a = bf16_f64(y_g)
+    b = bf16_f64(y_o)
+    if tokens_mask is not None:
+        a, b = a[tokens_mask], b[tokens_mask]
+    assert np.isfinite(a).all()
+    rms = np.sqrt(np.mean(b * b))
+    rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+    mx = np.abs(a - b).max() / rms
+    assert rel <= Y_REL_L2, f"rel L2 {rel:.3e}"
+    assert mx <= Y_MAX_ABS_RMS, f"max abs / rms {mx:.3e}"
+    return rel, mx
+
+
+def check_q2(layer, f, perm, tokens, same):
+    """GPU SwiGLU codes (perm order) vs the oracle's for the listed tokens.
+    A block's scale byte may differ by one step only when its amax sits on a
+    power-of-two boundary to within the fp32/fp64 difference; such blocks
+    (at most Q2_MISMATCH_FRAC of all) are excluded from the code check."""
+    hq_g, hs_g = layer.inter_quant()
+    k = layer.k
+    n_diff = n_tot = n_sdiff = n_blk = 0
+    for i, t in enumerate(tokens):
+        if not same[t]:
+            continue
+        for j in range(k):
+            row = perm[t * k + j]
+            sg = hs_g[row].astype(np.int64)
+            so = f.hs[i, j].astype(np.int64)
+            assert np.abs(sg - so).max() <= 1, f"Q2 scale differs by more than one step (t={t}, j={j})"
+            eq = np.repeat(sg == so, 128)
+            n_sdiff += int((sg != so).sum())
+            n_blk += sg.size
+            d = np.abs(e4m3_ordinal(hq_g[row]) - e4m3_ordinal(f.hq[i, j]))[eq]
+            assert d.size == 0 or d.max() <= 1, f"Q2 code more than one step off (t={t}, j={j})"
+            n_diff += int((d > 0).sum())
+            n_tot += d.size
+    frac = n_diff / max(n_tot, 1)
+    assert frac <= Q2_MISMATCH_FRAC, f"Q2 code mismatch fraction {frac:.2e}"
+    assert n_sdiff <= Q2_MISMATCH_FRAC * max(n_blk, 1) + 1, f"{n_sdiff} of {n_blk} Q2 scales differ"
+    return frac
+
+
+def full_check(layer, inp, tokens=None, check_intermediates=True):
+    """Run the GPU layer on all of inp.x; compare routing/dispatch for all
+    tokens and everything else on ``tokens`` (default all)."""
+    c = inp.cfg
+    y_g = run_layer(layer, inp)
+    f = oracle.forward(inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, c.k, c.score_func,
+                       inp.logit_bias, inp.sel_bias, tokens=tokens)
+    toks = f.tokens
+    ids_g, gates_g = layer.routing()
+    same = check_routing(f.route, ids_g, gates_g, c.k)
+    perm = check_dispatch(layer, f, ids_g, bool(same.all()))
+    aq_g, as_g = layer.act_quant()
+    assert np.array_equal(aq_g[toks], f.aq) and np.array_equal(as_g[toks], f.as_)
+    stats = {"near_tie_tokens": int((~same).sum())}
+    if check_intermediates:
+        stats["q2_mismatch"] = check_q2(layer, f, perm, toks, same)
+        o_g = layer.expert_out()
+        sel = np.nonzero(same[toks])[0]
+        rows = np.array([perm[toks[i] * c.k + j] for i in sel for j in range(c.k)], dtype=np.int64)
+        og = o_g[rows].astype(np.float64)
+        oo = f.o[sel].reshape(-1, c.H)
+        o_rel = np.linalg.norm(og - oo) / np.linalg.norm(oo)
+        assert o_rel <= Y_REL_L2, f"expert output rel L2 {o_rel:.3e}"
+        stats["expert_out_rel_l2"] = float(o_rel)
+    rel, mx = check_y(y_g[toks], f.y, same[toks])
+    stats.update(rel_l2=rel, max_abs_over_rms=mx)
+    return stats, y_g, f

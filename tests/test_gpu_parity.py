@@ -1,0 +1,112 @@
+"""GPU parity: the CUDA layer (through the C ABI) against the CPU oracle on
+seeded synthetic inputs — small shapes in full, the five workloads at full
+size on sampled tokens plus full routing/dispatch."""
+import numpy as np
+import pytest
+
+import synth
+from parity import full_check, make_layer, run_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def test_toy_full_parity():
+    inp = synth.make_inputs("toy")
+    layer = make_layer(inp)
+    stats, _, _ = full_check(layer, inp)
+    print("toy", stats)
+
+
+@pytest.mark.parametrize("shape", [
+    # T, H, E, I, k, bias, score
+    (1, 512, 16, 256, 8, "none", 0),        # single token
+    (3, 512, 16, 256, 8, "none", 0),        # ragged tiny
+    (300, 512, 16, 256, 8, "none", 0),      # several m-tiles per expert, ragged tail
+    (200, 384, 8, 256, 2, "normal:1.0", 0), # hidden not a multiple of 256 (128-wide down tiles)
+    (130, 256, 1, 128, 1, "none", 0),       # one expert: a dense SwiGLU FFN; 130 rows = 2 m-tiles
+    (64, 512, 16, 256, 8, "none", 1),       # softmax scores
+    (77, 1024, 40, 384, 6, "zipf:1.1", 0),  # skewed routing, k=6, E not a power of two
+    (129, 768, 512, 128, 8, "none", 0),     # E at its maximum
+])
+def test_shapes_full_parity(shape):
+    T, H, E, I, k, bias, score = shape
+    inp = synth.custom_inputs(T, H, E, I, k, seed=100 + T, bias=bias, score_func=score)
+    layer = make_layer(inp)
+    stats, _, _ = full_check(layer, inp)
+    print(shape, stats)
+
+
+def test_forward_host_matches_device_and_is_deterministic():
+    import torch
+    inp = synth.make_inputs("toy")
+    layer = make_layer(inp)
+    y1 = run_layer(layer, inp)
+    y2 = run_layer(layer, inp)
+    assert np.array_equal(y1, y2)
+    yh = layer.forward_host(np.ascontiguousarray(inp.x))
+    assert np.array_equal(yh, y1)
+    # a smaller T on the same handle, then back
+    y_small = run_layer(layer, inp, T=5)
+    assert np.array_equal(y_small, y1[:5])
+
+
+def test_zero_tokens_is_a_noop():
+    import torch
+    inp = synth.make_inputs("toy")
+    layer = make_layer(inp)
+    x = torch.empty((0, inp.cfg.H), dtype=torch.bfloat16, device="cuda")
+    y = layer.forward(x)
+    torch.cuda.synchronize()
+    assert y.shape == (0, inp.cfg.H)
+    layer.check_device_error()
+
+
+def test_argument_errors():
+    import torch
+    import fp8_mxfp4_expert_bf16_b300 as moe
+    inp = synth.make_inputs("toy")
+    c = inp.cfg
+    layer = moe.MoELayer(c.H, c.I, c.E, c.k, 16)
+    x = torch.zeros((4, c.H), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoEError) as ei:
+        layer.forward(x)
+    assert ei.value.status == 5                                   # not loaded
+    bad = inp.w13_s.copy()
+    bad[3, 7, 2] = 0xFF
+    with pytest.raises(moe.MoEError) as ei:
+        layer.load_weights(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, bad, inp.w2_q, inp.w2_s)
+    assert ei.value.status == 1                                   # NaN scale byte
+    layer.load_weights(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
+    with pytest.raises(moe.MoEError) as ei:
+        layer.forward(torch.zeros((17, c.H), dtype=torch.bfloat16, device="cuda"))
+    assert ei.value.status == 2                                   # T > max_tokens
+    xm = torch.zeros((4 * c.H + 8,), dtype=torch.bfloat16, device="cuda")[1:1 + 4 * c.H].view(4, c.H)
+    with pytest.raises(moe.MoEError) as ei:
+        layer.forward(xm)
+    assert ei.value.status == 1                                   # misaligned
+    y = layer.forward(x)
+    torch.cuda.synchronize()
+    layer.check_device_error()
+
+
+FULL = ["flash-decode", "pro-decode", "flash-prefill", "pro-prefill-skew"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads_sampled(name):
+    inp = synth.make_inputs(name)
+    T = inp.cfg.T
+    rng = np.random.default_rng(1)
+    tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 14, replace=False)]))
+    layer = make_layer(inp)
+    stats, y, _ = full_check(layer, inp, tokens=tokens)
+    print(name, stats)
+    from parity import bf16_f64
+    assert np.isfinite(bf16_f64(y)).all()
