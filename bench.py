@@ -76,55 +76,108 @@ def ncu_traffic(workload, kernel):
 
 
 class ClockSampler:
-    """Polls the SM clock and throttle reasons through NVML while running."""
+    """SM clock and throttle reasons while the timed region runs: NVML polled
+    every 5 ms, or (if the NVML bindings do not load) an ``nvidia-smi -lms``
+    sampler whose rows inside the marked window are kept."""
 
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
                0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+    SMI_FIELDS = ["clocks_event_reasons.sw_power_cap", "clocks_event_reasons.hw_slowdown",
+                  "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.hw_thermal_slowdown"]
 
     def __init__(self, index):
+        self.index = index
         self.samples, self.reasons, self.max_mhz = [], set(), None
         self._stop = threading.Event()
         self._mark = False
+        self.nv = None
+        self.proc = None
+        self.windows = []
         try:
             import pynvml
             pynvml.nvmlInit()
-            self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:
-            self.nv = None
+            self.nv = pynvml
+        except Exception as e:   # noqa: BLE001
+            self.nvml_error = str(e)
 
     def _run(self):
+        get_reasons = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
         while not self._stop.is_set():
-            if self._mark and self.nv is not None:
+            if self._mark:
                 try:
                     self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                    r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                    r = get_reasons(self.h) if get_reasons else 0
                     for bit, name in self.REASONS.items():
                         if r & bit:
                             self.reasons.add(name)
-                except Exception:
+                except Exception:   # noqa: BLE001
                     pass
             time.sleep(0.005)
 
     def __enter__(self):
-        self.t = threading.Thread(target=self._run, daemon=True)
-        self.t.start()
+        if self.nv is not None:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        else:
+            import subprocess
+            q = "timestamp,clocks.sm,clocks.max.sm," + ",".join(self.SMI_FIELDS)
+            try:
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                              "--format=csv,noheader,nounits", "-lms", "20"],
+                                             stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:   # noqa: BLE001
+                self.proc = None
+            time.sleep(0.3)
         return self
 
     def mark(self, on):
         self._mark = on
+        if self.nv is None:
+            if on:
+                self.windows.append([time.time(), None])
+            elif self.windows:
+                self.windows[-1][1] = time.time()
 
     def __exit__(self, *a):
         self._stop.set()
-        self.t.join()
+        if self.nv is not None:
+            self.t.join()
+        elif self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            import datetime
+            rows = []
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 7:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(f[1]), float(f[2]), f[3:7]))
+                except ValueError:
+                    continue
+            inside = [r for r in rows if any(w0 - 0.02 <= r[0] <= (w1 or w0) + 0.02 for w0, w1 in self.windows)]
+            use = inside or rows[-3:]
+            self.samples = [r[1] for r in use]
+            self.max_mhz = use[0][2] if use else None
+            names = ["sw_power_cap", "hw_slowdown", "sw_thermal_slowdown", "hw_thermal_slowdown"]
+            for r in use:
+                for n, v in zip(names, r[3]):
+                    if v.lower() == "active":
+                        self.reasons.add(n)
+            self.source = "nvidia-smi" + ("" if inside else " (no sample inside the timed window; nearest kept)")
 
     def summary(self):
-        if self.nv is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        if self.nv is None and not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"]}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples),
+                "source": "nvml" if self.nv is not None else getattr(self, "source", "nvidia-smi")}
 
 
 def dist_env():
@@ -234,7 +287,7 @@ def run_gpu(args, cfg):
     g2_bytes = active * ebytes2
     g1_flops = 2.0 * rows * (2 * c.I) * c.H
     g2_flops = 2.0 * rows * c.H * c.I
-    decode = c.T * c.k <= 4 * c.E   # few rows per expert: weight streaming binds
+    decode = rows <= 64 * max(active, 1)   # a few rows per expert: streaming the weights binds
 
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -338,8 +391,19 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="shrink the workload to this many experts (small profiling captures only)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the batch size T (small profiling captures only)")
     args = ap.parse_args()
     cfg = synth.CONFIGS[args.config]
+    import dataclasses
+    if args.experts:
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}-e{args.experts}", E=args.experts,
+                                  desc=cfg.desc + f" (reduced to {args.experts} experts)")
+    if args.tokens:
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}-t{args.tokens}", T=args.tokens,
+                                  desc=cfg.desc + f" (T overridden to {args.tokens})")
     if args.impl == "reference":
         return run_reference(args, cfg)
     return run_gpu(args, cfg)

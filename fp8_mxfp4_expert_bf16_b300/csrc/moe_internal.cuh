@@ -29,10 +29,10 @@ struct DevState {
     const uint16_t* wr = nullptr;   // [E][H] bf16
     const float* lb = nullptr;      // [E]
     const float* cb = nullptr;      // [E]
-    const uint8_t* w13q = nullptr;  // [E][2I][H/2]
-    const uint8_t* w2q = nullptr;   // [E][H][I/2]
-    const uint8_t* sfb13 = nullptr; // [E][KB1][NT1][2][512]  scale chunks in tcgen05.cp order
-    const uint8_t* sfb2 = nullptr;  // [E][KB2][NT2][BN2/128][512]
+    const uint8_t* w13q = nullptr;  // tile-major E2M1 [E][NT1][KB1][2][128][64 B] (gate half, up half)
+    const uint8_t* w2q = nullptr;   // tile-major E2M1 [E][NT2][KB2][BN2/128][128][64 B]
+    const uint8_t* sfb13 = nullptr; // [E][NT1][KB1][2][512]  scale chunks in tcgen05.cp order
+    const uint8_t* sfb2 = nullptr;  // [E][NT2][KB2][BN2/128][512]
 
     // workspace
     float* logits;        // [Tm][E]
@@ -56,6 +56,7 @@ struct DevState {
 
     // tensor maps (host copies, passed by value to the GEMM kernels)
     CUtensorMap tm_aq[kNumABox], tm_hq[kNumABox], tm_w13, tm_w2;
+    CUtensorMap tm_wr64, tm_wr128;   // router weights, 64 / 128-row boxes
     int num_sms;
 };
 
@@ -76,11 +77,16 @@ cudaError_t launch_combine(const DevState& s, uint16_t* y, int T, cudaStream_t s
 // load-time helpers (route.cu)
 cudaError_t launch_repack_sf(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
                              int K32, int mode, int I128, cudaStream_t st);
+cudaError_t launch_repack_w(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
+                            int mode, int I128, cudaStream_t st);
 cudaError_t launch_check_e8m0(const uint8_t* p, size_t n, int32_t* flag, cudaStream_t st);
 // getter helpers (route.cu)
 cudaError_t launch_unpad_perm(const DevState& s, int T, int32_t* out, cudaStream_t st);
 cudaError_t launch_gather_rows_u8(const DevState& s, int T, int which, uint8_t* q, uint8_t* sc, cudaStream_t st);
 cudaError_t launch_gather_obuf(const DevState& s, int T, float* out, cudaStream_t st);
+// router on the tensor cores (router_gemm.cu)
+cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, cudaStream_t st);
+cudaError_t router_set_attributes();
 // grouped GEMMs (mx_gemm.cu)
 cudaError_t launch_gemm1(const DevState& s, cudaStream_t st);
 cudaError_t launch_gemm2(const DevState& s, cudaStream_t st);

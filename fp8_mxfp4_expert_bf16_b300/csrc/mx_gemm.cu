@@ -15,9 +15,11 @@
 // middle for the gate/up GEMM; 256 output features for the down GEMM).
 // Warp roles:
 //   warp 0      TMA producer: per 128-wide K step, the activation tile
-//               (128 B rows, 128-byte swizzle), the weight tile (E2M1 codes
+//               (128 B rows, 128-byte swizzle), the weight tile (one
+//               contiguous block of the tile-major weight layout; E2M1 codes
 //               expanded by TMA into 16-byte groups, the operand format of
-//               kind::mxf8f6f4) and both scale-factor chunks;
+//               kind::mxf8f6f4) and both scale-factor chunks; it also runs an
+//               L2 prefetch stream a few K steps ahead of the ring;
 //   warp 1      TMEM owner and MMA issuer: copies the scale chunks into
 //               TMEM (tcgen05.cp) and issues 4 block-scaled 128x256x32 MMAs
 //               per stage into one fp32 accumulator in TMEM;
@@ -38,6 +40,9 @@
 namespace moe {
 
 constexpr int kStages = 4;
+// k-steps of weights the L2 prefetch stream runs ahead of the TMA ring
+constexpr int kPrefetchGateUp = 8;
+constexpr int kPrefetchDown = 8;
 constexpr int kABytes = kBM * 128;                                      // 16 KB activation tile
 constexpr int kBHalfBytes = 128 * 128;                                  // 16 KB: 128 weight rows in smem
 // A 128 x 128 E2M1 box occupies 16 KB of shared memory (each 8 bytes of
@@ -60,16 +65,15 @@ struct GemmArgs {
     const int32_t* mtile_expert;
     const int32_t* mtile_rows;
     const int32_t* n_mtiles;
+    const uint8_t* wq;           // tile-major E2M1 weights [E][NT][KB][halves][128][64 B]
     int KB;                      // K / 128
     int NT;                      // n-tiles per m-tile
     int halves;                  // n-tile width / 128 (2, or 1 for a 128-wide down GEMM tile)
-    int w_rows;                  // weight rows per expert (2I or H)
-    int half1_off;               // row offset of the second half inside an expert (I, or 128)
-    int half_stride;             // row step between consecutive n-tiles (128 for gate/up, 256/128 for down)
     // gate/up epilogue
     uint8_t* hq;                 // [R][I] e4m3
     uint32_t* hsf;               // [MT][I/128][128]
     int I;
+    int prefetch;                // k-steps the L2 prefetch stream runs ahead (0 = off)
     // down epilogue
     float* obuf;                 // [R][H]
     int H;
@@ -157,19 +161,44 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t last_phase[kStages];
             bool issued[kStages];
             for (int s = 0; s < kStages; ++s) issued[s] = false, last_phase[s] = 0;
+            // Tile metadata (expert, valid rows) is loaded one tile ahead so the
+            // global-load latency never sits between two TMA issues.
+            const int stride = gridDim.x;
+            auto load_e = [&](int tile) { return tile < total ? args.mtile_expert[tile / NT] : 0; };
+            auto load_rows = [&](int tile) { return tile < total ? args.mtile_rows[tile / NT] : 0; };
+            // L2 prefetch stream: the same (tile, k-step) sequence as the ring,
+            // args.prefetch k-steps ahead, for the weight boxes and their scales
+            int pf_tile = blockIdx.x, pf_kb = 0;
+            int pf_e = load_e(pf_tile), pf_e_next = load_e(pf_tile + stride);
+            auto prefetch_next = [&]() {
+                if (pf_tile >= total) return;
+                const int pnt = pf_tile - (pf_tile / NT) * NT;
+                const size_t blk = (((size_t)pf_e * NT + pnt) * KB + pf_kb) * args.halves;
+                bulk_prefetch_l2(args.wq + blk * 128 * 64, args.halves * kBHalfTxBytes);
+                bulk_prefetch_l2(args.sfb + blk * 512, args.halves * 512);
+                if (++pf_kb == KB) {
+                    pf_kb = 0;
+                    pf_tile += stride;
+                    pf_e = pf_e_next;
+                    pf_e_next = load_e(pf_tile + stride);
+                }
+            };
+            for (int i = 0; i < args.prefetch; ++i) prefetch_next();
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            int cur_e = load_e(blockIdx.x), cur_rows = load_rows(blockIdx.x);
+            for (int tile = blockIdx.x; tile < total && ok; tile += stride) {
                 const int mt = tile / NT, nt = tile - (tile / NT) * NT;
-                const int e = args.mtile_expert[mt];
-                const int rows = args.mtile_rows[mt];
+                const int e = cur_e;
+                const int rows = cur_rows;
+                cur_e = load_e(tile + stride);
+                cur_rows = load_rows(tile + stride);
                 const CUtensorMap* tA = rows <= 32 ? &tmA32 : (rows <= 64 ? &tmA64 : &tmA128);
                 const uint32_t a_bytes = (rows <= 32 ? 32u : (rows <= 64 ? 64u : 128u)) * 128u;
                 const uint32_t tx = a_bytes + args.halves * (kBHalfTxBytes + 512) + 512;
-                const int wrow0 = e * args.w_rows + nt * args.half_stride;
-                const int wrow1 = wrow0 + args.half1_off;
-                const uint8_t* sfb = args.sfb + (((size_t)e * KB) * NT + nt) * args.halves * 512;
-                const size_t sfb_kstep = (size_t)NT * args.halves * 512;
+                // first 128-row block of this tile's weights in the tile-major layout
+                const int wblk0 = ((e * NT + nt) * KB) * args.halves;
+                const uint8_t* sfb = args.sfb + (size_t)wblk0 * 512;
                 const uint32_t* sfa = args.sfa + (size_t)mt * KB * 128;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
@@ -183,12 +212,13 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t fb = smem_u32(&ctl->full[s]);
                     mbar_arrive_expect_tx(fb, tx);
                     tma_load_2d(smem_u32(st), tA, fb, kb * kBK, mt * kBM);
-                    tma_load_2d(smem_u32(st + kABytes), &tmW, fb, kb * kBK, wrow0);
-                    if (args.halves == 2) tma_load_2d(smem_u32(st + kABytes + kBHalfBytes), &tmW, fb, kb * kBK, wrow1);
+                    // both halves of the weight tile are one contiguous box of 128 * halves rows
+                    tma_load_2d(smem_u32(st + kABytes), &tmW, fb, 0, (wblk0 + kb * args.halves) * 128);
                     bulk_load(smem_u32(st + kSFAOff), sfa + (size_t)kb * 128, 512, fb);
-                    bulk_load(smem_u32(st + kSFBOff), sfb + kb * sfb_kstep, args.halves * 512, fb);
+                    bulk_load(smem_u32(st + kSFBOff), sfb + (size_t)kb * args.halves * 512, args.halves * 512, fb);
                     issued[s] = true;
                     last_phase[s] = ph;
+                    prefetch_next();
                 }
             }
             // wait for every copy this thread started before the CTA may exit
@@ -254,24 +284,35 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             tc_fence_after();
+            // Rows at or past `rows` hold padding or stale shared memory (any bit
+            // pattern): no arithmetic touches them, and a warp whose 32 rows are
+            // all invalid skips its TMEM loads entirely.
+            const bool warp_live = q * 32 < rows;
+            const bool row_live = row < rows;
             if (kMode == 0) {
                 float h[128];
+                if (warp_live) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t g[16], u[16];
-                    tmem_ld16(tl + kAccCol + 16u * c, g);
-                    tmem_ld16(tl + kAccCol + 128u + 16u * c, u);
-                    tmem_ld_wait();
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t g[16], u[16];
+                        tmem_ld16(tl + kAccCol + 16u * c, g);
+                        tmem_ld16(tl + kAccCol + 128u + 16u * c, u);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float gf = __uint_as_float(g[j]), uf = __uint_as_float(u[j]);
-                        h[16 * c + j] = gf / (1.0f + expf(-gf)) * uf;
+                        for (int j = 0; j < 16; ++j) {
+                            // invalid rows are replaced by zeros before any arithmetic;
+                            // silu(g) = g / (1 + e^-g) with the fast exponential and
+                            // division intrinsics (a few ulp of fp32)
+                            const float gf = row_live ? __uint_as_float(g[j]) : 0.0f;
+                            const float uf = row_live ? __uint_as_float(u[j]) : 0.0f;
+                            h[16 * c + j] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
+                        }
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty));
-                if (row < rows) {
+                if (row_live) {
                     float amax = 0.f;
 #pragma unroll
                     for (int j = 0; j < 128; ++j) amax = fmaxf(amax, fabsf(h[j]));
@@ -292,16 +333,18 @@ __global__ void __launch_bounds__(192, 1)
             } else {
                 const int ncols = 128 * args.halves;
                 float* dst = args.obuf + (size_t)(mt * kBM + row) * args.H + (size_t)nt * ncols;
-                for (int c = 0; c < ncols / 16; ++c) {
-                    uint32_t v[16];
-                    tmem_ld16(tl + kAccCol + 16u * c, v);
-                    tmem_ld_wait();
-                    if (row < rows) {
-                        float4* d4 = reinterpret_cast<float4*>(dst + 16 * c);
+                if (warp_live) {
+                    for (int c = 0; c < ncols / 16; ++c) {
+                        uint32_t v[16];
+                        tmem_ld16(tl + kAccCol + 16u * c, v);
+                        tmem_ld_wait();
+                        if (row_live) {
+                            float4* d4 = reinterpret_cast<float4*>(dst + 16 * c);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                            for (int j = 0; j < 4; ++j)
+                                d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                        }
                     }
                 }
                 tc_fence_before();
@@ -333,15 +376,14 @@ cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
     a.mtile_expert = s.mtile_expert;
     a.mtile_rows = s.mtile_rows;
     a.n_mtiles = s.n_mtiles;
+    a.wq = s.w13q;
     a.KB = s.KB1;
     a.NT = s.NT1;
     a.halves = 2;
-    a.w_rows = 2 * s.I;
-    a.half1_off = s.I;
-    a.half_stride = 128;
     a.hq = s.hq;
     a.hsf = s.hsf;
     a.I = s.I;
+    a.prefetch = kPrefetchGateUp;
     a.err = s.err;
     k_mx_gemm<0><<<s.num_sms, 192, kSmemBytes, st>>>(s.tm_aq[0], s.tm_aq[1], s.tm_aq[2], s.tm_w13, a);
     return cudaGetLastError();
@@ -355,14 +397,13 @@ cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
     a.mtile_expert = s.mtile_expert;
     a.mtile_rows = s.mtile_rows;
     a.n_mtiles = s.n_mtiles;
+    a.wq = s.w2q;
     a.KB = s.KB2;
     a.NT = s.NT2;
     a.halves = s.BN2 / 128;
-    a.w_rows = s.H;
-    a.half1_off = 128;
-    a.half_stride = s.BN2;
     a.obuf = s.obuf;
     a.H = s.H;
+    a.prefetch = kPrefetchDown;
     a.err = s.err;
     k_mx_gemm<1><<<s.num_sms, 192, kSmemBytes, st>>>(s.tm_hq[0], s.tm_hq[1], s.tm_hq[2], s.tm_w2, a);
     return cudaGetLastError();

@@ -265,9 +265,33 @@ __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict_
 }
 
 // (3) per chunk: stable rank of every (token, slot) among the chunk's tokens
-// routed to the same expert (popcount of a per-expert token bitmask), its
-// padded row = 128 * mtile_off[e] + chunk base + rank, then the 1 x 128 e4m3
-// quantisation of each token's row written to all k of its rows.
+// routed to the same expert (popcount of a per-expert token bitmask); its
+// padded row = 128 * mtile_off[e] + chunk base + rank.
+__global__ void __launch_bounds__(kChunk) k_scatter_rows(const int32_t* __restrict__ ids,
+                                                         const int32_t* __restrict__ chunk_base,
+                                                         const int32_t* __restrict__ mtile_off,
+                                                         int32_t* __restrict__ prow, int T, int E, int K)
+{
+    __shared__ uint32_t mask[kMaxExperts][kChunk / 32];
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int i = tid; i < E * (kChunk / 32); i += kChunk) (&mask[0][0])[i] = 0u;
+    __syncthreads();
+    const int t = blockIdx.x * kChunk + tid;
+    if (t < T)
+        for (int j = 0; j < K; ++j) atomicOr(&mask[min(max(ids[(size_t)t * K + j], 0), E - 1)][tid >> 5], 1u << lane);
+    __syncthreads();
+    if (t < T) {
+        for (int j = 0; j < K; ++j) {
+            const int e = min(max(ids[(size_t)t * K + j], 0), E - 1);
+            int rank = __popc(mask[e][tid >> 5] & ((1u << lane) - 1u));
+            for (int w = 0; w < (tid >> 5); ++w) rank += __popc(mask[e][w]);
+            prow[(size_t)t * K + j] = mtile_off[e] * kBM + chunk_base[(size_t)blockIdx.x * E + e] + rank;
+        }
+    }
+}
+
+// (4) 1 x 128 e4m3 quantisation of every token's activations, written to all
+// k of its rows.  One warp per (token, 128-wide block).
 //
 // Quantisation of one block of 128 values: amax; the smallest integer e with
 // amax <= 448 * 2^e (from amax = f * 2^p, f in [0.5,1): e = p-9 if f <= 0.875
@@ -291,52 +315,26 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
 
 __device__ __forceinline__ float pow2_neg(int e) { return __int_as_float((127 - e) << 23); }
 
-__global__ void __launch_bounds__(kChunk) k_scatter_quant(const uint16_t* __restrict__ x, const int32_t* __restrict__ ids,
-                                                          const int32_t* __restrict__ chunk_base,
-                                                          const int32_t* __restrict__ mtile_off,
-                                                          int32_t* __restrict__ prow, uint8_t* __restrict__ aq,
-                                                          uint32_t* __restrict__ asf, int T, int H, int E, int K)
+__global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restrict__ x, const int32_t* __restrict__ prow,
+                                                       uint8_t* __restrict__ aq, uint32_t* __restrict__ asf, int T,
+                                                       int H, int K)
 {
-    __shared__ uint32_t mask[kMaxExperts][kChunk / 32];
-    __shared__ int rows_s[kChunk][kMaxTopK];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < E * (kChunk / 32); i += kChunk) (&mask[0][0])[i] = 0u;
-    __syncthreads();
-    const int t = blockIdx.x * kChunk + tid;
-    if (t < T)
-        for (int j = 0; j < K; ++j) atomicOr(&mask[min(max(ids[(size_t)t * K + j], 0), E - 1)][tid >> 5], 1u << lane);
-    __syncthreads();
-    if (t < T) {
-        for (int j = 0; j < K; ++j) {
-            const int e = min(max(ids[(size_t)t * K + j], 0), E - 1);
-            int rank = __popc(mask[e][tid >> 5] & ((1u << lane) - 1u));
-            for (int w = 0; w < (tid >> 5); ++w) rank += __popc(mask[e][w]);
-            const int row = mtile_off[e] * kBM + chunk_base[(size_t)blockIdx.x * E + e] + rank;
-            prow[(size_t)t * K + j] = row;
-            rows_s[tid][j] = row;
-        }
+    const int KB = H / 128, lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gw >= (long long)T * KB) return;
+    const int t = (int)(gw / KB), b = (int)(gw - (long long)t * KB);
+    const int my_row = lane < K ? prow[(size_t)t * K + lane] : 0;
+    const uint2 v = *reinterpret_cast<const uint2*>(x + (size_t)t * H + b * 128 + lane * 4);
+    const float f0 = bf16_lo(v.x), f1 = bf16_hi(v.x), f2 = bf16_lo(v.y), f3 = bf16_hi(v.y);
+    const float amax = warp_max(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+    const int ex = act_block_exponent(amax);
+    const float inv = pow2_neg(ex);
+    const uint32_t word = e4m3x4(f0 * inv, f1 * inv, f2 * inv, f3 * inv);
+    for (int j = 0; j < K; ++j) {
+        const int row = __shfl_sync(0xffffffffu, my_row, j);
+        *reinterpret_cast<uint32_t*>(aq + (size_t)row * H + b * 128 + lane * 4) = word;
     }
-    __syncthreads();
-    const int KB = H / 128;
-    for (int i = warp; i < kChunk; i += kChunk / 32) {
-        const int tt = blockIdx.x * kChunk + i;
-        if (tt >= T) break;
-        const uint16_t* xr = x + (size_t)tt * H;
-        for (int b = 0; b < KB; ++b) {
-            const uint2 v = *reinterpret_cast<const uint2*>(xr + b * 128 + lane * 4);
-            const float f0 = bf16_lo(v.x), f1 = bf16_hi(v.x), f2 = bf16_lo(v.y), f3 = bf16_hi(v.y);
-            const float amax = warp_max(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
-            const int ex = act_block_exponent(amax);
-            const float inv = pow2_neg(ex);
-            const uint32_t word = e4m3x4(f0 * inv, f1 * inv, f2 * inv, f3 * inv);
-            for (int j = 0; j < K; ++j)
-                *reinterpret_cast<uint32_t*>(aq + (size_t)rows_s[i][j] * H + b * 128 + lane * 4) = word;
-            if (lane < K) {
-                const int row = rows_s[i][lane];
-                asf[sf_word_index(row >> 7, b, KB, row & 127)] = (uint32_t)(ex + 127) * 0x01010101u;
-            }
-        }
-    }
+    if (lane < K) asf[sf_word_index(my_row >> 7, b, KB, my_row & 127)] = (uint32_t)(ex + 127) * 0x01010101u;
 }
 
 cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStream_t st, int* nlaunch)
@@ -345,9 +343,10 @@ cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStr
     k_chunk_hist<<<nchunk, kChunk, 0, st>>>(s.ids, s.chunk_hist, T, s.E, s.K, s.err);
     k_scan<<<1, kMaxExperts, 0, st>>>(s.chunk_hist, s.chunk_base, s.counts, s.offsets, s.mtile_off, s.mtile_expert,
                                       s.mtile_rows, s.n_mtiles, nchunk, s.E);
-    k_scatter_quant<<<nchunk, kChunk, 0, st>>>(x, s.ids, s.chunk_base, s.mtile_off, s.prow, s.aq, s.asf, T, s.H, s.E,
-                                               s.K);
-    *nlaunch += 3;
+    k_scatter_rows<<<nchunk, kChunk, 0, st>>>(s.ids, s.chunk_base, s.mtile_off, s.prow, T, s.E, s.K);
+    const long long warps = (long long)T * (s.H / 128);
+    k_quant_scatter<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(x, s.prow, s.aq, s.asf, T, s.H, s.K);
+    *nlaunch += 4;
     return cudaGetLastError();
 }
 
@@ -392,37 +391,78 @@ cudaError_t launch_combine(const DevState& s, uint16_t* y, int T, cudaStream_t s
 }
 
 // ------------------------------------------------------------------ load time
-// Canonical scale bytes [E][rows_total][K32] -> 32-bit words in tcgen05.cp
-// chunk order [E][KB][NT][halves][128 words]; chunk (nt, half) holds the 128
-// weight rows of row block rb = half * I128 + nt (mode 0: gate/up halves of a
-// fused gate-up tile) or rb = nt * halves + half (mode 1: consecutive rows).
+// Weight rows of one expert are grouped into tiles of 128 * halves rows (a
+// GEMM n-tile) and K into 128-wide steps.  mode 0 (fused gate/up, R = 2I):
+// tile nt holds gate rows [128 nt, 128 nt + 128) as half 0 and the matching
+// up rows (I + same) as half 1.  mode 1 (down, R = H): tile nt holds rows
+// [128 halves nt, 128 halves (nt + 1)), half = which 128-row part.
+__device__ __forceinline__ void tile_of_row(int r, int mode, int halves, int I128, int& nt, int& half, int& rr)
+{
+    rr = r & 127;
+    const int blk = r >> 7;                 // 128-row block index within the expert
+    if (mode == 0) {
+        half = blk / I128;
+        nt = blk - half * I128;
+    } else {
+        nt = blk / halves;
+        half = blk - nt * halves;
+    }
+}
+
+// Canonical scale bytes [E][R][K/32] -> 32-bit words in tcgen05.cp chunk
+// order [E][NT][KB][halves][128 words]: row rr's word at (rr % 32) * 4 + rr / 32
+// holds the E8M0 bytes of the four 32-wide K sub-blocks of K-step kb.
 __global__ void k_repack_sf(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst, int E, int KB, int NT,
                             int halves, int rows_total, int K32, int mode, int I128)
 {
-    const size_t n = (size_t)E * KB * NT * halves * 128;
+    const size_t n = (size_t)E * rows_total * KB;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const int r = (int)(i % 128);
-        size_t q = i / 128;
-        const int hf = (int)(q % halves);
-        q /= halves;
-        const int nt = (int)(q % NT);
-        q /= NT;
-        const int kb = (int)(q % KB);
-        const int e = (int)(q / KB);
-        const int rb = (mode == 0) ? hf * I128 + nt : nt * halves + hf;
-        const int row = rb * 128 + r;
-        const uint8_t* s = src + ((size_t)e * rows_total + row) * K32 + kb * 4;
+        const int kb = (int)(i % KB);
+        const size_t er = i / KB;
+        const int r = (int)(er % rows_total);
+        const int e = (int)(er / rows_total);
+        int nt, half, rr;
+        tile_of_row(r, mode, halves, I128, nt, half, rr);
+        const uint8_t* s = src + er * K32 + kb * 4;
         const uint32_t w = (uint32_t)s[0] | ((uint32_t)s[1] << 8) | ((uint32_t)s[2] << 16) | ((uint32_t)s[3] << 24);
-        const size_t chunk = (((size_t)e * KB + kb) * NT + nt) * halves + hf;
-        dst[chunk * 128 + (r & 31) * 4 + (r >> 5)] = w;
+        const size_t chunk = (((size_t)e * NT + nt) * KB + kb) * halves + half;
+        dst[chunk * 128 + (rr & 31) * 4 + (rr >> 5)] = w;
     }
 }
 
 cudaError_t launch_repack_sf(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
                              int K32, int mode, int I128, cudaStream_t st)
 {
-    k_repack_sf<<<1184, 256, 0, st>>>(src, reinterpret_cast<uint32_t*>(dst), E, KB, NT, halves, rows_total, K32, mode,
+    k_repack_sf<<<2368, 256, 0, st>>>(src, reinterpret_cast<uint32_t*>(dst), E, KB, NT, halves, rows_total, K32, mode,
                                       I128);
+    return cudaGetLastError();
+}
+
+// Canonical packed E2M1 [E][R][K/2] -> tile-major [E][NT][KB][halves][128][64 B]:
+// the 128 * halves rows x 128 K-elements that one GEMM pipeline stage reads
+// become one contiguous block (64 bytes per row).  One thread per 16 bytes.
+__global__ void k_repack_w(const uint4* __restrict__ src, uint4* __restrict__ dst, int E, int KB, int NT, int halves,
+                           int rows_total, int mode, int I128)
+{
+    const size_t n = (size_t)E * rows_total * KB * 4;   // 16-byte pieces
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int q = (int)(i & 3);                 // 16-byte piece within the 64-byte row slice
+        const int kb = (int)((i >> 2) % KB);
+        const size_t er = (i >> 2) / KB;
+        const int r = (int)(er % rows_total);
+        const int e = (int)(er / rows_total);
+        int nt, half, rr;
+        tile_of_row(r, mode, halves, I128, nt, half, rr);
+        const size_t row_t = ((((size_t)e * NT + nt) * KB + kb) * halves + half) * 128 + rr;
+        dst[row_t * 4 + q] = src[i];
+    }
+}
+
+cudaError_t launch_repack_w(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
+                            int mode, int I128, cudaStream_t st)
+{
+    k_repack_w<<<4736, 256, 0, st>>>(reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), E, KB, NT,
+                                     halves, rows_total, mode, I128);
     return cudaGetLastError();
 }
 
