@@ -16,7 +16,7 @@ import numpy as np
 
 from .build import LIB as _LIB_PATH, build as _build
 
-__all__ = ["MoELayer", "MoEError", "lib", "declared_symbols", "STAGES"]
+__all__ = ["MoELayer", "MoEError", "lib", "declared_symbols", "STAGES", "route_noalloc"]
 
 _HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_mx.h")
 
@@ -77,6 +77,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_last_launch_count": (I, [P]),
         "moe_last_error": (ctypes.c_char_p, [P]),
         "moe_status_string": (ctypes.c_char_p, [I]),
+        "moe_route_noalloc": (S, [P, I, I, P, P, P, I, I, I, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -237,3 +238,23 @@ class MoELayer:
         out = np.empty((self.last_T * self.k, self.H), dtype=np.float32)
         self._check(self.L.moe_get_expert_out(self.h, _ptr(out)))
         return out
+
+
+def route_noalloc(x, router_w, logit_bias, sel_bias, k, score_func=0, ids=None, gates=None, stream=None):
+    """Router + top-k for callers that cannot allocate device memory on their
+    call path: all buffers are the caller's (cuda tensors), the logits
+    scratch is a fixed array inside the library (T * E <= 2^20).  Calls that
+    overlap on the GPU share that array and must be serialised."""
+    import torch
+    L = lib()
+    T, H = x.shape
+    E = router_w.shape[0]
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
+    if gates is None:
+        gates = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    st = L.moe_route_noalloc(_ptr(x), T, H, _ptr(router_w), _ptr(logit_bias), _ptr(sel_bias), E, k, score_func,
+                             _ptr(ids), _ptr(gates), MoELayer._stream(stream))
+    if st != 0:
+        raise MoEError(st, L.moe_last_error(None).decode())
+    return ids, gates

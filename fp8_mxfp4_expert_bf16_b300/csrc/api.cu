@@ -40,6 +40,9 @@ struct moe_handle {
 
 static thread_local std::string g_err;
 
+// Set the message moe_last_error(NULL) returns (for entry points without a handle).
+void moe_set_handle_free_error(const char* msg) { g_err = msg; }
+
 static moe_status fail(moe_handle* h, moe_status st, const char* fmt, ...)
 {
     char buf[512];

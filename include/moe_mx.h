@@ -158,6 +158,36 @@ int moe_last_launch_count(moe_handle* h);
 const char* moe_last_error(moe_handle* h);
 const char* moe_status_string(moe_status s);
 
+/* Routing that allocates no device memory (the pages have no counterpart of
+ * this entry point; it serves callers that cannot allocate on their call
+ * path: code whose device memory belongs to its own allocator or budget, and
+ * latency-critical loops in which cudaMalloc / cudaFree could synchronise
+ * the device and stall work already in flight).
+ *
+ * Computes the router and top-k gate of the layer (the same kernels as
+ * moe_forward) for T tokens, without a handle:
+ *   x          bf16 [T][H] device, 16-byte aligned
+ *   router_w   bf16 [E][H] device, 16-byte aligned
+ *   logit_bias fp32 [E] device or NULL (zeros); sel_bias fp32 [E] device or NULL
+ *   ids        int32 [T][k] device output (selection order)
+ *   gates      fp32 [T][k] device output
+ * on `stream`, on the current CUDA device (which must be sm_103).  H must be
+ * a multiple of 64, 1 <= E <= 512, 1 <= k <= min(E, 8).
+ *
+ * Scratch: the router logits go to a fixed array compiled into the library,
+ * T * E <= 1,048,576 floats (4 MiB); every GPU that loads the library holds
+ * it until the process exits.  Larger T * E fails with MOE_ERR_SHAPE.  The
+ * first call on a device also looks up that array's device address and sets
+ * a kernel attribute on that device; make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents, so calls that overlap on the GPU (different streams, or several
+ * threads) race and must be serialised by the caller.  A kernel wait that
+ * gives up is recorded in the array's error word but not reported here.
+ * Errors are reported through moe_last_error(NULL). */
+moe_status moe_route_noalloc(const uint16_t* x, int T, int H, const uint16_t* router_w, const float* logit_bias,
+                             const float* sel_bias, int E, int k, int score_func, int32_t* ids, float* gates,
+                             void* stream);
+
 #ifdef __cplusplus
 }
 #endif
