@@ -228,6 +228,8 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
     ALLOC(s.mtile_expert, sizeof(int32_t) * s.MTmax);
     ALLOC(s.mtile_rows, sizeof(int32_t) * s.MTmax);
     ALLOC(s.n_mtiles, sizeof(int32_t) * 4);
+    ALLOC(s.light_list, sizeof(int32_t) * s.MTmax);
+    ALLOC(s.heavy_list, sizeof(int32_t) * s.MTmax);
     ALLOC(s.prow, sizeof(int32_t) * s.Tm * s.K);
     ALLOC(s.aq, (size_t)s.Rmax * s.H);
     ALLOC(s.asf, sizeof(uint32_t) * (size_t)s.MTmax * s.KB1 * 128);
@@ -246,12 +248,13 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
               cudaMemset(s.hsf, 0, sizeof(uint32_t) * (size_t)s.MTmax * s.KB2 * 128) == cudaSuccess &&
               cudaMemset(s.err, 0, sizeof(int32_t) * 4) == cudaSuccess &&
               cudaMemset(s.n_mtiles, 0, sizeof(int32_t) * 4) == cudaSuccess;
-    const uint32_t boxes[kNumABox] = {32, 64, 128};
+    const uint32_t boxes[kNumABox] = {8, 16, 32, 64, 128};
     for (int i = 0; ok && i < kNumABox; ++i) {
         ok = make_map(&s.tm_aq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.aq, s.H, s.Rmax, s.H, 128, boxes[i]) &&
              make_map(&s.tm_hq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, s.I, s.Rmax, s.I, 128, boxes[i]);
     }
-    if (ok) ok = gemm_set_attributes() == cudaSuccess && router_set_attributes() == cudaSuccess;
+    if (ok)
+        ok = gemm_set_attributes() == cudaSuccess && router_set_attributes() == cudaSuccess;
     if (ok) ok = cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         moe_destroy(h);
@@ -279,21 +282,20 @@ moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float
     const size_t E = s.E, H = s.H, I = s.I;
     const size_t n_wr = E * H * 2, n_13q = E * 2 * I * H / 2, n_13s = E * 2 * I * H / 32, n_2q = E * H * I / 2,
                  n_2s = E * H * I / 32;
-    void *d_wr, *d_b, *d_13q, *d_2q, *d_sf13, *d_sf2, *d_tmp;
+    const int halves2 = s.BN2 / 128;
+    const uint64_t rows13 = (uint64_t)E * s.NT1 * s.KB1 * 2 * kWBlockRowsPerHalf;
+    const uint64_t rows2 = (uint64_t)E * s.NT2 * s.KB2 * halves2 * kWBlockRowsPerHalf;
+    void *d_wr, *d_b, *d_13, *d_2, *d_tmp;
     size_t n_tmp = n_13q;
     if (n_2q > n_tmp) n_tmp = n_2q;
     CUDA_TRY(h, cudaMalloc(&d_wr, n_wr));
     h->w_alloc[0] = d_wr;
     CUDA_TRY(h, cudaMalloc(&d_b, 2 * E * sizeof(float)));
     h->w_alloc[1] = d_b;
-    CUDA_TRY(h, cudaMalloc(&d_13q, n_13q));
-    h->w_alloc[2] = d_13q;
-    CUDA_TRY(h, cudaMalloc(&d_2q, n_2q));
-    h->w_alloc[3] = d_2q;
-    CUDA_TRY(h, cudaMalloc(&d_sf13, n_13s));
-    h->w_alloc[4] = d_sf13;
-    CUDA_TRY(h, cudaMalloc(&d_sf2, n_2s));
-    h->w_alloc[5] = d_sf2;
+    CUDA_TRY(h, cudaMalloc(&d_13, rows13 * 64));
+    h->w_alloc[2] = d_13;
+    CUDA_TRY(h, cudaMalloc(&d_2, rows2 * 64));
+    h->w_alloc[3] = d_2;
     CUDA_TRY(h, cudaMalloc(&d_tmp, n_tmp + 256));
     h->w_alloc[6] = d_tmp;
     float* d_lb = static_cast<float*>(d_b);
@@ -303,27 +305,25 @@ moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float
     CUDA_TRY(h, cudaMemset(d_b, 0, 2 * E * sizeof(float)));
     if (logit_bias) CUDA_TRY(h, cudaMemcpy(d_lb, logit_bias, E * sizeof(float), cudaMemcpyDefault));
     if (sel_bias) CUDA_TRY(h, cudaMemcpy(d_cb, sel_bias, E * sizeof(float), cudaMemcpyDefault));
-    const int halves2 = s.BN2 / 128;
-    // expert values: canonical [E][R][K/2] -> tile-major (one contiguous block per GEMM stage)
+    // expert values: canonical [E][R][K/2] -> interleaved tile-major blocks (one contiguous run per GEMM stage)
     CUDA_TRY(h, cudaMemcpy(tmp, w13_q, n_13q, cudaMemcpyDefault));
-    CUDA_TRY(h, launch_repack_w(tmp, static_cast<uint8_t*>(d_13q), s.E, s.KB1, s.NT1, 2, 2 * s.I, 0, s.I / 128, 0));
+    CUDA_TRY(h, launch_repack_w(tmp, static_cast<uint8_t*>(d_13), s.E, s.KB1, s.NT1, 2, 2 * s.I, 0, s.I / 128, 0));
     CUDA_TRY(h, cudaDeviceSynchronize());
     CUDA_TRY(h, cudaMemcpy(tmp, w2_q, n_2q, cudaMemcpyDefault));
-    CUDA_TRY(h, launch_repack_w(tmp, static_cast<uint8_t*>(d_2q), s.E, s.KB2, s.NT2, halves2, s.H, 1, s.I / 128, 0));
+    CUDA_TRY(h, launch_repack_w(tmp, static_cast<uint8_t*>(d_2), s.E, s.KB2, s.NT2, halves2, s.H, 1, s.I / 128, 0));
     CUDA_TRY(h, cudaDeviceSynchronize());
 
     int32_t* flag = s.err + 3;
     CUDA_TRY(h, cudaMemset(flag, 0, sizeof(int32_t)));
-    // w13 scales: [E][2I][H/32] -> chunks [E][I/128][H/128][gate, up][512 B]
+    // scales: canonical [E][R][K/32] -> the scale rows of the same blocks
     CUDA_TRY(h, cudaMemcpy(tmp, w13_s, n_13s, cudaMemcpyDefault));
     CUDA_TRY(h, launch_check_e8m0(tmp, n_13s, flag, 0));
-    CUDA_TRY(h, launch_repack_sf(tmp, static_cast<uint8_t*>(d_sf13), s.E, s.KB1, s.NT1, 2, 2 * s.I, s.H / 32, 0,
+    CUDA_TRY(h, launch_repack_sf(tmp, static_cast<uint8_t*>(d_13), s.E, s.KB1, s.NT1, 2, 2 * s.I, s.H / 32, 0,
                                  s.I / 128, 0));
     CUDA_TRY(h, cudaDeviceSynchronize());
-    // w2 scales: [E][H][I/32] -> chunks [E][H/BN2][I/128][BN2/128][512 B]
     CUDA_TRY(h, cudaMemcpy(tmp, w2_s, n_2s, cudaMemcpyDefault));
     CUDA_TRY(h, launch_check_e8m0(tmp, n_2s, flag, 0));
-    CUDA_TRY(h, launch_repack_sf(tmp, static_cast<uint8_t*>(d_sf2), s.E, s.KB2, s.NT2, halves2, s.H, s.I / 32, 1,
+    CUDA_TRY(h, launch_repack_sf(tmp, static_cast<uint8_t*>(d_2), s.E, s.KB2, s.NT2, halves2, s.H, s.I / 32, 1,
                                  s.I / 128, 0));
     CUDA_TRY(h, cudaDeviceSynchronize());
     int32_t nan_found = 0;
@@ -334,20 +334,17 @@ moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float
         CUDA_TRY(h, cudaMemset(flag, 0, sizeof(int32_t)));
         return fail(h, MOE_ERR_INVALID_ARG, "moe_load_weights: an expert scale byte is 0xFF (E8M0 NaN)");
     }
-    // tile-major weights as 2-D tensors of 64-byte rows; one box = one GEMM stage
-    const uint64_t rows13 = (uint64_t)E * s.NT1 * s.KB1 * 2 * 128, rows2 = (uint64_t)E * s.NT2 * s.KB2 * halves2 * 128;
-    if (!make_map(&s.tm_w13, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, d_13q, 128, rows13, 64, 128, 256) ||
-        !make_map(&s.tm_w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, d_2q, 128, rows2, 64, 128, 128 * halves2) ||
+    // interleaved blocks as 2-D tensors of 64-byte rows; a box covers one stage's weight rows
+    if (!make_map(&s.tm_w13, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, d_13, 128, rows13, 64, 128, 256) ||
+        !make_map(&s.tm_w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, d_2, 128, rows2, 64, 128, 128 * halves2) ||
         !make_map(&s.tm_wr64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_wr, H, E, H * 2, 64, 64) ||
         !make_map(&s.tm_wr128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_wr, H, E, H * 2, 64, 128))
         return fail(h, MOE_ERR_CUDA, "moe_load_weights: cuTensorMapEncodeTiled failed for the weights");
     s.wr = static_cast<const uint16_t*>(d_wr);
     s.lb = d_lb;
     s.cb = d_cb;
-    s.w13q = static_cast<const uint8_t*>(d_13q);
-    s.w2q = static_cast<const uint8_t*>(d_2q);
-    s.sfb13 = static_cast<const uint8_t*>(d_sf13);
-    s.sfb2 = static_cast<const uint8_t*>(d_sf2);
+    s.w13q = static_cast<const uint8_t*>(d_13);
+    s.w2q = static_cast<const uint8_t*>(d_2);
     h->loaded = true;
     h->last_T = -1;
     return MOE_OK;
@@ -399,11 +396,11 @@ moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, voi
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[2], st));
     CUDA_TRY(h, launch_dispatch(s, x, T, st, &n));
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[3], st));
-    CUDA_TRY(h, launch_gemm1(s, st));
-    ++n;
+    CUDA_TRY(h, launch_gemm1(s, st));   // light then heavy m-tiles
+    n += 2;
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[4], st));
     CUDA_TRY(h, launch_gemm2(s, st));
-    ++n;
+    n += 2;
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[5], st));
     CUDA_TRY(h, launch_combine(s, y, T, st));
     ++n;

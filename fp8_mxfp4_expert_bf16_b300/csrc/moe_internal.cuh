@@ -11,7 +11,9 @@ constexpr int kBK = 128;            // K elements per pipeline stage
 constexpr int kChunk = 256;         // tokens per dispatch chunk
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 8;
-constexpr int kNumABox = 3;         // activation tile maps with 32 / 64 / 128 rows
+constexpr int kNumABox = 5;         // activation tile maps with 8 / 16 / 32 / 64 / 128 rows
+constexpr int kWBlockRowsPerHalf = 136;   // interleaved weight block: 128 weight rows + 8 scale rows of 64 B
+constexpr int kLightRows = 32;      // m-tiles with at most this many rows use the light GEMM shape
 
 // Error word codes written by kernels (first writer wins).
 constexpr int kDevErrTimeout = 1;
@@ -29,10 +31,11 @@ struct DevState {
     const uint16_t* wr = nullptr;   // [E][H] bf16
     const float* lb = nullptr;      // [E]
     const float* cb = nullptr;      // [E]
-    const uint8_t* w13q = nullptr;  // tile-major E2M1 [E][NT1][KB1][2][128][64 B] (gate half, up half)
-    const uint8_t* w2q = nullptr;   // tile-major E2M1 [E][NT2][KB2][BN2/128][128][64 B]
-    const uint8_t* sfb13 = nullptr; // [E][NT1][KB1][2][512]  scale chunks in tcgen05.cp order
-    const uint8_t* sfb2 = nullptr;  // [E][NT2][KB2][BN2/128][512]
+    // interleaved tile-major blocks [E][NT][KB] of halves * 136 rows x 64 B:
+    // the stage's E2M1 weight rows (gate half, up half for w13), then its
+    // scale chunks in tcgen05.cp order
+    const uint8_t* w13q = nullptr;
+    const uint8_t* w2q = nullptr;
 
     // workspace
     float* logits;        // [Tm][E]
@@ -45,7 +48,9 @@ struct DevState {
     int32_t* mtile_off;   // [E+1] exclusive scan of ceil(count/128)
     int32_t* mtile_expert;// [MTmax]
     int32_t* mtile_rows;  // [MTmax] valid rows of each m-tile (1..128)
-    int32_t* n_mtiles;    // [1]
+    int32_t* n_mtiles;    // [4]: all m-tiles, light m-tiles (<= kLightRows valid rows), heavy m-tiles
+    int32_t* light_list;  // [MTmax] m-tiles with at most kLightRows valid rows (light GEMM shape)
+    int32_t* heavy_list;  // [MTmax] the other m-tiles (128-row GEMMs)
     int32_t* prow;        // [Tm*K] padded row of each (token, slot)
     uint8_t* aq;          // [Rmax][H]   e4m3 activations, expert-contiguous padded rows
     uint32_t* asf;        // [MTmax][KB1][128] scale words in tcgen05.cp order

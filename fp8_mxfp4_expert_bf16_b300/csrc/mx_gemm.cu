@@ -39,33 +39,45 @@
 
 namespace moe {
 
-constexpr int kStages = 4;
-// k-steps of weights the L2 prefetch stream runs ahead of the TMA ring
-constexpr int kPrefetchGateUp = 8;
-constexpr int kPrefetchDown = 8;
-constexpr int kABytes = kBM * 128;                                      // 16 KB activation tile
-constexpr int kBHalfBytes = 128 * 128;                                  // 16 KB: 128 weight rows in smem
+// Two shapes of the same kernel:
+//  heavy (m-tiles with more than 32 valid rows): 128-row activation slot,
+//    4-stage ring;
+//  light (at most 32 valid rows: decode, and an expert's last m-tile): the
+//    activation slot holds only the 32-row box (4 KB), which buys a 5th
+//    stage.  The MMA still reads 128 rows; rows 32..127 then come from the
+//    first 12 KB of the same stage's weight tile - finite or not, they only
+//    reach accumulator rows that the epilogue never uses.
+template <bool kLight>
+struct Shape {
+    static constexpr int kStages = kLight ? 5 : 4;
+    static constexpr int kABytes = kLight ? 32 * 128 : kBM * 128;
+    static constexpr int kBOff = kABytes;
+    static constexpr int kSFAOff = kBOff + 2 * 128 * 128;     // weight tile: 256 rows x 128 B (16-byte slots)
+    static constexpr int kSFBOff = kSFAOff + 512;
+    static constexpr int kStageStride = ((kSFBOff + 1024 + 1023) / 1024) * 1024;
+    static constexpr int kBarOff = kStages * kStageStride;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+};
+static_assert(Shape<false>::kSmemBytes <= 232448 && Shape<true>::kSmemBytes <= 232448, "shared memory");
 // A 128 x 128 E2M1 box occupies 16 KB of shared memory (each 8 bytes of
 // packed codes followed by an 8-byte gap) but completes only the 8 KB it
 // reads from global memory on the barrier's transaction count.
 constexpr uint32_t kBHalfTxBytes = 128 * 64;
-constexpr int kBBytes = 2 * kBHalfBytes;                                // 32 KB
-constexpr int kSFAOff = kABytes + kBBytes;                              // 512 B
-constexpr int kSFBOff = kSFAOff + 512;                                  // up to 1 KB
-constexpr int kStageStride = ((kSFBOff + 1024 + 1023) / 1024) * 1024;   // 51200
-constexpr int kBarOff = kStages * kStageStride;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;                        // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;      // accumulator: 256 fp32 columns
 constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), SFB at +8 (8 cols)
+// k-steps of weights the L2 prefetch stream runs ahead of the TMA ring
+constexpr int kPrefetchGateUp = 8;
+constexpr int kPrefetchDown = 8;
 
 struct GemmArgs {
-    const uint8_t* sfb;          // weight scale chunks [E][KB][NT][halves][512 B]
     const uint32_t* sfa;         // activation scale words [MT][KB][128]
     const int32_t* mtile_expert;
     const int32_t* mtile_rows;
-    const int32_t* n_mtiles;
-    const uint8_t* wq;           // tile-major E2M1 weights [E][NT][KB][halves][128][64 B]
+    const int32_t* list;         // the m-tiles this kernel processes
+    const int32_t* list_count;   // their number
+    const uint8_t* wq;           // interleaved tile-major blocks [E][NT][KB]: halves*128 weight rows, halves*8 scale rows
+    int box_rows[3];             // activation box heights of the three activation maps
     int KB;                      // K / 128
     int NT;                      // n-tiles per m-tile
     int halves;                  // n-tile width / 128 (2, or 1 for a 128-wide down GEMM tile)
@@ -80,6 +92,7 @@ struct GemmArgs {
     int32_t* err;
 };
 
+template <int kStages>
 struct SmemCtl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
@@ -90,7 +103,8 @@ struct SmemCtl {
     int abort;
 };
 
-__device__ __forceinline__ void raise_error(SmemCtl* ctl, int32_t* err, int where)
+template <class Ctl>
+__device__ __forceinline__ void raise_error(Ctl* ctl, int32_t* err, int where)
 {
     if (atomicCAS(err, 0, kDevErrTimeout) == 0) {
         err[1] = where;
@@ -117,14 +131,17 @@ __device__ __forceinline__ int act_block_exponent(float amax)
     return max(-127, min(127, e));
 }
 
-template <int kMode>   // 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows
+template <int kMode, bool kLight>   // mode 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows
 __global__ void __launch_bounds__(192, 1)
-    k_mx_gemm(const __grid_constant__ CUtensorMap tmA32, const __grid_constant__ CUtensorMap tmA64,
-              const __grid_constant__ CUtensorMap tmA128, const __grid_constant__ CUtensorMap tmW, const GemmArgs args)
+    k_mx_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+              const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmW, const GemmArgs args)
 {
+    using S = Shape<kLight>;
+    constexpr int kStages = S::kStages, kABytes = S::kABytes, kStageStride = S::kStageStride;
+    constexpr int kSFAOff = S::kSFAOff, kSFBOff = S::kSFBOff;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kBarOff);
+    auto* ctl = reinterpret_cast<SmemCtl<kStages>*>(smem + S::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -137,9 +154,9 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmA32);
-        tma_prefetch_desc(&tmA64);
-        tma_prefetch_desc(&tmA128);
+        tma_prefetch_desc(&tmA0);
+        tma_prefetch_desc(&tmA1);
+        tma_prefetch_desc(&tmA2);
         tma_prefetch_desc(&tmW);
     }
     if (warp == 1) {
@@ -153,7 +170,7 @@ __global__ void __launch_bounds__(192, 1)
     const volatile int* abrt = &ctl->abort;
 
     const int NT = args.NT, KB = args.KB;
-    const int total = (*args.n_mtiles) * NT;
+    const int total = (*args.list_count) * NT;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -161,44 +178,49 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t last_phase[kStages];
             bool issued[kStages];
             for (int s = 0; s < kStages; ++s) issued[s] = false, last_phase[s] = 0;
-            // Tile metadata (expert, valid rows) is loaded one tile ahead so the
+            // Tile metadata (m-tile, expert, valid rows) is loaded ahead so the
             // global-load latency never sits between two TMA issues.
             const int stride = gridDim.x;
-            auto load_e = [&](int tile) { return tile < total ? args.mtile_expert[tile / NT] : 0; };
-            auto load_rows = [&](int tile) { return tile < total ? args.mtile_rows[tile / NT] : 0; };
+            auto load_mt = [&](int tile) { return tile < total ? args.list[tile / NT] : 0; };
             // L2 prefetch stream: the same (tile, k-step) sequence as the ring,
             // args.prefetch k-steps ahead, for the weight boxes and their scales
             int pf_tile = blockIdx.x, pf_kb = 0;
-            int pf_e = load_e(pf_tile), pf_e_next = load_e(pf_tile + stride);
+            int pf_e = args.mtile_expert[load_mt(pf_tile)];
+            int pf_mt_next = load_mt(pf_tile + stride);
             auto prefetch_next = [&]() {
                 if (pf_tile >= total) return;
                 const int pnt = pf_tile - (pf_tile / NT) * NT;
-                const size_t blk = (((size_t)pf_e * NT + pnt) * KB + pf_kb) * args.halves;
-                bulk_prefetch_l2(args.wq + blk * 128 * 64, args.halves * kBHalfTxBytes);
-                bulk_prefetch_l2(args.sfb + blk * 512, args.halves * 512);
+                const size_t wrow = ((((size_t)pf_e * NT + pnt) * KB + pf_kb) * args.halves) * kWBlockRowsPerHalf;
+                bulk_prefetch_l2(args.wq + wrow * 64, args.halves * kWBlockRowsPerHalf * 64);
                 if (++pf_kb == KB) {
                     pf_kb = 0;
                     pf_tile += stride;
-                    pf_e = pf_e_next;
-                    pf_e_next = load_e(pf_tile + stride);
+                    pf_e = args.mtile_expert[pf_mt_next];
+                    pf_mt_next = load_mt(pf_tile + stride);
                 }
             };
             for (int i = 0; i < args.prefetch; ++i) prefetch_next();
             int it = 0;
             bool ok = true;
-            int cur_e = load_e(blockIdx.x), cur_rows = load_rows(blockIdx.x);
+            int cur_mt = load_mt(blockIdx.x);
+            int cur_e = args.mtile_expert[cur_mt], cur_rows = args.mtile_rows[cur_mt];
+            int nxt_mt = load_mt(blockIdx.x + stride);
             for (int tile = blockIdx.x; tile < total && ok; tile += stride) {
-                const int mt = tile / NT, nt = tile - (tile / NT) * NT;
+                const int mt = cur_mt, nt = tile - (tile / NT) * NT;
                 const int e = cur_e;
                 const int rows = cur_rows;
-                cur_e = load_e(tile + stride);
-                cur_rows = load_rows(tile + stride);
-                const CUtensorMap* tA = rows <= 32 ? &tmA32 : (rows <= 64 ? &tmA64 : &tmA128);
-                const uint32_t a_bytes = (rows <= 32 ? 32u : (rows <= 64 ? 64u : 128u)) * 128u;
+                cur_mt = nxt_mt;
+                cur_e = args.mtile_expert[cur_mt];
+                cur_rows = args.mtile_rows[cur_mt];
+                nxt_mt = load_mt(tile + 2 * stride);
+                // activation box: the smallest of the three heights that covers the valid rows
+                const int sel = rows <= args.box_rows[0] ? 0 : (rows <= args.box_rows[1] ? 1 : 2);
+                const CUtensorMap* tA = sel == 0 ? &tmA0 : (sel == 1 ? &tmA1 : &tmA2);
+                const uint32_t a_bytes =
+                    (uint32_t)(sel == 0 ? args.box_rows[0] : (sel == 1 ? args.box_rows[1] : args.box_rows[2])) * 128u;
                 const uint32_t tx = a_bytes + args.halves * (kBHalfTxBytes + 512) + 512;
-                // first 128-row block of this tile's weights in the tile-major layout
-                const int wblk0 = ((e * NT + nt) * KB) * args.halves;
-                const uint8_t* sfb = args.sfb + (size_t)wblk0 * 512;
+                // first row of this tile's interleaved weight blocks
+                const size_t wrow0 = ((size_t)(e * NT + nt) * KB) * args.halves * kWBlockRowsPerHalf;
                 const uint32_t* sfa = args.sfa + (size_t)mt * KB * 128;
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
@@ -212,10 +234,12 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t fb = smem_u32(&ctl->full[s]);
                     mbar_arrive_expect_tx(fb, tx);
                     tma_load_2d(smem_u32(st), tA, fb, kb * kBK, mt * kBM);
-                    // both halves of the weight tile are one contiguous box of 128 * halves rows
-                    tma_load_2d(smem_u32(st + kABytes), &tmW, fb, 0, (wblk0 + kb * args.halves) * 128);
+                    // the stage's weight rows (both halves) are one box; its scale chunks follow them
+                    const size_t wrow = wrow0 + (size_t)kb * args.halves * kWBlockRowsPerHalf;
+                    tma_load_2d(smem_u32(st + S::kBOff), &tmW, fb, 0, (int)wrow);
                     bulk_load(smem_u32(st + kSFAOff), sfa + (size_t)kb * 128, 512, fb);
-                    bulk_load(smem_u32(st + kSFBOff), sfb + (size_t)kb * args.halves * 512, args.halves * 512, fb);
+                    bulk_load(smem_u32(st + kSFBOff), args.wq + (wrow + (size_t)args.halves * 128) * 64,
+                              args.halves * 512, fb);
                     issued[s] = true;
                     last_phase[s] = ph;
                     prefetch_next();
@@ -257,7 +281,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t ad = desc_kmajor_sw128(st + 32u * k);
-                        const uint64_t bd = desc_kmajor_sw128(st + kABytes + 32u * k);
+                        const uint64_t bd = desc_kmajor_sw128(st + S::kBOff + 32u * k);
                         mma_mxf8f6f4(tmem + kAccCol, ad, bd, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
                                      (kb | k) != 0 ? 1u : 0u);
                     }
@@ -277,7 +301,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         int tcount = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tcount) {
-            const int mt = tile / NT, nt = tile - (tile / NT) * NT;
+            const int mt = args.list[tile / NT], nt = tile - (tile / NT) * NT;
             const int rows = args.mtile_rows[mt];
             if (!mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)tcount & 1u, abrt)) {
                 raise_error(ctl, args.err, 6);
@@ -361,21 +385,28 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-cudaError_t gemm_set_attributes()
+template <int kMode, bool kLight>
+static cudaError_t set_attr()
 {
-    cudaError_t e = cudaFuncSetAttribute(k_mx_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_mx_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    return cudaFuncSetAttribute(k_mx_gemm<kMode, kLight>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Shape<kLight>::kSmemBytes);
 }
 
-cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
+cudaError_t gemm_set_attributes()
+{
+    cudaError_t e = set_attr<0, false>();
+    if (e == cudaSuccess) e = set_attr<0, true>();
+    if (e == cudaSuccess) e = set_attr<1, false>();
+    if (e == cudaSuccess) e = set_attr<1, true>();
+    return e;
+}
+
+static GemmArgs gemm1_args(const DevState& s)
 {
     GemmArgs a{};
-    a.sfb = s.sfb13;
     a.sfa = s.asf;
     a.mtile_expert = s.mtile_expert;
     a.mtile_rows = s.mtile_rows;
-    a.n_mtiles = s.n_mtiles;
     a.wq = s.w13q;
     a.KB = s.KB1;
     a.NT = s.NT1;
@@ -385,18 +416,15 @@ cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
     a.I = s.I;
     a.prefetch = kPrefetchGateUp;
     a.err = s.err;
-    k_mx_gemm<0><<<s.num_sms, 192, kSmemBytes, st>>>(s.tm_aq[0], s.tm_aq[1], s.tm_aq[2], s.tm_w13, a);
-    return cudaGetLastError();
+    return a;
 }
 
-cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
+static GemmArgs gemm2_args(const DevState& s)
 {
     GemmArgs a{};
-    a.sfb = s.sfb2;
     a.sfa = s.hsf;
     a.mtile_expert = s.mtile_expert;
     a.mtile_rows = s.mtile_rows;
-    a.n_mtiles = s.n_mtiles;
     a.wq = s.w2q;
     a.KB = s.KB2;
     a.NT = s.NT2;
@@ -405,7 +433,39 @@ cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
     a.H = s.H;
     a.prefetch = kPrefetchDown;
     a.err = s.err;
-    k_mx_gemm<1><<<s.num_sms, 192, kSmemBytes, st>>>(s.tm_hq[0], s.tm_hq[1], s.tm_hq[2], s.tm_w2, a);
+    return a;
+}
+
+// Light m-tiles first (their kernel's grid drains while the heavy kernel
+// starts), then heavy m-tiles; each kernel finds its own tile count on the
+// device, so an empty list costs one short launch.
+cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
+{
+    GemmArgs a = gemm1_args(s);
+    a.list = s.light_list;
+    a.list_count = s.n_mtiles + 1;
+    a.box_rows[0] = 8, a.box_rows[1] = 16, a.box_rows[2] = 32;
+    k_mx_gemm<0, true><<<s.num_sms, 192, Shape<true>::kSmemBytes, st>>>(s.tm_aq[0], s.tm_aq[1], s.tm_aq[2], s.tm_w13, a);
+    a.list = s.heavy_list;
+    a.list_count = s.n_mtiles + 2;
+    a.box_rows[0] = 32, a.box_rows[1] = 64, a.box_rows[2] = 128;
+    k_mx_gemm<0, false><<<s.num_sms, 192, Shape<false>::kSmemBytes, st>>>(s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13,
+                                                                           a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
+{
+    GemmArgs a = gemm2_args(s);
+    a.list = s.light_list;
+    a.list_count = s.n_mtiles + 1;
+    a.box_rows[0] = 8, a.box_rows[1] = 16, a.box_rows[2] = 32;
+    k_mx_gemm<1, true><<<s.num_sms, 192, Shape<true>::kSmemBytes, st>>>(s.tm_hq[0], s.tm_hq[1], s.tm_hq[2], s.tm_w2, a);
+    a.list = s.heavy_list;
+    a.list_count = s.n_mtiles + 2;
+    a.box_rows[0] = 32, a.box_rows[1] = 64, a.box_rows[2] = 128;
+    k_mx_gemm<1, false><<<s.num_sms, 192, Shape<false>::kSmemBytes, st>>>(s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2,
+                                                                           a);
     return cudaGetLastError();
 }
 

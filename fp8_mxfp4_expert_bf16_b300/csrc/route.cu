@@ -227,13 +227,16 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot)
 
 // (2) one block: per-expert running sums over chunks (chunk base offsets),
 // expert counts, exclusive scans (offsets, m-tile offsets) and the m-tile
-// list (expert and valid rows of every 128-row tile).
+// lists: every 128-row m-tile with its expert and valid rows, and the split
+// into light m-tiles (at most kLightRows valid rows: only an expert's last
+// m-tile can be one) and heavy m-tiles, each list in m-tile order.
 __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict__ chunk_hist,
                                                       int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
                                                       int32_t* __restrict__ offsets, int32_t* __restrict__ mtile_off,
                                                       int32_t* __restrict__ mtile_expert,
                                                       int32_t* __restrict__ mtile_rows, int32_t* __restrict__ n_mtiles,
-                                                      int nchunk, int E)
+                                                      int32_t* __restrict__ light_list,
+                                                      int32_t* __restrict__ heavy_list, int nchunk, int E)
 {
     __shared__ int warp_tot[32];
     const int e = threadIdx.x;
@@ -247,8 +250,13 @@ __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict_
         counts[e] = run;
     }
     const int mt = (run + kBM - 1) / kBM;
+    const int rem = run - (mt - 1) * kBM;                 // rows of the last m-tile
+    const int light = (mt > 0 && rem <= kLightRows) ? 1 : 0;
+    const int heavy = mt - light;
     const int ex_cnt = block_exclusive_scan<kMaxExperts>(run, warp_tot);
     const int ex_mt = block_exclusive_scan<kMaxExperts>(mt, warp_tot);
+    const int ex_light = block_exclusive_scan<kMaxExperts>(light, warp_tot);
+    const int ex_heavy = block_exclusive_scan<kMaxExperts>(heavy, warp_tot);
     if (e < E) {
         offsets[e] = ex_cnt;
         mtile_off[e] = ex_mt;
@@ -256,10 +264,14 @@ __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict_
             mtile_expert[ex_mt + m] = e;
             mtile_rows[ex_mt + m] = min(kBM, run - kBM * m);
         }
+        for (int m = 0; m < heavy; ++m) heavy_list[ex_heavy + m] = ex_mt + m;
+        if (light) light_list[ex_light] = ex_mt + mt - 1;
         if (e == E - 1) {
             offsets[E] = ex_cnt + run;
             mtile_off[E] = ex_mt + mt;
-            *n_mtiles = ex_mt + mt;
+            n_mtiles[0] = ex_mt + mt;
+            n_mtiles[1] = ex_light + light;
+            n_mtiles[2] = ex_heavy + heavy;
         }
     }
 }
@@ -342,7 +354,7 @@ cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStr
     const int nchunk = (T + kChunk - 1) / kChunk;
     k_chunk_hist<<<nchunk, kChunk, 0, st>>>(s.ids, s.chunk_hist, T, s.E, s.K, s.err);
     k_scan<<<1, kMaxExperts, 0, st>>>(s.chunk_hist, s.chunk_base, s.counts, s.offsets, s.mtile_off, s.mtile_expert,
-                                      s.mtile_rows, s.n_mtiles, nchunk, s.E);
+                                      s.mtile_rows, s.n_mtiles, s.light_list, s.heavy_list, nchunk, s.E);
     k_scatter_rows<<<nchunk, kChunk, 0, st>>>(s.ids, s.chunk_base, s.mtile_off, s.prow, T, s.E, s.K);
     const long long warps = (long long)T * (s.H / 128);
     k_quant_scatter<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(x, s.prow, s.aq, s.asf, T, s.H, s.K);
@@ -409,10 +421,19 @@ __device__ __forceinline__ void tile_of_row(int r, int mode, int halves, int I12
     }
 }
 
-// Canonical scale bytes [E][R][K/32] -> 32-bit words in tcgen05.cp chunk
-// order [E][NT][KB][halves][128 words]: row rr's word at (rr % 32) * 4 + rr / 32
-// holds the E8M0 bytes of the four 32-wide K sub-blocks of K-step kb.
-__global__ void k_repack_sf(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst, int E, int KB, int NT,
+// Both projections are stored as one interleaved, tile-major buffer: for
+// every (expert e, n-tile nt, K-step kb) a block of halves * 136 rows of 64
+// bytes - the halves * 128 weight rows of that GEMM stage (E2M1 codes, 128
+// per row) followed by halves * 8 rows holding the stage's scale chunks
+// (512 bytes per 128 weight rows, in tcgen05.cp order: row rr's word at
+// (rr % 32) * 4 + rr / 32 holds the E8M0 bytes of the four 32-wide K
+// sub-blocks).  One stage then reads one contiguous run of memory.
+__host__ __device__ __forceinline__ size_t wblock_row(int e, int nt, int kb, int NT, int KB, int halves)
+{
+    return ((((size_t)e * NT + nt) * KB + kb) * halves) * kWBlockRowsPerHalf;
+}
+
+__global__ void k_repack_sf(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int E, int KB, int NT,
                             int halves, int rows_total, int K32, int mode, int I128)
 {
     const size_t n = (size_t)E * rows_total * KB;
@@ -425,22 +446,21 @@ __global__ void k_repack_sf(const uint8_t* __restrict__ src, uint32_t* __restric
         tile_of_row(r, mode, halves, I128, nt, half, rr);
         const uint8_t* s = src + er * K32 + kb * 4;
         const uint32_t w = (uint32_t)s[0] | ((uint32_t)s[1] << 8) | ((uint32_t)s[2] << 16) | ((uint32_t)s[3] << 24);
-        const size_t chunk = (((size_t)e * NT + nt) * KB + kb) * halves + half;
-        dst[chunk * 128 + (rr & 31) * 4 + (rr >> 5)] = w;
+        const size_t sf_row = wblock_row(e, nt, kb, NT, KB, halves) + (size_t)halves * 128;
+        uint32_t* chunk = reinterpret_cast<uint32_t*>(dst + sf_row * 64 + (size_t)half * 512);
+        chunk[(rr & 31) * 4 + (rr >> 5)] = w;
     }
 }
 
 cudaError_t launch_repack_sf(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
                              int K32, int mode, int I128, cudaStream_t st)
 {
-    k_repack_sf<<<2368, 256, 0, st>>>(src, reinterpret_cast<uint32_t*>(dst), E, KB, NT, halves, rows_total, K32, mode,
-                                      I128);
+    k_repack_sf<<<2368, 256, 0, st>>>(src, dst, E, KB, NT, halves, rows_total, K32, mode, I128);
     return cudaGetLastError();
 }
 
-// Canonical packed E2M1 [E][R][K/2] -> tile-major [E][NT][KB][halves][128][64 B]:
-// the 128 * halves rows x 128 K-elements that one GEMM pipeline stage reads
-// become one contiguous block (64 bytes per row).  One thread per 16 bytes.
+// Canonical packed E2M1 [E][R][K/2] -> the weight rows of the interleaved
+// tile-major buffer.  One thread per 16 bytes.
 __global__ void k_repack_w(const uint4* __restrict__ src, uint4* __restrict__ dst, int E, int KB, int NT, int halves,
                            int rows_total, int mode, int I128)
 {
@@ -453,7 +473,7 @@ __global__ void k_repack_w(const uint4* __restrict__ src, uint4* __restrict__ ds
         const int e = (int)(er / rows_total);
         int nt, half, rr;
         tile_of_row(r, mode, halves, I128, nt, half, rr);
-        const size_t row_t = ((((size_t)e * NT + nt) * KB + kb) * halves + half) * 128 + rr;
+        const size_t row_t = wblock_row(e, nt, kb, NT, KB, halves) + (size_t)half * 128 + rr;
         dst[row_t * 4 + q] = src[i];
     }
 }
