@@ -218,6 +218,7 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
         return fail(nullptr, st, "%s", m.c_str());             \
     }
     ALLOC(s.logits, sizeof(float) * s.Tm * s.E);
+    ALLOC(s.logit_part, sizeof(float) * kRouterMaxSplit * (s.Tm < kRouterSplitMaxT ? s.Tm : kRouterSplitMaxT) * s.E);
     ALLOC(s.ids, sizeof(int32_t) * s.Tm * s.K);
     ALLOC(s.gates, sizeof(float) * s.Tm * s.K);
     ALLOC(s.chunk_hist, sizeof(int32_t) * s.nchunk_max * s.E);
@@ -387,14 +388,22 @@ moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, voi
     if (!make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(x), s.H, (uint64_t)T, (uint64_t)s.H * 2,
                   64, 128))
         return fail(h, MOE_ERR_CUDA, "moe_forward: cuTensorMapEncodeTiled failed for x");
+    const int ksplit = router_split(T, s.H);
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[0], st));
-    CUDA_TRY(h, launch_router_tc(s, tmX, T, st));
+    CUDA_TRY(h, launch_router_tc(s, tmX, T, st, ksplit));
     ++n;
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[1], st));
-    CUDA_TRY(h, launch_topk(s, T, st));
+    CUDA_TRY(h, launch_topk(s, T, st, ksplit));
     ++n;
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[2], st));
-    CUDA_TRY(h, launch_dispatch(s, x, T, st, &n));
+    if (T <= kChunk) {
+        // small batch: histogram, scan and ranks in one single-block kernel
+        CUDA_TRY(h, launch_dispatch_small(s, T, st));
+        CUDA_TRY(h, launch_quant_scatter(s, x, T, st));
+        n += 2;
+    } else {
+        CUDA_TRY(h, launch_dispatch(s, x, T, st, &n));
+    }
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[3], st));
     CUDA_TRY(h, launch_gemm1(s, st));   // light then heavy m-tiles
     n += 2;

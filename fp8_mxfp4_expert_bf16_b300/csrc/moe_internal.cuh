@@ -12,7 +12,9 @@ constexpr int kChunk = 256;         // tokens per dispatch chunk
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 8;
 constexpr int kNumABox = 5;         // activation tile maps with 8 / 16 / 32 / 64 / 128 rows
-constexpr int kWBlockRowsPerHalf = 136;   // interleaved weight block: 128 weight rows + 8 scale rows of 64 B
+constexpr int kWBlockRowsPerHalf = 136;
+constexpr int kRouterMaxSplit = 16;       // split-K factor of the router for small batches
+constexpr int kRouterSplitMaxT = 512;     // batches up to this size use the split-K router   // interleaved weight block: 128 weight rows + 8 scale rows of 64 B
 constexpr int kLightRows = 32;      // m-tiles with at most this many rows use the light GEMM shape
 
 // Error word codes written by kernels (first writer wins).
@@ -39,6 +41,7 @@ struct DevState {
 
     // workspace
     float* logits;        // [Tm][E]
+    float* logit_part;    // [kRouterMaxSplit][min(Tm, kRouterSplitMaxT)][E] split-K partial logits (small T)
     int32_t* ids;         // [Tm][K]
     float* gates;         // [Tm][K]
     int32_t* chunk_hist;  // [nchunk_max][E]
@@ -76,7 +79,9 @@ __host__ __device__ __forceinline__ size_t sf_word_index(int mt, int kb, int KB,
 
 // launchers (route.cu)
 cudaError_t launch_router(const DevState& s, const uint16_t* x, int T, cudaStream_t st);
-cudaError_t launch_topk(const DevState& s, int T, cudaStream_t st);
+cudaError_t launch_topk(const DevState& s, int T, cudaStream_t st, int ksplit = 1);
+cudaError_t launch_dispatch_small(const DevState& s, int T, cudaStream_t st);
+cudaError_t launch_quant_scatter(const DevState& s, const uint16_t* x, int T, cudaStream_t st);
 cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStream_t st, int* nlaunch);
 cudaError_t launch_combine(const DevState& s, uint16_t* y, int T, cudaStream_t st);
 // load-time helpers (route.cu)
@@ -90,7 +95,8 @@ cudaError_t launch_unpad_perm(const DevState& s, int T, int32_t* out, cudaStream
 cudaError_t launch_gather_rows_u8(const DevState& s, int T, int which, uint8_t* q, uint8_t* sc, cudaStream_t st);
 cudaError_t launch_gather_obuf(const DevState& s, int T, float* out, cudaStream_t st);
 // router on the tensor cores (router_gemm.cu)
-cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, cudaStream_t st);
+cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, cudaStream_t st, int ksplit = 1);
+int router_split(int T, int H);
 cudaError_t router_set_attributes();
 // grouped GEMMs (mx_gemm.cu)
 cudaError_t launch_gemm1(const DevState& s, cudaStream_t st);

@@ -88,24 +88,45 @@ cudaError_t launch_router(const DevState& s, const uint16_t* x, int T, cudaStrea
 }
 
 // ------------------------------------------------------------------ top-k
-// One warp per token.  Scores s = sigmoid(l) (or softmax over experts), keys
-// = s + correction bias; k rounds of a warp arg-max over (key desc, index
-// asc); gates = selected scores / their sum (summed in selection order).
-__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, const float* __restrict__ cb,
-                                              int32_t* __restrict__ ids, float* __restrict__ gates, int T, int E,
-                                              int K, int score_func)
+// Router logits of token t for this lane's experts (e = lane + 32 i): either
+// the finished logits, or the sum of the split-K partial products in split
+// order plus the logit bias (then also stored as the token's logits).
+constexpr int kMaxV = kMaxExperts / 32;
+
+__device__ __forceinline__ void token_logits(const float* __restrict__ logits, const float* __restrict__ part,
+                                             int ksplit, const float* __restrict__ lb, float* __restrict__ logits_out,
+                                             int t, int T, int E, int lane, float (&l)[kMaxV])
 {
-    constexpr int kMaxV = kMaxExperts / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= T) return;
-    const float* l = logits + (size_t)t * E;
-    float sc[kMaxV], key[kMaxV];
 #pragma unroll
     for (int i = 0; i < kMaxV; ++i) {
         const int e = lane + 32 * i;
-        sc[i] = (e < E) ? l[e] : -INFINITY;
+        if (e >= E) {
+            l[i] = -INFINITY;
+        } else if (ksplit > 1) {
+            // all partial loads are issued before the (ordered) additions
+            float p[kRouterMaxSplit];
+#pragma unroll
+            for (int z = 0; z < kRouterMaxSplit; ++z) p[z] = z < ksplit ? part[((size_t)z * T + t) * E + e] : 0.f;
+            float v = 0.f;
+#pragma unroll
+            for (int z = 0; z < kRouterMaxSplit; ++z) v += p[z];
+            v += lb[e];
+            logits_out[(size_t)t * E + e] = v;
+            l[i] = v;
+        } else {
+            l[i] = logits[(size_t)t * E + e];
+        }
     }
+}
+
+// Scores s = sigmoid(l) (or softmax over experts), keys = s + correction
+// bias; k rounds of a warp arg-max over (key desc, index asc); gates =
+// selected scores / their sum (summed in selection order).  Lane j < k ends
+// with slot j's expert and gate.
+__device__ __forceinline__ void warp_topk(float (&sc)[kMaxV], const float* __restrict__ cb, int E, int K,
+                                          int score_func, int lane, int& my_id, float& my_gate)
+{
+    float key[kMaxV];
     if (score_func == 0) {
 #pragma unroll
         for (int i = 0; i < kMaxV; ++i) sc[i] = 1.0f / (1.0f + expf(-sc[i]));
@@ -131,8 +152,8 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
         key[i] = isnan(kv) ? -INFINITY : kv;   // a NaN score ranks last, so every slot gets a valid expert
     }
     uint32_t taken = 0;
-    int my_id = 0;
     float my_s = 0.f, ssum = 0.f;
+    my_id = 0;
     for (int j = 0; j < K; ++j) {
         float bk = -INFINITY, bs = 0.f;
         int be = INT_MAX;
@@ -163,15 +184,33 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
         }
         ssum += bs;
     }
+    my_gate = my_s / ssum;
+}
+
+// One warp per token.
+__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, const float* __restrict__ part,
+                                              int ksplit, const float* __restrict__ lb, float* __restrict__ logits_out,
+                                              const float* __restrict__ cb, int32_t* __restrict__ ids,
+                                              float* __restrict__ gates, int T, int E, int K, int score_func)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    float sc[kMaxV];
+    token_logits(logits, part, ksplit, lb, logits_out, t, T, E, lane, sc);
+    int id;
+    float g;
+    warp_topk(sc, cb, E, K, score_func, lane, id, g);
     if (lane < K) {
-        ids[(size_t)t * K + lane] = my_id;
-        gates[(size_t)t * K + lane] = my_s / ssum;
+        ids[(size_t)t * K + lane] = id;
+        gates[(size_t)t * K + lane] = g;
     }
 }
 
-cudaError_t launch_topk(const DevState& s, int T, cudaStream_t st)
+cudaError_t launch_topk(const DevState& s, int T, cudaStream_t st, int ksplit)
 {
-    k_topk<<<(T + 7) / 8, 256, 0, st>>>(s.logits, s.cb, s.ids, s.gates, T, s.E, s.K, s.score_func);
+    k_topk<<<(T + 7) / 8, 256, 0, st>>>(s.logits, s.logit_part, ksplit, s.lb, s.logits, s.cb, s.ids, s.gates, T, s.E,
+                                        s.K, s.score_func);
     return cudaGetLastError();
 }
 
@@ -347,6 +386,93 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
         *reinterpret_cast<uint32_t*>(aq + (size_t)row * H + b * 128 + lane * 4) = word;
     }
     if (lane < K) asf[sf_word_index(my_row >> 7, b, KB, my_row & 127)] = (uint32_t)(ex + 127) * 0x01010101u;
+}
+
+// Small batches (T <= 256, one dispatch chunk): one block builds the expert
+// histogram and token bit-masks, the scan and m-tile lists, and the stable
+// ranks - the work of k_chunk_hist, k_scan and k_scatter_rows in a single
+// launch.
+constexpr int kSmallT = kChunk;
+
+__global__ void __launch_bounds__(kMaxExperts) k_dispatch_small(
+    const int32_t* __restrict__ ids, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ mtile_off, int32_t* __restrict__ mtile_expert, int32_t* __restrict__ mtile_rows,
+    int32_t* __restrict__ n_mtiles, int32_t* __restrict__ light_list, int32_t* __restrict__ heavy_list,
+    int32_t* __restrict__ prow, int T, int E, int K)
+{
+    __shared__ int hist[kMaxExperts];
+    __shared__ int mt_off_s[kMaxExperts];
+    __shared__ uint32_t mask[kMaxExperts][kSmallT / 32];
+    __shared__ int warp_tot[32];
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int i = tid; i < kMaxExperts; i += blockDim.x) hist[i] = 0;
+    for (int i = tid; i < kMaxExperts * (kSmallT / 32); i += blockDim.x) (&mask[0][0])[i] = 0u;
+    __syncthreads();
+    int my_ids[kMaxTopK];
+    if (tid < T) {
+        for (int j = 0; j < K; ++j) {
+            const int ex = min(max(ids[(size_t)tid * K + j], 0), E - 1);
+            my_ids[j] = ex;
+            atomicAdd(&hist[ex], 1);
+            atomicOr(&mask[ex][tid >> 5], 1u << lane);
+        }
+    }
+    __syncthreads();
+    // counts, scans, m-tile lists (thread = expert)
+    const int e = tid;
+    const int run = e < E ? hist[e] : 0;
+    const int mt = (run + kBM - 1) / kBM;
+    const int rem = run - (mt - 1) * kBM;
+    const int light = (mt > 0 && rem <= kLightRows) ? 1 : 0;
+    const int heavy = mt - light;
+    const int ex_cnt = block_exclusive_scan<kMaxExperts>(run, warp_tot);
+    const int ex_mt = block_exclusive_scan<kMaxExperts>(mt, warp_tot);
+    const int ex_light = block_exclusive_scan<kMaxExperts>(light, warp_tot);
+    const int ex_heavy = block_exclusive_scan<kMaxExperts>(heavy, warp_tot);
+    if (e < E) {
+        counts[e] = run;
+        offsets[e] = ex_cnt;
+        mtile_off[e] = ex_mt;
+        mt_off_s[e] = ex_mt;
+        for (int m = 0; m < mt; ++m) {
+            mtile_expert[ex_mt + m] = e;
+            mtile_rows[ex_mt + m] = min(kBM, run - kBM * m);
+        }
+        for (int m = 0; m < heavy; ++m) heavy_list[ex_heavy + m] = ex_mt + m;
+        if (light) light_list[ex_light] = ex_mt + mt - 1;
+        if (e == E - 1) {
+            offsets[E] = ex_cnt + run;
+            mtile_off[E] = ex_mt + mt;
+            n_mtiles[0] = ex_mt + mt;
+            n_mtiles[1] = ex_light + light;
+            n_mtiles[2] = ex_heavy + heavy;
+        }
+    }
+    __syncthreads();
+    // stable ranks (thread = token)
+    if (tid < T) {
+        for (int j = 0; j < K; ++j) {
+            const int ex = my_ids[j];
+            int rank = __popc(mask[ex][tid >> 5] & ((1u << lane) - 1u));
+            for (int w = 0; w < (tid >> 5); ++w) rank += __popc(mask[ex][w]);
+            prow[(size_t)tid * K + j] = mt_off_s[ex] * kBM + rank;
+        }
+    }
+}
+
+cudaError_t launch_dispatch_small(const DevState& s, int T, cudaStream_t st)
+{
+    k_dispatch_small<<<1, kMaxExperts, 0, st>>>(s.ids, s.counts, s.offsets, s.mtile_off, s.mtile_expert,
+                                                s.mtile_rows, s.n_mtiles, s.light_list, s.heavy_list, s.prow, T, s.E,
+                                                s.K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_scatter(const DevState& s, const uint16_t* x, int T, cudaStream_t st)
+{
+    const long long warps = (long long)T * (s.H / 128);
+    k_quant_scatter<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(x, s.prow, s.aq, s.asf, T, s.H, s.K);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStream_t st, int* nlaunch)

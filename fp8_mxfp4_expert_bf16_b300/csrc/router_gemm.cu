@@ -62,15 +62,20 @@ __device__ __forceinline__ void router_fail(RouterCtl* ctl, int32_t* err, int wh
     *(volatile int*)&ctl->abort = 1;
 }
 
+// Split-K (blockIdx.z, small batches): each CTA sums `KB` of the K-steps
+// starting at z * KB and stores raw partial products to part[z][t][e]; the
+// top-k kernel adds the partials in split order plus the logit bias.
 __global__ void __launch_bounds__(128, 1)
     k_router_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                const float* __restrict__ lb, float* __restrict__ logits, int T, int E, int KB, int N, int32_t* err)
+                const float* __restrict__ lb, float* __restrict__ logits, float* __restrict__ part, int T, int E,
+                int KB, int N, int32_t* err)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     RouterCtl* ctl = reinterpret_cast<RouterCtl*>(smem + kRBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x, nt = blockIdx.y;
+    const int kb0 = blockIdx.z * KB;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRStages; ++s) {
@@ -106,8 +111,8 @@ __global__ void __launch_bounds__(128, 1)
             uint8_t* st = smem + s * kRStageStride;
             const uint32_t fb = smem_u32(&ctl->full[s]);
             mbar_arrive_expect_tx(fb, tx);
-            tma_load_2d(smem_u32(st), &tmX, fb, kb * 64, mt * 128);
-            tma_load_2d(smem_u32(st + kRABytes), &tmW, fb, kb * 64, nt * N);
+            tma_load_2d(smem_u32(st), &tmX, fb, (kb0 + kb) * 64, mt * 128);
+            tma_load_2d(smem_u32(st + kRABytes), &tmW, fb, (kb0 + kb) * 64, nt * N);
             last = kb;
         }
         // every copy started here has landed before the CTA may exit
@@ -155,7 +160,10 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int e = nt * N + 16 * c + j;
-                    if (e < E) logits[(size_t)t * E + e] = __uint_as_float(v[j]) + lb[e];
+                    if (e < E) {
+                        if (part) part[((size_t)blockIdx.z * T + t) * E + e] = __uint_as_float(v[j]);
+                        else logits[(size_t)t * E + e] = __uint_as_float(v[j]) + lb[e];
+                    }
                 }
             }
         }
@@ -177,12 +185,24 @@ cudaError_t router_set_attributes()
 
 int router_tile_n(int T) { return T <= 512 ? 64 : 128; }
 
-cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, cudaStream_t st)
+// Split factor for a batch of T tokens: up to kRouterMaxSplit, at least 4
+// K-steps (of 64) per split, dividing the K-steps evenly; 1 for large T.
+int router_split(int T, int H)
+{
+    if (T > kRouterSplitMaxT) return 1;
+    const int KB = H / 64;
+    int S = kRouterMaxSplit;
+    while (S > 1 && (KB % S != 0 || KB / S < 4)) S >>= 1;
+    return S;
+}
+
+cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, cudaStream_t st, int ksplit)
 {
     const int N = router_tile_n(T);
-    dim3 grid((T + 127) / 128, (s.E + N - 1) / N);
-    k_router_tc<<<grid, 128, kRSmemBytes, st>>>(tmX, N == 64 ? s.tm_wr64 : s.tm_wr128, s.lb, s.logits, T, s.E,
-                                                s.H / 64, N, s.err);
+    dim3 grid((T + 127) / 128, (s.E + N - 1) / N, ksplit);
+    k_router_tc<<<grid, 128, kRSmemBytes, st>>>(tmX, N == 64 ? s.tm_wr64 : s.tm_wr128, s.lb, s.logits,
+                                                ksplit > 1 ? s.logit_part : nullptr, T, s.E, s.H / 64 / ksplit, N,
+                                                s.err);
     return cudaGetLastError();
 }
 
