@@ -23,9 +23,11 @@
 //   warp 1      TMEM owner and MMA issuer: copies the scale chunks into
 //               TMEM (tcgen05.cp) and issues 4 block-scaled 128x256x32 MMAs
 //               per stage into one fp32 accumulator in TMEM;
-//   warps 2-5   epilogue: TMEM -> registers; gate/up: h = silu(g) * u and
-//               re-quantisation of h to e4m3 per 1 x 128 block; down: fp32
-//               rows to the expert-output buffer.
+//   warps 2-9   epilogue (two warps per TMEM lane quarter, each half of the
+//               columns): TMEM -> registers; gate/up: h = silu(g) * u and
+//               re-quantisation of h to e4m3 per 1 x 128 block (the two
+//               warps of a row combine their amax through shared memory);
+//               down: fp32 rows to the expert-output buffer.
 // All waits are bounded in time; a wait that gives up writes an error word,
 // raises a CTA-wide abort flag, and the CTA drains its copies / MMAs and
 // frees TMEM before exiting.
@@ -56,7 +58,7 @@ struct Shape {
     static constexpr int kSFBOff = kSFAOff + 512;
     static constexpr int kStageStride = ((kSFBOff + 1024 + 1023) / 1024) * 1024;
     static constexpr int kBarOff = kStages * kStageStride;
-    static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+    static constexpr int kSmemBytes = kBarOff + 2048 + 1024;
 };
 static_assert(Shape<false>::kSmemBytes <= 232448 && Shape<true>::kSmemBytes <= 232448, "shared memory");
 // A 128 x 128 E2M1 box occupies 16 KB of shared memory (each 8 bytes of
@@ -66,6 +68,8 @@ constexpr uint32_t kBHalfTxBytes = 128 * 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;      // accumulator: 256 fp32 columns
 constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), SFB at +8 (8 cols)
+constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
+constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, epilogue warps
 // k-steps of weights the L2 prefetch stream runs ahead of the TMA ring
 constexpr int kPrefetchGateUp = 8;
 constexpr int kPrefetchDown = 8;
@@ -99,8 +103,10 @@ struct SmemCtl {
     uint64_t acc_full;
     uint64_t acc_empty;
     uint64_t drain;
+    uint64_t red_full[2];
     uint32_t tmem_base;
     int abort;
+    float red[2][8][32];          // per-warp row amax halves, double-buffered by tile parity
 };
 
 template <class Ctl>
@@ -132,7 +138,7 @@ __device__ __forceinline__ int act_block_exponent(float amax)
 }
 
 template <int kMode, bool kLight>   // mode 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     k_mx_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
               const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmW, const GemmArgs args)
 {
@@ -150,7 +156,9 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
         mbar_init(smem_u32(&ctl->acc_full), 1);
-        mbar_init(smem_u32(&ctl->acc_empty), 4);
+        mbar_init(smem_u32(&ctl->acc_empty), kEpiWarps);
+        mbar_init(smem_u32(&ctl->red_full[0]), kEpiWarps);
+        mbar_init(smem_u32(&ctl->red_full[1]), kEpiWarps);
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort = 0;
         fence_mbar_init();
@@ -296,7 +304,12 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue
+        // Eight warps, two per TMEM lane quarter: warp pair (q, q + 4) shares
+        // rows 32q .. 32q+31 and splits the columns, which halves the time the
+        // accumulator is held before the next tile's MMAs may start.
+        const int ew = warp - 2;                      // 0..7
         const int q = warp & 3;                       // this warp's TMEM lane quarter
+        const int hw = ew >> 2;                       // which half of the columns
         const int row = q * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         int tcount = 0;
@@ -314,13 +327,14 @@ __global__ void __launch_bounds__(192, 1)
             const bool warp_live = q * 32 < rows;
             const bool row_live = row < rows;
             if (kMode == 0) {
-                float h[128];
+                // this warp: middle columns [64 hw, 64 hw + 64) of the tile's 128
+                float h[64];
                 if (warp_live) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < 4; ++c) {
                         uint32_t g[16], u[16];
-                        tmem_ld16(tl + kAccCol + 16u * c, g);
-                        tmem_ld16(tl + kAccCol + 128u + 16u * c, u);
+                        tmem_ld16(tl + kAccCol + 64u * hw + 16u * c, g);
+                        tmem_ld16(tl + kAccCol + 128u + 64u * hw + 16u * c, u);
                         tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -332,19 +346,33 @@ __global__ void __launch_bounds__(192, 1)
                             h[16 * c + j] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
                         }
                     }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) h[j] = 0.0f;
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty));
-                if (row_live) {
-                    float amax = 0.f;
+                // the row's amax over all 128 columns: combine with the partner warp
+                float amax = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 128; ++j) amax = fmaxf(amax, fabsf(h[j]));
+                for (int j = 0; j < 64; ++j) amax = fmaxf(amax, fabsf(h[j]));
+                const int p = tcount & 1;
+                ctl->red[p][ew][lane] = amax;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ctl->red_full[p]));
+                if (!mbar_wait(smem_u32(&ctl->red_full[p]), (uint32_t)(tcount >> 1) & 1u, abrt)) {
+                    raise_error(ctl, args.err, 7);
+                    break;
+                }
+                amax = fmaxf(amax, ctl->red[p][ew ^ 4][lane]);
+                if (row_live) {
                     const int ex = act_block_exponent(amax);
                     const float inv = __int_as_float((127 - ex) << 23);
-                    uint4* dst = reinterpret_cast<uint4*>(args.hq + (size_t)(mt * kBM + row) * args.I + nt * 128);
+                    uint4* dst =
+                        reinterpret_cast<uint4*>(args.hq + (size_t)(mt * kBM + row) * args.I + nt * 128 + 64 * hw);
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
+                    for (int v = 0; v < 4; ++v) {
                         uint4 w;
                         w.x = e4m3x4(h[16 * v + 0] * inv, h[16 * v + 1] * inv, h[16 * v + 2] * inv, h[16 * v + 3] * inv);
                         w.y = e4m3x4(h[16 * v + 4] * inv, h[16 * v + 5] * inv, h[16 * v + 6] * inv, h[16 * v + 7] * inv);
@@ -352,15 +380,17 @@ __global__ void __launch_bounds__(192, 1)
                         w.w = e4m3x4(h[16 * v + 12] * inv, h[16 * v + 13] * inv, h[16 * v + 14] * inv, h[16 * v + 15] * inv);
                         dst[v] = w;
                     }
-                    args.hsf[sf_word_index(mt, nt, args.I / 128, row)] = (uint32_t)(ex + 127) * 0x01010101u;
+                    if (hw == 0)
+                        args.hsf[sf_word_index(mt, nt, args.I / 128, row)] = (uint32_t)(ex + 127) * 0x01010101u;
                 }
             } else {
-                const int ncols = 128 * args.halves;
-                float* dst = args.obuf + (size_t)(mt * kBM + row) * args.H + (size_t)nt * ncols;
+                // this warp: output columns [hw * ncols / 2, (hw + 1) * ncols / 2)
+                const int ncols = 128 * args.halves, half_cols = ncols / 2;
+                float* dst = args.obuf + (size_t)(mt * kBM + row) * args.H + (size_t)nt * ncols + hw * half_cols;
                 if (warp_live) {
-                    for (int c = 0; c < ncols / 16; ++c) {
+                    for (int c = 0; c < half_cols / 16; ++c) {
                         uint32_t v[16];
-                        tmem_ld16(tl + kAccCol + 16u * c, v);
+                        tmem_ld16(tl + kAccCol + (uint32_t)(hw * half_cols) + 16u * c, v);
                         tmem_ld_wait();
                         if (row_live) {
                             float4* d4 = reinterpret_cast<float4*>(dst + 16 * c);
@@ -445,11 +475,11 @@ cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
     a.list = s.light_list;
     a.list_count = s.n_mtiles + 1;
     a.box_rows[0] = 8, a.box_rows[1] = 16, a.box_rows[2] = 32;
-    k_mx_gemm<0, true><<<s.num_sms, 192, Shape<true>::kSmemBytes, st>>>(s.tm_aq[0], s.tm_aq[1], s.tm_aq[2], s.tm_w13, a);
+    k_mx_gemm<0, true><<<s.num_sms, kThreads, Shape<true>::kSmemBytes, st>>>(s.tm_aq[0], s.tm_aq[1], s.tm_aq[2], s.tm_w13, a);
     a.list = s.heavy_list;
     a.list_count = s.n_mtiles + 2;
     a.box_rows[0] = 32, a.box_rows[1] = 64, a.box_rows[2] = 128;
-    k_mx_gemm<0, false><<<s.num_sms, 192, Shape<false>::kSmemBytes, st>>>(s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13,
+    k_mx_gemm<0, false><<<s.num_sms, kThreads, Shape<false>::kSmemBytes, st>>>(s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13,
                                                                            a);
     return cudaGetLastError();
 }
@@ -460,11 +490,11 @@ cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
     a.list = s.light_list;
     a.list_count = s.n_mtiles + 1;
     a.box_rows[0] = 8, a.box_rows[1] = 16, a.box_rows[2] = 32;
-    k_mx_gemm<1, true><<<s.num_sms, 192, Shape<true>::kSmemBytes, st>>>(s.tm_hq[0], s.tm_hq[1], s.tm_hq[2], s.tm_w2, a);
+    k_mx_gemm<1, true><<<s.num_sms, kThreads, Shape<true>::kSmemBytes, st>>>(s.tm_hq[0], s.tm_hq[1], s.tm_hq[2], s.tm_w2, a);
     a.list = s.heavy_list;
     a.list_count = s.n_mtiles + 2;
     a.box_rows[0] = 32, a.box_rows[1] = 64, a.box_rows[2] = 128;
-    k_mx_gemm<1, false><<<s.num_sms, 192, Shape<false>::kSmemBytes, st>>>(s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2,
+    k_mx_gemm<1, false><<<s.num_sms, kThreads, Shape<false>::kSmemBytes, st>>>(s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2,
                                                                            a);
     return cudaGetLastError();
 }

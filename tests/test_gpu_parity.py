@@ -110,3 +110,29 @@ def test_full_size_workloads_sampled(name):
     print(name, stats)
     from parity import bf16_f64
     assert np.isfinite(bf16_f64(y)).all()
+
+
+def test_forward_captures_in_a_cuda_graph():
+    """moe_forward enqueues kernels only (no sync, no readback): it can be
+    captured in a CUDA graph, and replays give the eager result."""
+    import torch
+    inp = synth.make_inputs("toy")
+    layer = make_layer(inp)
+    y_eager = run_layer(layer, inp)
+    x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).cuda()
+    y = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(x, y, s)      # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(x, y)
+    y.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    layer.check_device_error()
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), y_eager)
