@@ -16,7 +16,7 @@ import numpy as np
 
 from .build import LIB as _LIB_PATH, build as _build
 
-__all__ = ["MoELayer", "MoEError", "lib", "declared_symbols", "STAGES", "route_noalloc"]
+__all__ = ["MoELayer", "MoEError", "lib", "declared_symbols", "STAGES", "route_noalloc", "mxfp4_quantize"]
 
 _HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_mx.h")
 
@@ -78,6 +78,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_last_error": (ctypes.c_char_p, [P]),
         "moe_status_string": (ctypes.c_char_p, [I]),
         "moe_route_noalloc": (S, [P, I, I, P, P, P, I, I, I, P, P, P]),
+        "moe_mxfp4_quantize": (S, [P, ctypes.c_size_t, I, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -258,3 +259,16 @@ def route_noalloc(x, router_w, logit_bias, sel_bias, k, score_func=0, ids=None, 
     if st != 0:
         raise MoEError(st, L.moe_last_error(None).decode())
     return ids, gates
+
+
+def mxfp4_quantize(w, stream=None):
+    """fp32 cuda tensor [rows, K] -> (packed uint8 [rows, K/2], scales uint8 [rows, K/32]) on the device."""
+    import torch
+    L = lib()
+    rows, K = w.shape
+    packed = torch.empty((rows, K // 2), dtype=torch.uint8, device=w.device)
+    scales = torch.empty((rows, K // 32), dtype=torch.uint8, device=w.device)
+    st = L.moe_mxfp4_quantize(_ptr(w), rows, K, _ptr(packed), _ptr(scales), MoELayer._stream(stream))
+    if st != 0:
+        raise MoEError(st, L.moe_last_error(None).decode())
+    return packed, scales

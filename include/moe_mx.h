@@ -158,6 +158,22 @@ int moe_last_launch_count(moe_handle* h);
 const char* moe_last_error(moe_handle* h);
 const char* moe_status_string(moe_status s);
 
+/* MXFP4 quantisation of fp32 weights on the device: the weight format of
+ * "MiMo V2.6 Pro and Flash architecture teardown", section "Why Are the
+ * V2.6 Files Half the Size of V2.5?" (two E2M1 values per byte, one E8M0
+ * scale per 32 values), which the page says the experts were re-rounded to
+ * after every RL update.  OCP Microscaling v1.0 rule per 32 consecutive
+ * values of a row: X = floor(log2(amax)) - 2 clamped to [-127, 127], scale
+ * byte X + 127 (127 for an all-zero block), code = nearest E2M1 value of
+ * v / 2^X with ties to the even code, saturating at 6.
+ *   w       fp32 [rows][K] device, finite values, 16-byte aligned
+ *   packed  u8 [rows][K/2] device output, element 2i in the low nibble
+ *   scales  u8 [rows][K/32] device output
+ * K must be a positive multiple of 32.  Enqueued on `stream` (current
+ * device); errors through moe_last_error(NULL).  The output is the
+ * w13_q / w13_s (or w2_q / w2_s) input of moe_load_weights. */
+moe_status moe_mxfp4_quantize(const float* w, size_t rows, int K, uint8_t* packed, uint8_t* scales, void* stream);
+
 /* Routing that allocates no device memory (the pages have no counterpart of
  * this entry point; it serves callers that cannot allocate on their call
  * path: code whose device memory belongs to its own allocator or budget, and
