@@ -291,7 +291,6 @@ def run_gpu(args, cfg):
 
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    layer.set_profiling(True)
     with ClockSampler(device) as clk:
         barrier()
         clk.mark(True)
@@ -303,9 +302,26 @@ def run_gpu(args, cfg):
         barrier()
         clk.mark(False)
     ms_total = ev0.elapsed_time(ev1)
-    stage = layer.stage_times()       # averages over the last <= 64 timed forwards
-    layer.set_profiling(False)
     launches = layer.launch_count() * args.steps
+    layer.check_device_error()
+
+    # Kernel durations: the same K forwards once more, with the library's CUDA
+    # events recorded between the kernels on the forward's stream.  The events
+    # stop consecutive kernels from overlapping (programmatic dependent
+    # launch), so this window is timed separately from the one above.
+    ev2 = torch.cuda.Event(enable_timing=True)
+    ev3 = torch.cuda.Event(enable_timing=True)
+    layer.set_profiling(True)
+    barrier()
+    with torch.cuda.stream(stream):
+        ev2.record(stream)
+        for _ in range(args.steps):
+            layer.forward(x, y, stream)
+        ev3.record(stream)
+    barrier()
+    ms_profiled = ev2.elapsed_time(ev3) / args.steps
+    stage = layer.stage_times()       # averages over the last <= 64 forwards of that window
+    layer.set_profiling(False)
     layer.check_device_error()
 
     t_local = torch.tensor([ms_total], dtype=torch.float64, device=f"cuda:{device}")
@@ -366,6 +382,9 @@ def run_gpu(args, cfg):
                                                   "weights from HBM"),
             "roofline": roof,
             "stage_ms": stage,
+            "stage_window": {"ms_per_step": ms_profiled,
+                             "how": "a second window of the same K forwards with CUDA events between the kernels "
+                                    "on the forward's stream (stage_ms and the roofline's kernel time come from it)"},
             "routing": {"active_experts": active, "rows": rows, "max_count": int(counts.max()),
                         "min_count": int(counts.min())},
             "cpu_baseline": cpu,

@@ -405,11 +405,11 @@ moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, voi
         CUDA_TRY(h, launch_dispatch(s, x, T, st, &n));
     }
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[3], st));
-    CUDA_TRY(h, launch_gemm1(s, st));   // light then heavy m-tiles
-    n += 2;
+    CUDA_TRY(h, launch_gemm1(s, st));   // light then heavy m-tiles, one launch
+    ++n;
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[4], st));
     CUDA_TRY(h, launch_gemm2(s, st));
-    n += 2;
+    ++n;
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[5], st));
     CUDA_TRY(h, launch_combine(s, y, T, st));
     ++n;

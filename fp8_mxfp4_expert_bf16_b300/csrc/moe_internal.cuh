@@ -12,9 +12,9 @@ constexpr int kChunk = 256;         // tokens per dispatch chunk
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 8;
 constexpr int kNumABox = 5;         // activation tile maps with 8 / 16 / 32 / 64 / 128 rows
-constexpr int kWBlockRowsPerHalf = 136;
+constexpr int kWBlockRowsPerHalf = 136;   // interleaved weight block: 128 weight rows + 8 scale rows of 64 B
 constexpr int kRouterMaxSplit = 16;       // split-K factor of the router for small batches
-constexpr int kRouterSplitMaxT = 512;     // batches up to this size use the split-K router   // interleaved weight block: 128 weight rows + 8 scale rows of 64 B
+constexpr int kRouterSplitMaxT = 512;     // batches up to this size use the split-K router
 constexpr int kLightRows = 32;      // m-tiles with at most this many rows use the light GEMM shape
 
 // Error word codes written by kernels (first writer wins).
@@ -66,7 +66,28 @@ struct DevState {
     CUtensorMap tm_aq[kNumABox], tm_hq[kNumABox], tm_w13, tm_w2;
     CUtensorMap tm_wr64, tm_wr128;   // router weights, 64 / 128-row boxes
     int num_sms;
+    bool pdl = true;     // launch the forward's kernels with programmatic stream serialisation
 };
+
+// Launch `kernel` on `st`; with `pdl` the launch may begin while the previous
+// kernel on the stream is still running (the kernel itself waits, with
+// griddep_wait, before it touches what that kernel writes).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                          Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 // Word index of row r of m-tile mt, K-block kb, in a scale-factor buffer laid
 // out for tcgen05.cp .32x128b.warpx4: per (mt, kb) 128 words, row r at word
@@ -78,7 +99,6 @@ __host__ __device__ __forceinline__ size_t sf_word_index(int mt, int kb, int KB,
 }
 
 // launchers (route.cu)
-cudaError_t launch_router(const DevState& s, const uint16_t* x, int T, cudaStream_t st);
 cudaError_t launch_topk(const DevState& s, int T, cudaStream_t st, int ksplit = 1);
 cudaError_t launch_dispatch_small(const DevState& s, int T, cudaStream_t st);
 cudaError_t launch_quant_scatter(const DevState& s, const uint16_t* x, int T, cudaStream_t st);

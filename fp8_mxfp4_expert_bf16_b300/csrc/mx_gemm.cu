@@ -9,8 +9,10 @@
 // recipe "XiaomiMiMo/MiMo-V2.6-Pro-RL", "Overview" (computed as block-wise
 // FP8 e4m3).
 //
-// One persistent CTA per SM walks a static list of (m-tile, n-tile) tiles.
-// An m-tile is 128 consecutive padded rows of one expert; an n-tile is 256
+// One persistent CTA per SM walks two static lists of (m-tile, n-tile)
+// tiles: first the light m-tiles (at most 32 valid rows), then the heavy
+// ones, each phase with the shared-memory ring shape that suits it.  An
+// m-tile is 128 consecutive padded rows of one expert; an n-tile is 256
 // weight rows (gate 128 + up 128 of one 128-wide slice of the expert's
 // middle for the gate/up GEMM; 256 output features for the down GEMM).
 // Warp roles:
@@ -28,6 +30,11 @@
 //               re-quantisation of h to e4m3 per 1 x 128 block (the two
 //               warps of a row combine their amax through shared memory);
 //               down: fp32 rows to the expert-output buffer.
+// Programmatic dependent launch: the kernel may start while the previous
+// kernel of the forward (which writes the activations) is still running.
+// Before waiting for it, the producer streams what does not depend on it:
+// the weight tiles of the first ring stages and an L2 prefetch of the
+// following ones.  Only then does it wait and load the activation tiles.
 // All waits are bounded in time; a wait that gives up writes an error word,
 // raises a CTA-wide abort flag, and the CTA drains its copies / MMAs and
 // frees TMEM before exiting.
@@ -41,7 +48,7 @@
 
 namespace moe {
 
-// Two shapes of the same kernel:
+// The two ring shapes (one kernel runs both phases in turn):
 //  heavy (m-tiles with more than 32 valid rows): 128-row activation slot,
 //    4-stage ring;
 //  light (at most 32 valid rows: decode, and an expert's last m-tile): the
@@ -57,10 +64,13 @@ struct Shape {
     static constexpr int kSFAOff = kBOff + 2 * 128 * 128;     // weight tile: 256 rows x 128 B (16-byte slots)
     static constexpr int kSFBOff = kSFAOff + 512;
     static constexpr int kStageStride = ((kSFBOff + 1024 + 1023) / 1024) * 1024;
-    static constexpr int kBarOff = kStages * kStageStride;
-    static constexpr int kSmemBytes = kBarOff + 2048 + 1024;
+    static constexpr int kRingBytes = kStages * kStageStride;
+    // activation box heights of the phase's three activation maps
+    static constexpr int kBox0 = kLight ? 8 : 32, kBox1 = kLight ? 16 : 64, kBox2 = kLight ? 32 : 128;
 };
-static_assert(Shape<false>::kSmemBytes <= 232448 && Shape<true>::kSmemBytes <= 232448, "shared memory");
+constexpr int kRingBytes =
+    Shape<true>::kRingBytes > Shape<false>::kRingBytes ? Shape<true>::kRingBytes : Shape<false>::kRingBytes;
+
 // A 128 x 128 E2M1 box occupies 16 KB of shared memory (each 8 bytes of
 // packed codes followed by an 8-byte gap) but completes only the 8 KB it
 // reads from global memory on the barrier's transaction count.
@@ -78,10 +88,11 @@ struct GemmArgs {
     const uint32_t* sfa;         // activation scale words [MT][KB][128]
     const int32_t* mtile_expert;
     const int32_t* mtile_rows;
-    const int32_t* list;         // the m-tiles this kernel processes
-    const int32_t* list_count;   // their number
+    const int32_t* light_list;   // m-tiles of the light phase, and their number
+    const int32_t* light_count;
+    const int32_t* heavy_list;   // m-tiles of the heavy phase, and their number
+    const int32_t* heavy_count;
     const uint8_t* wq;           // interleaved tile-major blocks [E][NT][KB]: halves*128 weight rows, halves*8 scale rows
-    int box_rows[3];             // activation box heights of the three activation maps
     int KB;                      // K / 128
     int NT;                      // n-tiles per m-tile
     int halves;                  // n-tile width / 128 (2, or 1 for a 128-wide down GEMM tile)
@@ -97,26 +108,46 @@ struct GemmArgs {
 };
 
 template <int kStages>
-struct SmemCtl {
+struct PhaseCtl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t acc_full;
     uint64_t acc_empty;
     uint64_t drain;
     uint64_t red_full[2];
-    uint32_t tmem_base;
-    int abort;
     float red[2][8][32];          // per-warp row amax halves, double-buffered by tile parity
 };
 
-template <class Ctl>
-__device__ __forceinline__ void raise_error(Ctl* ctl, int32_t* err, int where)
+struct GemmCtl {
+    PhaseCtl<Shape<true>::kStages> light;
+    PhaseCtl<Shape<false>::kStages> heavy;
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr int kSmemBytes = kRingBytes + (int)sizeof(GemmCtl) + 1024;   // + alignment of the ring to 1 KB
+static_assert(kSmemBytes <= 232448, "shared memory");
+
+__device__ __forceinline__ void raise_error(GemmCtl* g, int32_t* err, int where)
 {
     if (atomicCAS(err, 0, kDevErrTimeout) == 0) {
         err[1] = where;
         err[2] = blockIdx.x;
     }
-    *(volatile int*)&ctl->abort = 1;
+    *(volatile int*)&g->abort = 1;
+}
+
+template <int kStages>
+__device__ __forceinline__ void init_phase(PhaseCtl<kStages>& pc)
+{
+    for (int s = 0; s < kStages; ++s) {
+        mbar_init(smem_u32(&pc.full[s]), 1);
+        mbar_init(smem_u32(&pc.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&pc.acc_full), 1);
+    mbar_init(smem_u32(&pc.acc_empty), kEpiWarps);
+    mbar_init(smem_u32(&pc.red_full[0]), kEpiWarps);
+    mbar_init(smem_u32(&pc.red_full[1]), kEpiWarps);
+    mbar_init(smem_u32(&pc.drain), 1);
 }
 
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
@@ -137,51 +168,46 @@ __device__ __forceinline__ int act_block_exponent(float amax)
     return max(-127, min(127, e));
 }
 
-template <int kMode, bool kLight>   // mode 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows
-__global__ void __launch_bounds__(kThreads, 1)
-    k_mx_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-              const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmW, const GemmArgs args)
+// The producer's wait for the previous kernel of the forward (done once per
+// CTA, before the first activation load).  Tile lists and weights are read
+// before it: the lists come from the dispatch kernel, which had completed
+// before the previous kernel passed its own wait and allowed this one to
+// start.  The gate/up GEMM then lets the next kernel (the down GEMM) be
+// scheduled at once, so that its CTAs take over SMs as this kernel's CTAs
+// finish and stream their first weights meanwhile; the down GEMM lets its
+// successor (the combine, which has nothing to do before its own wait) be
+// scheduled only near the end of each CTA's work, so that waiting combine
+// blocks do not sit beside running GEMM CTAs.
+template <int kMode>
+__device__ __forceinline__ void producer_wait_once(bool& waited)
+{
+    if (!waited) {
+        griddep_wait();
+        if (kMode == 0) griddep_launch_dependents();
+        waited = true;
+    }
+}
+
+// One phase (the light or the heavy m-tile list) of the grouped GEMM.  Every
+// role drains its own work before returning: the producer waits until its
+// copies have landed, the MMA issuer until its MMAs have completed, the
+// epilogue has read its last accumulator.
+template <int kMode, bool kLight>
+__device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<Shape<kLight>::kStages>& pc,
+                                           uint32_t tmem, const CUtensorMap* tmA0, const CUtensorMap* tmA1,
+                                           const CUtensorMap* tmA2, const CUtensorMap* tmW, const GemmArgs& args,
+                                           const int32_t* list, int count, bool& waited)
 {
     using S = Shape<kLight>;
-    constexpr int kStages = S::kStages, kABytes = S::kABytes, kStageStride = S::kStageStride;
+    constexpr int kStages = S::kStages, kStageStride = S::kStageStride;
     constexpr int kSFAOff = S::kSFAOff, kSFBOff = S::kSFBOff;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    auto* ctl = reinterpret_cast<SmemCtl<kStages>*>(smem + S::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&ctl->full[s]), 1);
-            mbar_init(smem_u32(&ctl->empty[s]), 1);
-        }
-        mbar_init(smem_u32(&ctl->acc_full), 1);
-        mbar_init(smem_u32(&ctl->acc_empty), kEpiWarps);
-        mbar_init(smem_u32(&ctl->red_full[0]), kEpiWarps);
-        mbar_init(smem_u32(&ctl->red_full[1]), kEpiWarps);
-        mbar_init(smem_u32(&ctl->drain), 1);
-        ctl->abort = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&tmA0);
-        tma_prefetch_desc(&tmA1);
-        tma_prefetch_desc(&tmA2);
-        tma_prefetch_desc(&tmW);
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = ctl->tmem_base;
-    const volatile int* abrt = &ctl->abort;
-
+    const volatile int* abrt = &g->abort;
     const int NT = args.NT, KB = args.KB;
-    const int total = (*args.list_count) * NT;
+    const int total = count * NT;
 
     if (warp == 0) {
-        if (lane == 0) {
+        if (lane == 0 && (int)blockIdx.x < total) {
             // ------------------------------------------------ TMA producer
             uint32_t last_phase[kStages];
             bool issued[kStages];
@@ -189,9 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Tile metadata (m-tile, expert, valid rows) is loaded ahead so the
             // global-load latency never sits between two TMA issues.
             const int stride = gridDim.x;
-            auto load_mt = [&](int tile) { return tile < total ? args.list[tile / NT] : 0; };
+            auto load_mt = [&](int tile) { return tile < total ? list[tile / NT] : 0; };
             // L2 prefetch stream: the same (tile, k-step) sequence as the ring,
-            // args.prefetch k-steps ahead, for the weight boxes and their scales
+            // for the weight boxes and their scales
+            // (one prefetch per stage loaded, so it stays args.prefetch k-steps ahead)
             int pf_tile = blockIdx.x, pf_kb = 0;
             int pf_e = args.mtile_expert[load_mt(pf_tile)];
             int pf_mt_next = load_mt(pf_tile + stride);
@@ -208,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             for (int i = 0; i < args.prefetch; ++i) prefetch_next();
-            int it = 0;
+            int it = 0, pre = 0;
             bool ok = true;
             int cur_mt = load_mt(blockIdx.x);
             int cur_e = args.mtile_expert[cur_mt], cur_rows = args.mtile_rows[cur_mt];
@@ -222,29 +249,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cur_rows = args.mtile_rows[cur_mt];
                 nxt_mt = load_mt(tile + 2 * stride);
                 // activation box: the smallest of the three heights that covers the valid rows
-                const int sel = rows <= args.box_rows[0] ? 0 : (rows <= args.box_rows[1] ? 1 : 2);
-                const CUtensorMap* tA = sel == 0 ? &tmA0 : (sel == 1 ? &tmA1 : &tmA2);
-                const uint32_t a_bytes =
-                    (uint32_t)(sel == 0 ? args.box_rows[0] : (sel == 1 ? args.box_rows[1] : args.box_rows[2])) * 128u;
+                const int sel = rows <= S::kBox0 ? 0 : (rows <= S::kBox1 ? 1 : 2);
+                const CUtensorMap* tA = sel == 0 ? tmA0 : (sel == 1 ? tmA1 : tmA2);
+                const uint32_t a_bytes = (uint32_t)(sel == 0 ? S::kBox0 : (sel == 1 ? S::kBox1 : S::kBox2)) * 128u;
                 const uint32_t tx = a_bytes + args.halves * (kBHalfTxBytes + 512) + 512;
                 // first row of this tile's interleaved weight blocks
                 const size_t wrow0 = ((size_t)(e * NT + nt) * KB) * args.halves * kWBlockRowsPerHalf;
                 const uint32_t* sfa = args.sfa + (size_t)mt * KB * 128;
+                if (!waited) {
+                    // Before the wait: the weight tile and its scales for the
+                    // first ring stages (free at the start of a phase), each
+                    // barrier armed with the stage's full byte count.
+                    pre = KB < kStages ? KB : kStages;
+                    for (int kb = 0; kb < pre; ++kb) {
+                        uint8_t* st = smem + kb * kStageStride;
+                        const uint32_t fb = smem_u32(&pc.full[kb]);
+                        mbar_arrive_expect_tx(fb, tx);
+                        const size_t wrow = wrow0 + (size_t)kb * args.halves * kWBlockRowsPerHalf;
+                        tma_load_2d(smem_u32(st + S::kBOff), tmW, fb, 0, (int)wrow);
+                        bulk_load(smem_u32(st + kSFBOff), args.wq + (wrow + (size_t)args.halves * 128) * 64,
+                                  args.halves * 512, fb);
+                        issued[kb] = true;
+                        last_phase[kb] = 0;
+                        prefetch_next();
+                    }
+                    producer_wait_once<kMode>(waited);
+                    for (int kb = 0; kb < pre; ++kb) {
+                        uint8_t* st = smem + kb * kStageStride;
+                        const uint32_t fb = smem_u32(&pc.full[kb]);
+                        tma_load_2d(smem_u32(st), tA, fb, kb * kBK, mt * kBM);
+                        bulk_load(smem_u32(st + kSFAOff), sfa + (size_t)kb * 128, 512, fb);
+                    }
+                }
                 for (int kb = 0; kb < KB; ++kb, ++it) {
+                    if (it < pre) continue;   // issued before the wait
                     const int s = it % kStages;
                     const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                    if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abrt)) {
-                        raise_error(ctl, args.err, 1);
+                    if (!mbar_wait(smem_u32(&pc.empty[s]), ph ^ 1u, abrt)) {
+                        raise_error(g, args.err, 1);
                         ok = false;
                         break;
                     }
                     uint8_t* st = smem + s * kStageStride;
-                    const uint32_t fb = smem_u32(&ctl->full[s]);
+                    const uint32_t fb = smem_u32(&pc.full[s]);
                     mbar_arrive_expect_tx(fb, tx);
                     tma_load_2d(smem_u32(st), tA, fb, kb * kBK, mt * kBM);
                     // the stage's weight rows (both halves) are one box; its scale chunks follow them
                     const size_t wrow = wrow0 + (size_t)kb * args.halves * kWBlockRowsPerHalf;
-                    tma_load_2d(smem_u32(st + S::kBOff), &tmW, fb, 0, (int)wrow);
+                    tma_load_2d(smem_u32(st + S::kBOff), tmW, fb, 0, (int)wrow);
                     bulk_load(smem_u32(st + kSFAOff), sfa + (size_t)kb * 128, 512, fb);
                     bulk_load(smem_u32(st + kSFBOff), args.wq + (wrow + (size_t)args.halves * 128) * 64,
                               args.halves * 512, fb);
@@ -253,11 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     prefetch_next();
                 }
             }
-            // wait for every copy this thread started before the CTA may exit
+            // wait for every copy this thread started before the ring is reused
             int zero = 0;
             for (int s = 0; s < kStages; ++s)
-                if (issued[s] && !mbar_wait(smem_u32(&ctl->full[s]), last_phase[s], &zero))
-                    raise_error(ctl, args.err, 2);
+                if (issued[s] && !mbar_wait(smem_u32(&pc.full[s]), last_phase[s], &zero))
+                    raise_error(g, args.err, 2);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -266,16 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0, tcount = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
-                if (tcount > 0 && !mbar_wait(smem_u32(&ctl->acc_empty), (uint32_t)(tcount - 1) & 1u, abrt)) {
-                    raise_error(ctl, args.err, 3);
+                if (tcount > 0 && !mbar_wait(smem_u32(&pc.acc_empty), (uint32_t)(tcount - 1) & 1u, abrt)) {
+                    raise_error(g, args.err, 3);
                     break;
                 }
                 tc_fence_after();
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                    if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abrt)) {
-                        raise_error(ctl, args.err, 4);
+                    if (!mbar_wait(smem_u32(&pc.full[s]), ph, abrt)) {
+                        raise_error(g, args.err, 4);
                         ok = false;
                         break;
                     }
@@ -293,14 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_mxf8f6f4(tmem + kAccCol, ad, bd, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
                                      (kb | k) != 0 ? 1u : 0u);
                     }
-                    tc_commit(smem_u32(&ctl->empty[s]));
+                    tc_commit(smem_u32(&pc.empty[s]));
                 }
-                if (ok) tc_commit(smem_u32(&ctl->acc_full));
+                if (ok) tc_commit(smem_u32(&pc.acc_full));
             }
-            // all MMAs of this thread complete before TMEM is released
+            // all MMAs of this thread complete before the ring or TMEM is reused
             int zero = 0;
-            tc_commit(smem_u32(&ctl->drain));
-            if (!mbar_wait(smem_u32(&ctl->drain), 0u, &zero)) raise_error(ctl, args.err, 5);
+            tc_commit(smem_u32(&pc.drain));
+            if (!mbar_wait(smem_u32(&pc.drain), 0u, &zero)) raise_error(g, args.err, 5);
         }
     } else {
         // ---------------------------------------------------- epilogue
@@ -314,10 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         int tcount = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tcount) {
-            const int mt = args.list[tile / NT], nt = tile - (tile / NT) * NT;
+            const int mt = list[tile / NT], nt = tile - (tile / NT) * NT;
             const int rows = args.mtile_rows[mt];
-            if (!mbar_wait(smem_u32(&ctl->acc_full), (uint32_t)tcount & 1u, abrt)) {
-                raise_error(ctl, args.err, 6);
+            if (!mbar_wait(smem_u32(&pc.acc_full), (uint32_t)tcount & 1u, abrt)) {
+                raise_error(g, args.err, 6);
                 break;
             }
             tc_fence_after();
@@ -332,8 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (warp_live) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        uint32_t g[16], u[16];
-                        tmem_ld16(tl + kAccCol + 64u * hw + 16u * c, g);
+                        uint32_t gg[16], u[16];
+                        tmem_ld16(tl + kAccCol + 64u * hw + 16u * c, gg);
                         tmem_ld16(tl + kAccCol + 128u + 64u * hw + 16u * c, u);
                         tmem_ld_wait();
 #pragma unroll
@@ -341,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // invalid rows are replaced by zeros before any arithmetic;
                             // silu(g) = g / (1 + e^-g) with the fast exponential and
                             // division intrinsics (a few ulp of fp32)
-                            const float gf = row_live ? __uint_as_float(g[j]) : 0.0f;
+                            const float gf = row_live ? __uint_as_float(gg[j]) : 0.0f;
                             const float uf = row_live ? __uint_as_float(u[j]) : 0.0f;
                             h[16 * c + j] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
                         }
@@ -352,20 +404,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty));
+                if (lane == 0) mbar_arrive(smem_u32(&pc.acc_empty));
                 // the row's amax over all 128 columns: combine with the partner warp
                 float amax = 0.f;
 #pragma unroll
                 for (int j = 0; j < 64; ++j) amax = fmaxf(amax, fabsf(h[j]));
                 const int p = tcount & 1;
-                ctl->red[p][ew][lane] = amax;
+                pc.red[p][ew][lane] = amax;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ctl->red_full[p]));
-                if (!mbar_wait(smem_u32(&ctl->red_full[p]), (uint32_t)(tcount >> 1) & 1u, abrt)) {
-                    raise_error(ctl, args.err, 7);
+                if (lane == 0) mbar_arrive(smem_u32(&pc.red_full[p]));
+                if (!mbar_wait(smem_u32(&pc.red_full[p]), (uint32_t)(tcount >> 1) & 1u, abrt)) {
+                    raise_error(g, args.err, 7);
                     break;
                 }
-                amax = fmaxf(amax, ctl->red[p][ew ^ 4][lane]);
+                amax = fmaxf(amax, pc.red[p][ew ^ 4][lane]);
                 if (row_live) {
                     const int ex = act_block_exponent(amax);
                     const float inv = __int_as_float((127 - ex) << 23);
@@ -403,11 +455,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty));
+                if (lane == 0) mbar_arrive(smem_u32(&pc.acc_empty));
             }
         }
     }
+}
 
+template <int kMode>   // mode 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows
+__global__ void __launch_bounds__(kThreads, 1)
+    k_mx_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+              const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
+              const __grid_constant__ CUtensorMap tmA4, const __grid_constant__ CUtensorMap tmW, const GemmArgs args)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    GemmCtl* g = reinterpret_cast<GemmCtl*>(smem + kRingBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        init_phase(g->light);
+        init_phase(g->heavy);
+        g->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA0);
+        tma_prefetch_desc(&tmA1);
+        tma_prefetch_desc(&tmA2);
+        tma_prefetch_desc(&tmA3);
+        tma_prefetch_desc(&tmA4);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&g->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = g->tmem_base;
+    bool waited = false;   // the producer's wait for the previous kernel (producer thread only)
+
+    gemm_phase<kMode, true>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA2, &tmW, args, args.light_list,
+                            *args.light_count, waited);
+    // the heavy phase reuses the ring and the accumulator: every role of the
+    // light phase has drained its own work
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (!*(volatile int*)&g->abort)
+        gemm_phase<kMode, false>(smem, g, g->heavy, tmem, &tmA2, &tmA3, &tmA4, &tmW, args, args.heavy_list,
+                                 *args.heavy_count, waited);
+    // a CTA without tiles still waits before it lets the next kernel start
+    if (warp == 0 && lane == 0) {
+        producer_wait_once<kMode>(waited);
+        griddep_launch_dependents();
+    }
+
+    tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -415,28 +518,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int kMode, bool kLight>
-static cudaError_t set_attr()
-{
-    return cudaFuncSetAttribute(k_mx_gemm<kMode, kLight>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Shape<kLight>::kSmemBytes);
-}
-
 cudaError_t gemm_set_attributes()
 {
-    cudaError_t e = set_attr<0, false>();
-    if (e == cudaSuccess) e = set_attr<0, true>();
-    if (e == cudaSuccess) e = set_attr<1, false>();
-    if (e == cudaSuccess) e = set_attr<1, true>();
+    cudaError_t e = cudaFuncSetAttribute(k_mx_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_mx_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     return e;
 }
 
-static GemmArgs gemm1_args(const DevState& s)
+static GemmArgs common_args(const DevState& s)
 {
     GemmArgs a{};
-    a.sfa = s.asf;
     a.mtile_expert = s.mtile_expert;
     a.mtile_rows = s.mtile_rows;
+    a.light_list = s.light_list;
+    a.light_count = s.n_mtiles + 1;
+    a.heavy_list = s.heavy_list;
+    a.heavy_count = s.n_mtiles + 2;
+    a.err = s.err;
+    return a;
+}
+
+// Light m-tiles (activation boxes of 8 / 16 / 32 rows: maps 0..2), then heavy
+// m-tiles (32 / 64 / 128 rows: maps 2..4), in one launch.
+cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
+{
+    GemmArgs a = common_args(s);
+    a.sfa = s.asf;
     a.wq = s.w13q;
     a.KB = s.KB1;
     a.NT = s.NT1;
@@ -445,16 +552,14 @@ static GemmArgs gemm1_args(const DevState& s)
     a.hsf = s.hsf;
     a.I = s.I;
     a.prefetch = kPrefetchGateUp;
-    a.err = s.err;
-    return a;
+    return launch_kernel(k_mx_gemm<0>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_aq[0], s.tm_aq[1],
+                         s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13, a);
 }
 
-static GemmArgs gemm2_args(const DevState& s)
+cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
 {
-    GemmArgs a{};
+    GemmArgs a = common_args(s);
     a.sfa = s.hsf;
-    a.mtile_expert = s.mtile_expert;
-    a.mtile_rows = s.mtile_rows;
     a.wq = s.w2q;
     a.KB = s.KB2;
     a.NT = s.NT2;
@@ -462,41 +567,8 @@ static GemmArgs gemm2_args(const DevState& s)
     a.obuf = s.obuf;
     a.H = s.H;
     a.prefetch = kPrefetchDown;
-    a.err = s.err;
-    return a;
-}
-
-// Light m-tiles first (their kernel's grid drains while the heavy kernel
-// starts), then heavy m-tiles; each kernel finds its own tile count on the
-// device, so an empty list costs one short launch.
-cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
-{
-    GemmArgs a = gemm1_args(s);
-    a.list = s.light_list;
-    a.list_count = s.n_mtiles + 1;
-    a.box_rows[0] = 8, a.box_rows[1] = 16, a.box_rows[2] = 32;
-    k_mx_gemm<0, true><<<s.num_sms, kThreads, Shape<true>::kSmemBytes, st>>>(s.tm_aq[0], s.tm_aq[1], s.tm_aq[2], s.tm_w13, a);
-    a.list = s.heavy_list;
-    a.list_count = s.n_mtiles + 2;
-    a.box_rows[0] = 32, a.box_rows[1] = 64, a.box_rows[2] = 128;
-    k_mx_gemm<0, false><<<s.num_sms, kThreads, Shape<false>::kSmemBytes, st>>>(s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13,
-                                                                           a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
-{
-    GemmArgs a = gemm2_args(s);
-    a.list = s.light_list;
-    a.list_count = s.n_mtiles + 1;
-    a.box_rows[0] = 8, a.box_rows[1] = 16, a.box_rows[2] = 32;
-    k_mx_gemm<1, true><<<s.num_sms, kThreads, Shape<true>::kSmemBytes, st>>>(s.tm_hq[0], s.tm_hq[1], s.tm_hq[2], s.tm_w2, a);
-    a.list = s.heavy_list;
-    a.list_count = s.n_mtiles + 2;
-    a.box_rows[0] = 32, a.box_rows[1] = 64, a.box_rows[2] = 128;
-    k_mx_gemm<1, false><<<s.num_sms, kThreads, Shape<false>::kSmemBytes, st>>>(s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2,
-                                                                           a);
-    return cudaGetLastError();
+    return launch_kernel(k_mx_gemm<1>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_hq[0], s.tm_hq[1],
+                         s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2, a);
 }
 
 }  // namespace moe

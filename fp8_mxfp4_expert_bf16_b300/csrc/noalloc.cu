@@ -154,6 +154,7 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int H, const u
     cudaError_t e = cudaMemsetAsync(scratch + kNoAllocZeroOff, 0, (kNoAllocWords - kNoAllocZeroOff) * sizeof(float), s);
 
     DevState ds{};
+    ds.pdl = false;   // plain stream order, as for any other library call on the caller's stream
     ds.H = H;
     ds.E = E;
     ds.K = k;

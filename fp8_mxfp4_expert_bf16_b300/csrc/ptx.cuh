@@ -112,6 +112,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  : "memory");
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while
+// the previous kernel on its stream is still running.  griddep_wait blocks
+// until that kernel has completed and its memory writes are visible (a no-op
+// for a kernel launched without the attribute); griddep_launch_dependents
+// lets the next kernel be scheduled once every CTA of this one has issued it
+// (or exited).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols)
 {

@@ -15,6 +15,7 @@
 #include <cstdint>
 
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -32,59 +33,6 @@ __device__ __forceinline__ float warp_sum(float v)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
-}
-
-// ------------------------------------------------------------------ router
-// logits[t][e] = sum_h x[t][h] * Wr[e][h] + logit_bias[e]: bf16 products are
-// exact in fp32, accumulation in fp32.  One warp per (expert, 16 tokens);
-// lanes stride over h in 8-element (16-byte) vectors, then a warp reduction.
-constexpr int kRouterTok = 16;
-
-__global__ void __launch_bounds__(256) k_router_simt(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
-                                                     const float* __restrict__ lb, float* __restrict__ logits, int T,
-                                                     int H, int E)
-{
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * 8 + warp;
-    const int t0 = blockIdx.y * kRouterTok;
-    if (e >= E) return;
-    float acc[kRouterTok];
-#pragma unroll
-    for (int i = 0; i < kRouterTok; ++i) acc[i] = 0.f;
-    const uint16_t* w = wr + (size_t)e * H;
-    for (int h = lane * 8; h < H; h += 256) {
-        const uint4 wv = *reinterpret_cast<const uint4*>(w + h);
-        const float wf[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
-                             bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
-#pragma unroll
-        for (int i = 0; i < kRouterTok; ++i) {
-            const int t = t0 + i;
-            if (t < T) {
-                const uint4 xv = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h);
-                acc[i] = fmaf(bf16_lo(xv.x), wf[0], acc[i]);
-                acc[i] = fmaf(bf16_hi(xv.x), wf[1], acc[i]);
-                acc[i] = fmaf(bf16_lo(xv.y), wf[2], acc[i]);
-                acc[i] = fmaf(bf16_hi(xv.y), wf[3], acc[i]);
-                acc[i] = fmaf(bf16_lo(xv.z), wf[4], acc[i]);
-                acc[i] = fmaf(bf16_hi(xv.z), wf[5], acc[i]);
-                acc[i] = fmaf(bf16_lo(xv.w), wf[6], acc[i]);
-                acc[i] = fmaf(bf16_hi(xv.w), wf[7], acc[i]);
-            }
-        }
-    }
-    const float bias = lb[e];
-#pragma unroll
-    for (int i = 0; i < kRouterTok; ++i) {
-        const float v = warp_sum(acc[i]);
-        if (lane == i && t0 + i < T) logits[(size_t)(t0 + i) * E + e] = v + bias;
-    }
-}
-
-cudaError_t launch_router(const DevState& s, const uint16_t* x, int T, cudaStream_t st)
-{
-    dim3 grid((s.E + 7) / 8, (T + kRouterTok - 1) / kRouterTok);
-    k_router_simt<<<grid, 256, 0, st>>>(x, s.wr, s.lb, s.logits, T, s.H, s.E);
-    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ top-k
@@ -193,6 +141,8 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
                                               const float* __restrict__ cb, int32_t* __restrict__ ids,
                                               float* __restrict__ gates, int T, int E, int K, int score_func)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
@@ -207,11 +157,71 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
     }
 }
 
+// Small batches (split-K router): one block per token.  Each thread adds the
+// split partials of up to kMaxExperts / kTopkSplitThreads experts in split
+// order, then the logit bias, and stores the token's logits; warp 0 then
+// selects from the logits in shared memory.  All partial loads of a thread
+// are issued before its additions.
+constexpr int kTopkSplitThreads = 128;
+constexpr int kTopkSplitPer = kMaxExperts / kTopkSplitThreads;
+
+__global__ void __launch_bounds__(kTopkSplitThreads) k_topk_split(const float* __restrict__ part, int ksplit,
+                                                                  const float* __restrict__ lb,
+                                                                  float* __restrict__ logits_out,
+                                                                  const float* __restrict__ cb, int32_t* __restrict__ ids,
+                                                                  float* __restrict__ gates, int T, int E, int K,
+                                                                  int score_func)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    __shared__ float l_s[kMaxExperts];
+    const int t = blockIdx.x;
+    float p[kTopkSplitPer][kRouterMaxSplit];
+#pragma unroll
+    for (int i = 0; i < kTopkSplitPer; ++i) {
+        const int e = threadIdx.x + kTopkSplitThreads * i;
+#pragma unroll
+        for (int z = 0; z < kRouterMaxSplit; ++z)
+            p[i][z] = (e < E && z < ksplit) ? part[((size_t)z * T + t) * E + e] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kTopkSplitPer; ++i) {
+        const int e = threadIdx.x + kTopkSplitThreads * i;
+        if (e < E) {
+            float v = 0.f;
+#pragma unroll
+            for (int z = 0; z < kRouterMaxSplit; ++z) v += p[i][z];
+            v += lb[e];
+            logits_out[(size_t)t * E + e] = v;
+            l_s[e] = v;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    float sc[kMaxV];
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i) {
+        const int e = lane + 32 * i;
+        sc[i] = e < E ? l_s[e] : -INFINITY;
+    }
+    int id;
+    float g;
+    warp_topk(sc, cb, E, K, score_func, lane, id, g);
+    if (lane < K) {
+        ids[(size_t)t * K + lane] = id;
+        gates[(size_t)t * K + lane] = g;
+    }
+}
+
 cudaError_t launch_topk(const DevState& s, int T, cudaStream_t st, int ksplit)
 {
-    k_topk<<<(T + 7) / 8, 256, 0, st>>>(s.logits, s.logit_part, ksplit, s.lb, s.logits, s.cb, s.ids, s.gates, T, s.E,
-                                        s.K, s.score_func);
-    return cudaGetLastError();
+    if (ksplit > 1)
+        return launch_kernel(k_topk_split, dim3(T), dim3(kTopkSplitThreads), 0, st, s.pdl, (const float*)s.logit_part,
+                             ksplit, s.lb, s.logits, s.cb, s.ids, s.gates, T, s.E, s.K, s.score_func);
+    return launch_kernel(k_topk, dim3((T + 7) / 8), dim3(256), 0, st, s.pdl, (const float*)s.logits,
+                         (const float*)s.logit_part, ksplit, s.lb, s.logits, s.cb, s.ids, s.gates, T, s.E, s.K,
+                         s.score_func);
 }
 
 // ------------------------------------------------------------------ dispatch
@@ -219,6 +229,8 @@ cudaError_t launch_topk(const DevState& s, int T, cudaStream_t st, int ksplit)
 __global__ void __launch_bounds__(kChunk) k_chunk_hist(const int32_t* __restrict__ ids, int32_t* __restrict__ chunk_hist,
                                                        int T, int E, int K, int32_t* err)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int hist[kMaxExperts];
     for (int e = threadIdx.x; e < E; e += kChunk) hist[e] = 0;
     __syncthreads();
@@ -277,6 +289,8 @@ __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict_
                                                       int32_t* __restrict__ light_list,
                                                       int32_t* __restrict__ heavy_list, int nchunk, int E)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int warp_tot[32];
     const int e = threadIdx.x;
     int run = 0;
@@ -323,6 +337,8 @@ __global__ void __launch_bounds__(kChunk) k_scatter_rows(const int32_t* __restri
                                                          const int32_t* __restrict__ mtile_off,
                                                          int32_t* __restrict__ prow, int T, int E, int K)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ uint32_t mask[kMaxExperts][kChunk / 32];
     const int tid = threadIdx.x, lane = tid & 31;
     for (int i = tid; i < E * (kChunk / 32); i += kChunk) (&mask[0][0])[i] = 0u;
@@ -370,6 +386,8 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
                                                        uint8_t* __restrict__ aq, uint32_t* __restrict__ asf, int T,
                                                        int H, int K)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     const int KB = H / 128, lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (gw >= (long long)T * KB) return;
@@ -400,6 +418,8 @@ __global__ void __launch_bounds__(kMaxExperts) k_dispatch_small(
     int32_t* __restrict__ n_mtiles, int32_t* __restrict__ light_list, int32_t* __restrict__ heavy_list,
     int32_t* __restrict__ prow, int T, int E, int K)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int hist[kMaxExperts];
     __shared__ int mt_off_s[kMaxExperts];
     __shared__ uint32_t mask[kMaxExperts][kSmallT / 32];
@@ -462,39 +482,47 @@ __global__ void __launch_bounds__(kMaxExperts) k_dispatch_small(
 
 cudaError_t launch_dispatch_small(const DevState& s, int T, cudaStream_t st)
 {
-    k_dispatch_small<<<1, kMaxExperts, 0, st>>>(s.ids, s.counts, s.offsets, s.mtile_off, s.mtile_expert,
-                                                s.mtile_rows, s.n_mtiles, s.light_list, s.heavy_list, s.prow, T, s.E,
-                                                s.K);
-    return cudaGetLastError();
+    return launch_kernel(k_dispatch_small, dim3(1), dim3(kMaxExperts), 0, st, s.pdl, (const int32_t*)s.ids, s.counts,
+                         s.offsets, s.mtile_off, s.mtile_expert, s.mtile_rows, s.n_mtiles, s.light_list, s.heavy_list,
+                         s.prow, T, s.E, s.K);
 }
 
 cudaError_t launch_quant_scatter(const DevState& s, const uint16_t* x, int T, cudaStream_t st)
 {
     const long long warps = (long long)T * (s.H / 128);
-    k_quant_scatter<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(x, s.prow, s.aq, s.asf, T, s.H, s.K);
-    return cudaGetLastError();
+    return launch_kernel(k_quant_scatter, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, st, s.pdl, x,
+                         (const int32_t*)s.prow, s.aq, s.asf, T, s.H, s.K);
 }
 
 cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStream_t st, int* nlaunch)
 {
     const int nchunk = (T + kChunk - 1) / kChunk;
-    k_chunk_hist<<<nchunk, kChunk, 0, st>>>(s.ids, s.chunk_hist, T, s.E, s.K, s.err);
-    k_scan<<<1, kMaxExperts, 0, st>>>(s.chunk_hist, s.chunk_base, s.counts, s.offsets, s.mtile_off, s.mtile_expert,
-                                      s.mtile_rows, s.n_mtiles, s.light_list, s.heavy_list, nchunk, s.E);
-    k_scatter_rows<<<nchunk, kChunk, 0, st>>>(s.ids, s.chunk_base, s.mtile_off, s.prow, T, s.E, s.K);
-    const long long warps = (long long)T * (s.H / 128);
-    k_quant_scatter<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(x, s.prow, s.aq, s.asf, T, s.H, s.K);
+    cudaError_t e = launch_kernel(k_chunk_hist, dim3(nchunk), dim3(kChunk), 0, st, s.pdl, (const int32_t*)s.ids,
+                                  s.chunk_hist, T, s.E, s.K, s.err);
+    if (e == cudaSuccess)
+        e = launch_kernel(k_scan, dim3(1), dim3(kMaxExperts), 0, st, s.pdl, (const int32_t*)s.chunk_hist, s.chunk_base,
+                          s.counts, s.offsets, s.mtile_off, s.mtile_expert, s.mtile_rows, s.n_mtiles, s.light_list,
+                          s.heavy_list, nchunk, s.E);
+    if (e == cudaSuccess)
+        e = launch_kernel(k_scatter_rows, dim3(nchunk), dim3(kChunk), 0, st, s.pdl, (const int32_t*)s.ids,
+                          (const int32_t*)s.chunk_base, (const int32_t*)s.mtile_off, s.prow, T, s.E, s.K);
+    if (e == cudaSuccess) e = launch_quant_scatter(s, x, T, st);
     *nlaunch += 4;
-    return cudaGetLastError();
+    return e;
 }
 
 // ------------------------------------------------------------------ combine
 // y[t] = bf16_rne( sum_j gate[t][j] * o[row(t, j)] ), fp32 fused multiply-adds
-// in slot order.
+// in slot order.  Block (t, c): 1024 columns of token t, one float4 per
+// thread; the k expert-output loads are all issued before the additions.
+constexpr int kCombineCols = 1024;
+
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ obuf, const int32_t* __restrict__ prow,
                                                  const float* __restrict__ gates, uint16_t* __restrict__ y, int H,
                                                  int K)
 {
+    griddep_wait();
+    griddep_launch_dependents();
     __shared__ int rows[kMaxTopK];
     __shared__ float g[kMaxTopK];
     const int t = blockIdx.x;
@@ -503,29 +531,35 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ obuf,
         g[threadIdx.x] = gates[(size_t)t * K + threadIdx.x];
     }
     __syncthreads();
-    const int H4 = H / 4;
-    for (int h4 = threadIdx.x; h4 < H4; h4 += blockDim.x) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < K; ++j) {
-            const float4 o = reinterpret_cast<const float4*>(obuf + (size_t)rows[j] * H)[h4];
-            acc.x = fmaf(g[j], o.x, acc.x);
-            acc.y = fmaf(g[j], o.y, acc.y);
-            acc.z = fmaf(g[j], o.z, acc.z);
-            acc.w = fmaf(g[j], o.w, acc.w);
+    const int h4 = blockIdx.y * (kCombineCols / 4) + threadIdx.x;
+    if (h4 >= H / 4) return;
+    float4 o[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+        if (j < K) o[j] = reinterpret_cast<const float4*>(obuf + (size_t)rows[j] * H)[h4];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        if (j < K) {
+            acc.x = fmaf(g[j], o[j].x, acc.x);
+            acc.y = fmaf(g[j], o[j].y, acc.y);
+            acc.z = fmaf(g[j], o[j].z, acc.z);
+            acc.w = fmaf(g[j], o[j].w, acc.w);
         }
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 out;
-        out.x = *reinterpret_cast<const uint32_t*>(&lo);
-        out.y = *reinterpret_cast<const uint32_t*>(&hi);
-        reinterpret_cast<uint2*>(y + (size_t)t * H)[h4] = out;
     }
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 out;
+    out.x = *reinterpret_cast<const uint32_t*>(&lo);
+    out.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(y + (size_t)t * H)[h4] = out;
 }
 
 cudaError_t launch_combine(const DevState& s, uint16_t* y, int T, cudaStream_t st)
 {
-    k_combine<<<T, 256, 0, st>>>(s.obuf, s.prow, s.gates, y, s.H, s.K);
-    return cudaGetLastError();
+    const dim3 grid(T, (s.H + kCombineCols - 1) / kCombineCols);
+    return launch_kernel(k_combine, grid, dim3(256), 0, st, s.pdl, (const float*)s.obuf, (const int32_t*)s.prow,
+                         (const float*)s.gates, y, s.H, s.K);
 }
 
 // ------------------------------------------------------------------ load time

@@ -95,6 +95,10 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // x (and the logit buffers) belong to the previous kernel on the stream
+    // until it has completed
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem = ctl->tmem_base;
     const volatile int* abrt = &ctl->abort;
 
@@ -200,10 +204,8 @@ cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, c
 {
     const int N = router_tile_n(T);
     dim3 grid((T + 127) / 128, (s.E + N - 1) / N, ksplit);
-    k_router_tc<<<grid, 128, kRSmemBytes, st>>>(tmX, N == 64 ? s.tm_wr64 : s.tm_wr128, s.lb, s.logits,
-                                                ksplit > 1 ? s.logit_part : nullptr, T, s.E, s.H / 64 / ksplit, N,
-                                                s.err);
-    return cudaGetLastError();
+    return launch_kernel(k_router_tc, grid, dim3(128), kRSmemBytes, st, s.pdl, tmX, N == 64 ? s.tm_wr64 : s.tm_wr128,
+                         s.lb, s.logits, ksplit > 1 ? s.logit_part : nullptr, T, s.E, s.H / 64 / ksplit, N, s.err);
 }
 
 }  // namespace moe
