@@ -15,7 +15,7 @@ constexpr int kNumABox = 5;         // activation tile maps with 8 / 16 / 32 / 6
 constexpr int kWBlockRowsPerHalf = 136;   // interleaved weight block: 128 weight rows + 8 scale rows of 64 B
 constexpr int kRouterMaxSplit = 16;       // split-K factor of the router for small batches
 constexpr int kRouterSplitMaxT = 512;     // batches up to this size use the split-K router
-constexpr int kLightRows = 32;      // m-tiles with at most this many rows use the light GEMM shape
+constexpr int kLightRows = 16;      // m-tiles with at most this many rows use the light GEMM shape
 
 // Error word codes written by kernels (first writer wins).
 constexpr int kDevErrTimeout = 1;

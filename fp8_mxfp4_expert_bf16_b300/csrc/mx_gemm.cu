@@ -10,7 +10,7 @@
 // FP8 e4m3).
 //
 // One persistent CTA per SM walks two static lists of (m-tile, n-tile)
-// tiles: first the light m-tiles (at most 32 valid rows), then the heavy
+// tiles: first the light m-tiles (at most 16 valid rows), then the heavy
 // ones, each phase with the shared-memory ring shape that suits it.  An
 // m-tile is 128 consecutive padded rows of one expert; an n-tile is 256
 // weight rows (gate 128 + up 128 of one 128-wide slice of the expert's
@@ -20,8 +20,7 @@
 //               (128 B rows, 128-byte swizzle), the weight tile (one
 //               contiguous block of the tile-major weight layout; E2M1 codes
 //               expanded by TMA into 16-byte groups, the operand format of
-//               kind::mxf8f6f4) and both scale-factor chunks; it also runs an
-//               L2 prefetch stream a few K steps ahead of the ring;
+//               kind::mxf8f6f4) and both scale-factor chunks;
 //   warp 1      TMEM owner and MMA issuer: copies the scale chunks into
 //               TMEM (tcgen05.cp) and issues 4 block-scaled 128x256x32 MMAs
 //               per stage into one fp32 accumulator in TMEM;
@@ -33,8 +32,8 @@
 // Programmatic dependent launch: the kernel may start while the previous
 // kernel of the forward (which writes the activations) is still running.
 // Before waiting for it, the producer streams what does not depend on it:
-// the weight tiles of the first ring stages and an L2 prefetch of the
-// following ones.  Only then does it wait and load the activation tiles.
+// the weight tiles of the first ring stages.  Only then does it wait and
+// load the activation tiles.
 // All waits are bounded in time; a wait that gives up writes an error word,
 // raises a CTA-wide abort flag, and the CTA drains its copies / MMAs and
 // frees TMEM before exiting.
@@ -49,24 +48,28 @@
 namespace moe {
 
 // The two ring shapes (one kernel runs both phases in turn):
-//  heavy (m-tiles with more than 32 valid rows): 128-row activation slot,
-//    4-stage ring;
-//  light (at most 32 valid rows: decode, and an expert's last m-tile): the
-//    activation slot holds only the 32-row box (4 KB), which buys a 5th
-//    stage.  The MMA still reads 128 rows; rows 32..127 then come from the
-//    first 12 KB of the same stage's weight tile - finite or not, they only
-//    reach accumulator rows that the epilogue never uses.
+//  heavy (m-tiles with more than kLightRows = 16 valid rows): 128-row
+//    activation slot, 4-stage ring;
+//  light (at most 16 valid rows: decode, and an expert's last m-tile): the
+//    activation slot holds only the 16-row box (2 KB), which buys 6 stages.
+//    The MMA still reads 128 rows; rows 16..127 then come from the first
+//    14 KB of the same stage's weight tile - finite or not, they only reach
+//    accumulator rows that the epilogue never uses.
+// With six stages in flight per SM (about 100 KB of weights) the weight
+// stream needs no separate L2 prefetch; one measured on top of the ring
+// slowed both GEMMs.
 template <bool kLight>
 struct Shape {
-    static constexpr int kStages = kLight ? 5 : 4;
-    static constexpr int kABytes = kLight ? 32 * 128 : kBM * 128;
+    static_assert(kLightRows == 16, "light ring shape");
+    static constexpr int kStages = kLight ? 6 : 4;
+    static constexpr int kABytes = kLight ? 16 * 128 : kBM * 128;
     static constexpr int kBOff = kABytes;
     static constexpr int kSFAOff = kBOff + 2 * 128 * 128;     // weight tile: 256 rows x 128 B (16-byte slots)
     static constexpr int kSFBOff = kSFAOff + 512;
     static constexpr int kStageStride = ((kSFBOff + 1024 + 1023) / 1024) * 1024;
     static constexpr int kRingBytes = kStages * kStageStride;
-    // activation box heights of the phase's three activation maps
-    static constexpr int kBox0 = kLight ? 8 : 32, kBox1 = kLight ? 16 : 64, kBox2 = kLight ? 32 : 128;
+    // activation box heights of the phase's activation maps (light: two)
+    static constexpr int kBox0 = kLight ? 8 : 32, kBox1 = kLight ? 16 : 64, kBox2 = kLight ? 16 : 128;
 };
 constexpr int kRingBytes =
     Shape<true>::kRingBytes > Shape<false>::kRingBytes ? Shape<true>::kRingBytes : Shape<false>::kRingBytes;
@@ -80,9 +83,6 @@ constexpr uint32_t kAccCol = 0;      // accumulator: 256 fp32 columns
 constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), SFB at +8 (8 cols)
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, epilogue warps
-// k-steps of weights the L2 prefetch stream runs ahead of the TMA ring
-constexpr int kPrefetchGateUp = 8;
-constexpr int kPrefetchDown = 8;
 
 struct GemmArgs {
     const uint32_t* sfa;         // activation scale words [MT][KB][128]
@@ -100,7 +100,6 @@ struct GemmArgs {
     uint8_t* hq;                 // [R][I] e4m3
     uint32_t* hsf;               // [MT][I/128][128]
     int I;
-    int prefetch;                // k-steps the L2 prefetch stream runs ahead (0 = off)
     // down epilogue
     float* obuf;                 // [R][H]
     int H;
@@ -216,25 +215,6 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
             // global-load latency never sits between two TMA issues.
             const int stride = gridDim.x;
             auto load_mt = [&](int tile) { return tile < total ? list[tile / NT] : 0; };
-            // L2 prefetch stream: the same (tile, k-step) sequence as the ring,
-            // for the weight boxes and their scales
-            // (one prefetch per stage loaded, so it stays args.prefetch k-steps ahead)
-            int pf_tile = blockIdx.x, pf_kb = 0;
-            int pf_e = args.mtile_expert[load_mt(pf_tile)];
-            int pf_mt_next = load_mt(pf_tile + stride);
-            auto prefetch_next = [&]() {
-                if (pf_tile >= total) return;
-                const int pnt = pf_tile - (pf_tile / NT) * NT;
-                const size_t wrow = ((((size_t)pf_e * NT + pnt) * KB + pf_kb) * args.halves) * kWBlockRowsPerHalf;
-                bulk_prefetch_l2(args.wq + wrow * 64, args.halves * kWBlockRowsPerHalf * 64);
-                if (++pf_kb == KB) {
-                    pf_kb = 0;
-                    pf_tile += stride;
-                    pf_e = args.mtile_expert[pf_mt_next];
-                    pf_mt_next = load_mt(pf_tile + stride);
-                }
-            };
-            for (int i = 0; i < args.prefetch; ++i) prefetch_next();
             int it = 0, pre = 0;
             bool ok = true;
             int cur_mt = load_mt(blockIdx.x);
@@ -271,7 +251,6 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                                   args.halves * 512, fb);
                         issued[kb] = true;
                         last_phase[kb] = 0;
-                        prefetch_next();
                     }
                     producer_wait_once<kMode>(waited);
                     for (int kb = 0; kb < pre; ++kb) {
@@ -302,7 +281,6 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                               args.halves * 512, fb);
                     issued[s] = true;
                     last_phase[s] = ph;
-                    prefetch_next();
                 }
             }
             // wait for every copy this thread started before the ring is reused
@@ -494,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = g->tmem_base;
     bool waited = false;   // the producer's wait for the previous kernel (producer thread only)
 
-    gemm_phase<kMode, true>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA2, &tmW, args, args.light_list,
+    gemm_phase<kMode, true>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args, args.light_list,
                             *args.light_count, waited);
     // the heavy phase reuses the ring and the accumulator: every role of the
     // light phase has drained its own work
@@ -538,7 +516,7 @@ static GemmArgs common_args(const DevState& s)
     return a;
 }
 
-// Light m-tiles (activation boxes of 8 / 16 / 32 rows: maps 0..2), then heavy
+// Light m-tiles (activation boxes of 8 / 16 rows: maps 0, 1), then heavy
 // m-tiles (32 / 64 / 128 rows: maps 2..4), in one launch.
 cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
 {
@@ -551,7 +529,6 @@ cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
     a.hq = s.hq;
     a.hsf = s.hsf;
     a.I = s.I;
-    a.prefetch = kPrefetchGateUp;
     return launch_kernel(k_mx_gemm<0>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_aq[0], s.tm_aq[1],
                          s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13, a);
 }
@@ -566,7 +543,6 @@ cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
     a.halves = s.BN2 / 128;
     a.obuf = s.obuf;
     a.H = s.H;
-    a.prefetch = kPrefetchDown;
     return launch_kernel(k_mx_gemm<1>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_hq[0], s.tm_hq[1],
                          s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2, a);
 }
