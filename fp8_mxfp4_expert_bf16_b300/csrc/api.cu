@@ -77,7 +77,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
     return fn;
 }
 
-// 2-D tensor map over a row-major [rows][inner] tensor.
+// 2-D tensor map over a row-major [rows][inner] tensor, 128-byte swizzle.
 static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t rows,
                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows)
 {

@@ -103,6 +103,7 @@ struct GemmArgs {
     // down epilogue
     float* obuf;                 // [R][H]
     int H;
+    int early_trigger;           // let the next kernel be scheduled right after the wait (else at the end)
     int32_t* err;
 };
 
@@ -171,19 +172,44 @@ __device__ __forceinline__ int act_block_exponent(float amax)
 // CTA, before the first activation load).  Tile lists and weights are read
 // before it: the lists come from the dispatch kernel, which had completed
 // before the previous kernel passed its own wait and allowed this one to
-// start.  The gate/up GEMM then lets the next kernel (the down GEMM) be
-// scheduled at once, so that its CTAs take over SMs as this kernel's CTAs
-// finish and stream their first weights meanwhile; the down GEMM lets its
+// start.  A GEMM followed by another GEMM then lets it be scheduled at
+// once (early_trigger), so that its CTAs take over SMs as this kernel's CTAs
+// finish and stream their first weights meanwhile; the last GEMM lets its
 // successor (the combine, which has nothing to do before its own wait) be
 // scheduled only near the end of each CTA's work, so that waiting combine
 // blocks do not sit beside running GEMM CTAs.
-template <int kMode>
-__device__ __forceinline__ void producer_wait_once(bool& waited)
+__device__ __forceinline__ void producer_wait_once(bool& waited, int early_trigger)
 {
     if (!waited) {
         griddep_wait();
-        if (kMode == 0) griddep_launch_dependents();
+        if (early_trigger) griddep_launch_dependents();
         waited = true;
+    }
+}
+
+// Down-GEMM epilogue of one warp: `ncols` (64 or 128) fp32 accumulator
+// columns of its 32 TMEM lanes go to registers, the accumulator is released
+// (arrive on `acc_empty`), then each live lane stores its row's columns.
+__device__ __forceinline__ void store_rows_after_release(uint32_t taddr, int ncols, bool warp_live, bool row_live,
+                                                         float* dst, uint32_t acc_empty, int lane)
+{
+    uint32_t v[128];
+    if (warp_live) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (32 * c < ncols) tmem_ld32(taddr + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+        tmem_ld_wait();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(acc_empty);
+    if (warp_live && row_live) {
+        float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (4 * j < ncols)
+                d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
     }
 }
 
@@ -252,7 +278,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         issued[kb] = true;
                         last_phase[kb] = 0;
                     }
-                    producer_wait_once<kMode>(waited);
+                    producer_wait_once(waited, args.early_trigger);
                     for (int kb = 0; kb < pre; ++kb) {
                         uint8_t* st = smem + kb * kStageStride;
                         const uint32_t fb = smem_u32(&pc.full[kb]);
@@ -414,26 +440,13 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         args.hsf[sf_word_index(mt, nt, args.I / 128, row)] = (uint32_t)(ex + 127) * 0x01010101u;
                 }
             } else {
-                // this warp: output columns [hw * ncols / 2, (hw + 1) * ncols / 2)
+                // this warp: output columns [hw * ncols / 2, (hw + 1) * ncols / 2).  The
+                // whole slice is read into registers first and the accumulator released,
+                // so the next tile's MMAs run while the rows are stored.
                 const int ncols = 128 * args.halves, half_cols = ncols / 2;
                 float* dst = args.obuf + (size_t)(mt * kBM + row) * args.H + (size_t)nt * ncols + hw * half_cols;
-                if (warp_live) {
-                    for (int c = 0; c < half_cols / 16; ++c) {
-                        uint32_t v[16];
-                        tmem_ld16(tl + kAccCol + (uint32_t)(hw * half_cols) + 16u * c, v);
-                        tmem_ld_wait();
-                        if (row_live) {
-                            float4* d4 = reinterpret_cast<float4*>(dst + 16 * c);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&pc.acc_empty));
+                store_rows_after_release(tl + kAccCol + (uint32_t)(hw * half_cols), half_cols, warp_live, row_live, dst,
+                                         smem_u32(&pc.acc_empty), lane);
             }
         }
     }
@@ -484,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  *args.heavy_count, waited);
     // a CTA without tiles still waits before it lets the next kernel start
     if (warp == 0 && lane == 0) {
-        producer_wait_once<kMode>(waited);
+        producer_wait_once(waited, args.early_trigger);
         griddep_launch_dependents();
     }
 
@@ -516,9 +529,7 @@ static GemmArgs common_args(const DevState& s)
     return a;
 }
 
-// Light m-tiles (activation boxes of 8 / 16 rows: maps 0, 1), then heavy
-// m-tiles (32 / 64 / 128 rows: maps 2..4), in one launch.
-cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
+static GemmArgs gemm1_args(const DevState& s)
 {
     GemmArgs a = common_args(s);
     a.sfa = s.asf;
@@ -529,11 +540,10 @@ cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
     a.hq = s.hq;
     a.hsf = s.hsf;
     a.I = s.I;
-    return launch_kernel(k_mx_gemm<0>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_aq[0], s.tm_aq[1],
-                         s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13, a);
+    return a;
 }
 
-cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
+static GemmArgs gemm2_args(const DevState& s)
 {
     GemmArgs a = common_args(s);
     a.sfa = s.hsf;
@@ -543,6 +553,23 @@ cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
     a.halves = s.BN2 / 128;
     a.obuf = s.obuf;
     a.H = s.H;
+    return a;
+}
+
+// Light m-tiles (activation boxes of 8 / 16 rows: maps 0, 1), then heavy
+// m-tiles (32 / 64 / 128 rows: maps 2..4), in one launch.
+cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
+{
+    GemmArgs a = gemm1_args(s);
+    a.early_trigger = 1;   // the down GEMM follows
+    return launch_kernel(k_mx_gemm<0>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_aq[0], s.tm_aq[1],
+                         s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13, a);
+}
+
+cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
+{
+    GemmArgs a = gemm2_args(s);
+    a.early_trigger = 0;   // the combine follows
     return launch_kernel(k_mx_gemm<1>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_hq[0], s.tm_hq[1],
                          s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2, a);
 }
