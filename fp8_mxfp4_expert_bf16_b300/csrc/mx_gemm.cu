@@ -187,14 +187,16 @@ __device__ __forceinline__ void producer_wait_once(bool& waited, int early_trigg
     }
 }
 
-// Down-GEMM epilogue of one warp: `ncols` (64 or 128) fp32 accumulator
-// columns of its 32 TMEM lanes go to registers, the accumulator is released
-// (arrive on `acc_empty`), then each live lane stores its row's columns.
-__device__ __forceinline__ void store_rows_after_release(uint32_t taddr, int ncols, bool warp_live, bool row_live,
-                                                         float* dst, uint32_t acc_empty, int lane)
+// Down-GEMM epilogue of one warp, light m-tiles (at most kLightRows valid
+// rows): `ncols` (64 or 128) fp32 accumulator columns of its 32 TMEM lanes
+// go to registers, the accumulator is released (arrive on `acc_empty`), then
+// each live lane stores its own row.  With so few rows the stores are short
+// and the accumulator is held only for the TMEM reads.
+__device__ __forceinline__ void store_rows_direct(uint32_t taddr, int ncols, int live_rows, float* dst0,
+                                                  size_t row_stride, uint32_t acc_empty, int lane)
 {
     uint32_t v[128];
-    if (warp_live) {
+    if (live_rows > 0) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
             if (32 * c < ncols) tmem_ld32(taddr + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
@@ -203,13 +205,58 @@ __device__ __forceinline__ void store_rows_after_release(uint32_t taddr, int nco
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(acc_empty);
-    if (warp_live && row_live) {
-        float4* d4 = reinterpret_cast<float4*>(dst);
+    if (lane < live_rows) {
+        float4* d4 = reinterpret_cast<float4*>(dst0 + (size_t)lane * row_stride);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             if (4 * j < ncols)
                 d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+    }
+}
+
+// Down-GEMM epilogue of one warp, heavy m-tiles: kCols (64 or 128) fp32
+// accumulator columns of its 32 TMEM lanes (rows), 32 columns at a time: read into
+// registers, transposed across the warp with a five-step butterfly of
+// shuffles so that lane l holds column l of all 32 rows, and stored one row
+// per instruction (32 lanes x 4 B = one full 128-byte line, instead of 32
+// rows' 16-byte pieces).  The accumulator is released (arrive on
+// `acc_empty`) as soon as the last block has been read.  dst0 is row 0 of
+// the warp's 32 rows, `live_rows` how many of them are valid, rows
+// `row_stride` floats apart.
+template <int kCols>
+__device__ __forceinline__ void store_rows_transposed(uint32_t taddr, int live_rows, float* dst0, size_t row_stride,
+                                                      uint32_t acc_empty, int lane)
+{
+#pragma unroll 1
+    for (int b = 0; b < kCols / 32; ++b) {
+        uint32_t a[32];
+        if (live_rows > 0) {
+            tmem_ld32(taddr + 32u * b, a);
+            tmem_ld_wait();
+        }
+        if (b == kCols / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+        if (live_rows <= 0) continue;
+#pragma unroll
+        for (int sft = 16; sft >= 1; sft >>= 1) {
+            const bool upper = (lane & sft) != 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                if ((i & sft) == 0) {
+                    const uint32_t send = upper ? a[i] : a[i + sft];
+                    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, sft);
+                    if (upper) a[i] = recv;
+                    else a[i + sft] = recv;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < live_rows) dst0[(size_t)j * row_stride + 32 * b + lane] = __uint_as_float(a[j]);
     }
 }
 
@@ -444,9 +491,16 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 // whole slice is read into registers first and the accumulator released,
                 // so the next tile's MMAs run while the rows are stored.
                 const int ncols = 128 * args.halves, half_cols = ncols / 2;
-                float* dst = args.obuf + (size_t)(mt * kBM + row) * args.H + (size_t)nt * ncols + hw * half_cols;
-                store_rows_after_release(tl + kAccCol + (uint32_t)(hw * half_cols), half_cols, warp_live, row_live, dst,
-                                         smem_u32(&pc.acc_empty), lane);
+                float* dst0 =
+                    args.obuf + (size_t)(mt * kBM + q * 32) * args.H + (size_t)nt * ncols + hw * half_cols;
+                const int live = warp_live ? min(32, rows - q * 32) : 0;
+                const uint32_t taddr = tl + kAccCol + (uint32_t)(hw * half_cols);
+                if (kLight)
+                    store_rows_direct(taddr, half_cols, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
+                else if (half_cols == 128)
+                    store_rows_transposed<128>(taddr, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
+                else
+                    store_rows_transposed<64>(taddr, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
             }
         }
     }
