@@ -23,7 +23,9 @@ Readings where the pages are silent (each is listed in the design notes):
   * activation function SwiGLU: h = silu(gate) * up, gate rows [0, I) of the
     fused gate/up matrix, up rows [I, 2I);
   * activation blocks are 1 x 128 along K with a power-of-two (E8M0) scale,
-    the smallest one that keeps the block's amax within e4m3's 448;
+    the smallest one that keeps the block's amax within e4m3's 448; the
+    variant with an fp32 scale amax / 448 takes the values at fp32 and
+    divides in fp32 (an all-zero block: scale 0, zero codes);
   * the correction bias is added to the scores for selection only; the
     router's logit bias is added to the logits;
   * gates are the selected (unbiased) scores renormalised to sum to 1;
@@ -75,6 +77,7 @@ def _L():
             ("orc_e4m3_decode_array", None, [p, sz, p]), ("orc_e4m3_encode_array", None, [p, sz, p]),
             ("orc_bf16_encode_array", None, [p, sz, p]),
             ("orc_act_quant_rows", None, [p, sz, i32, i32, p, p]),
+            ("orc_act_quant_rows_f32s", None, [p, sz, i32, i32, p, p]),
             ("orc_mxfp4_quant_rows", None, [p, sz, i32, p, p]),
             ("orc_mxfp4_decode_rows", None, [p, p, sz, i32, p]),
         ]:
@@ -153,25 +156,41 @@ def e4m3_encode_array(v: np.ndarray) -> np.ndarray:
     return out
 
 
-def act_quant(v: np.ndarray, blk: int = 128):
-    """Per-row 1 x blk e4m3 quantisation with an E8M0 power-of-two scale.
+ACT_SCALE_E8M0 = 0
+ACT_SCALE_F32 = 1
+
+
+def act_quant(v: np.ndarray, blk: int = 128, mode: int = ACT_SCALE_E8M0):
+    """Per-row 1 x blk e4m3 quantisation.
 
     [P2 "Overview": block-wise e4m3; P3 "Self-Hosting": dynamic activation
-    scheme.]  Returns (codes u8 [rows, n], scale bytes u8 [rows, n/blk]).
+    scheme.]  mode ACT_SCALE_E8M0: a power-of-two scale per block, the
+    smallest that keeps the block's amax within 448, returned as E8M0 bytes
+    (u8 [rows, n/blk]).  mode ACT_SCALE_F32: s = fp32(amax / 448) per block
+    of the values taken at fp32, codes e4m3(fp32(v / s)), returned as
+    float32 [rows, n/blk] (0 for an all-zero block).  Codes u8 [rows, n].
     """
     v = np.ascontiguousarray(v, dtype=np.float64)
     rows, n = v.shape
     assert n % blk == 0
     q = np.empty((rows, n), dtype=np.uint8)
-    s = np.empty((rows, n // blk), dtype=np.uint8)
-    _L().orc_act_quant_rows(_ptr(v), rows, n, blk, _ptr(q), _ptr(s))
+    if mode == ACT_SCALE_F32:
+        s = np.empty((rows, n // blk), dtype=np.float32)
+        _L().orc_act_quant_rows_f32s(_ptr(v), rows, n, blk, _ptr(q), _ptr(s))
+    else:
+        s = np.empty((rows, n // blk), dtype=np.uint8)
+        _L().orc_act_quant_rows(_ptr(v), rows, n, blk, _ptr(q), _ptr(s))
     return q, s
 
 
 def act_dequant(q: np.ndarray, s: np.ndarray, blk: int = 128) -> np.ndarray:
-    """Exact value of quantised activations: e4m3(q) * 2^(s-127)."""
+    """Exact value of quantised activations: e4m3(q) * scale, the scale an
+    E8M0 byte (2^(s-127)) or an fp32 value, by the dtype of ``s``."""
     vals = e4m3_decode_array(q)
-    scale = np.ldexp(1.0, s.astype(np.int64) - 127)
+    if s.dtype == np.float32:
+        scale = s.astype(np.float64)
+    else:
+        scale = np.ldexp(1.0, s.astype(np.int64) - 127)
     return vals * np.repeat(scale, blk, axis=-1)
 
 
@@ -277,22 +296,23 @@ def silu(g: np.ndarray) -> np.ndarray:
     return g / (1.0 + np.exp(-g))
 
 
-def expert_ffn(a: np.ndarray, w13_q, w13_s, w2_q, w2_s):
+def expert_ffn(a: np.ndarray, w13_q, w13_s, w2_q, w2_s, act_scale_mode: int = ACT_SCALE_E8M0):
     """One expert's SwiGLU FFN on exact activation values a [n, H].
 
     [P5 "How Big Is Each Expert?": gate, up and down projections around a
     2,048-wide middle; P5 "Why Are the V2.6 Files Half...": MXFP4 experts.]
     gate/up = a . W13^T with W13 [2I, H] decoded exactly (gate rows first);
-    h = silu(gate) * up in fp64; h re-quantised per 1 x 128 block to e4m3;
-    o = dequant(h) . W2^T with W2 [H, I].
-    Returns (h fp64 [n, I], hq u8 [n, I], hs u8 [n, I/128], o fp64 [n, H]).
+    h = silu(gate) * up in fp64; h re-quantised per 1 x 128 block to e4m3
+    (scales by ``act_scale_mode``); o = dequant(h) . W2^T with W2 [H, I].
+    Returns (h fp64 [n, I], hq u8 [n, I], hs [n, I/128] (E8M0 bytes or fp32),
+    o fp64 [n, H]).
     """
     W13 = mxfp4_decode(w13_q, w13_s)
     I2 = W13.shape[0]
     I = I2 // 2
     gu = a @ W13.T
     h = silu(gu[:, :I]) * gu[:, I:]
-    hq, hs = act_quant(h, 128)
+    hq, hs = act_quant(h, 128, act_scale_mode)
     W2 = mxfp4_decode(w2_q, w2_s)
     o = act_dequant(hq, hs, 128) @ W2.T
     return h, hq, hs, o
@@ -306,9 +326,9 @@ class Forward:
     perm: np.ndarray
     tokens: np.ndarray      # int64 [n] the tokens whose outputs were computed
     aq: np.ndarray          # u8 [n, H]   Q1 codes of those tokens
-    as_: np.ndarray         # u8 [n, H/128]
+    as_: np.ndarray         # [n, H/128] E8M0 bytes (u8) or fp32 scales
     hq: np.ndarray          # u8 [n, k, I] Q2 codes per (token, slot)
-    hs: np.ndarray          # u8 [n, k, I/128]
+    hs: np.ndarray          # [n, k, I/128] E8M0 bytes (u8) or fp32 scales
     h: np.ndarray           # f64 [n, k, I] pre-quantisation SwiGLU output
     o: np.ndarray           # f64 [n, k, H] expert outputs before the gate weighting
     y64: np.ndarray         # f64 [n, H] gate-weighted sum before rounding
@@ -317,7 +337,7 @@ class Forward:
 
 def forward(x_bf16, router_w_bf16, w13_q, w13_s, w2_q, w2_s, k: int,
             score_func: int = SCORE_SIGMOID, logit_bias=None, sel_bias=None,
-            tokens=None) -> Forward:
+            tokens=None, act_scale_mode: int = ACT_SCALE_E8M0) -> Forward:
     """The whole layer: route, dispatch, quantise, experts, combine.
 
     Routing, counts, offsets and the permutation cover every token; the
@@ -330,17 +350,17 @@ def forward(x_bf16, router_w_bf16, w13_q, w13_s, w2_q, w2_s, k: int,
     counts, offsets, perm = dispatch(r.ids, E)
     toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     n = toks.size
-    aq, as_ = act_quant(bf16_to_f64(x_bf16[toks]), 128)
+    aq, as_ = act_quant(bf16_to_f64(x_bf16[toks]), 128, act_scale_mode)
     a = act_dequant(aq, as_, 128)
     I = w2_q.shape[2] * 2
     hq = np.zeros((n, k, I), dtype=np.uint8)
-    hs = np.zeros((n, k, I // 128), dtype=np.uint8)
+    hs = np.zeros((n, k, I // 128), dtype=np.float32 if act_scale_mode == ACT_SCALE_F32 else np.uint8)
     h = np.zeros((n, k, I), dtype=np.float64)
     o = np.zeros((n, k, H), dtype=np.float64)
     sel = r.ids[toks]
     for e in np.unique(sel):
         rows, slots = np.nonzero(sel == e)
-        h_e, hq_e, hs_e, o_e = expert_ffn(a[rows], w13_q[e], w13_s[e], w2_q[e], w2_s[e])
+        h_e, hq_e, hs_e, o_e = expert_ffn(a[rows], w13_q[e], w13_s[e], w2_q[e], w2_s[e], act_scale_mode)
         h[rows, slots] = h_e
         hq[rows, slots] = hq_e
         hs[rows, slots] = hs_e

@@ -144,6 +144,35 @@ void orc_act_quant_row(const double* v, int n, int blk, uint8_t* q, uint8_t* sca
     }
 }
 
+/* The fp32-scale variant of the same 1 x blk quantisation (the "dynamic
+ * activation scheme" read as a per-block fp32 scale): each value is taken
+ * at fp32 (the precision the activations are computed in), the block scale
+ * is s = amax / 448 divided in fp32, and the code is e4m3 (round to nearest
+ * even, saturating) of the fp32 quotient v / s.  An all-zero block stores
+ * s = 0 and zero codes.  Dequantised value: e4m3(q) * s. */
+void orc_act_quant_row_f32s(const double* v, int n, int blk, uint8_t* q, float* scale)
+{
+    for (int b = 0; b < n / blk; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < blk; ++i) {
+            const float a = fabsf((float)v[b * blk + i]);
+            if (a > amax) amax = a;
+        }
+        const float sc = amax / 448.0f;
+        scale[b] = sc;
+        for (int i = 0; i < blk; ++i) {
+            const float x = (float)v[b * blk + i];
+            q[b * blk + i] = amax > 0.0f ? (uint8_t)orc_e4m3_encode((double)(x / sc)) : (uint8_t)0;
+        }
+    }
+}
+
+void orc_act_quant_rows_f32s(const double* v, size_t rows, int n, int blk, uint8_t* q, float* scale)
+{
+    for (size_t r = 0; r < rows; ++r)
+        orc_act_quant_row_f32s(v + r * (size_t)n, n, blk, q + r * (size_t)n, scale + r * (size_t)(n / blk));
+}
+
 /* E2M1 code of one value already divided by its block scale, round to
  * nearest with ties to the even code, saturating at +-6. */
 uint32_t orc_e2m1_encode(double v)
