@@ -48,6 +48,9 @@ def peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
+ACT_SCALES = {"e8m0": 0, "f32": 1}
+
+
 def workload_desc(cfg):
     return {"workload": cfg.name, "desc": cfg.desc, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I, "top_k": cfg.k,
             "seed": cfg.seed, "routing_bias": cfg.bias, "score": "sigmoid" if cfg.score_func == 0 else "softmax"}
@@ -187,7 +190,7 @@ def dist_env():
     return ws, rank, local
 
 
-def oracle_sample(inp, budget_s=12.0, max_tokens=None):
+def oracle_sample(inp, budget_s=12.0, max_tokens=None, act_scale_mode=0):
     """Time the CPU oracle token by token on the workload (routing of the
     whole batch included in every call) until the time budget is spent."""
     import oracle
@@ -198,7 +201,7 @@ def oracle_sample(inp, budget_s=12.0, max_tokens=None):
     done = 0
     for t in order:
         oracle.forward(inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, c.k, c.score_func,
-                       inp.logit_bias, inp.sel_bias, tokens=[int(t)])
+                       inp.logit_bias, inp.sel_bias, tokens=[int(t)], act_scale_mode=act_scale_mode)
         done += 1
         if time.perf_counter() - t0 >= budget_s or (max_tokens and done >= max_tokens):
             break
@@ -223,10 +226,12 @@ def run_reference(args, cfg):
     tokens = 0
     elapsed = 0.0
     for _ in range(args.warmup):
-        oracle_sample(inp, budget_s=args.ref_budget / max(args.steps, 1), max_tokens=1)
+        oracle_sample(inp, budget_s=args.ref_budget / max(args.steps, 1), max_tokens=1,
+                      act_scale_mode=ACT_SCALES[args.act_scale])
     per = []
     for _ in range(args.steps):
-        n, el = oracle_sample(inp, budget_s=args.ref_budget / max(args.steps, 1))
+        n, el = oracle_sample(inp, budget_s=args.ref_budget / max(args.steps, 1),
+                              act_scale_mode=ACT_SCALES[args.act_scale])
         tokens += n
         elapsed += el
         per.append(el)
@@ -236,7 +241,7 @@ def run_reference(args, cfg):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * elapsed / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_desc(cfg),
+        "config": dict(workload_desc(cfg), act_scale=args.act_scale),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{tokens} tokens of the {cfg.name} batch, one oracle call per token "
                                    f"(routing of all {cfg.T} tokens + that token's {cfg.k} expert FFNs, fp64)"},
@@ -260,7 +265,8 @@ def run_gpu(args, cfg):
     torch.cuda.set_device(device)
     inp = synth.make_inputs(cfg)
     c = cfg
-    layer = moe.MoELayer(c.H, c.I, c.E, c.k, c.T, c.score_func, device=device)
+    act_mode = ACT_SCALES[args.act_scale]
+    layer = moe.MoELayer(c.H, c.I, c.E, c.k, c.T, c.score_func, device=device, act_scale_mode=act_mode)
     layer.load_weights(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
     x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).to(f"cuda:{device}")
     y = torch.empty_like(x)
@@ -368,7 +374,7 @@ def run_gpu(args, cfg):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        n, el = oracle_sample(inp, budget_s=args.ref_budget)
+        n, el = oracle_sample(inp, budget_s=args.ref_budget, act_scale_mode=act_mode)
         cpu = {"value": n / el, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{n} tokens of the {cfg.name} batch, one oracle call per token "
                          f"(routing of all {cfg.T} tokens + that token's {cfg.k} expert FFNs, fp64)"}
@@ -377,7 +383,8 @@ def run_gpu(args, cfg):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e2m1 (fp32 accumulate)",
-            "data": "synthetic", "config": dict(workload_desc(cfg), parallelism=f"replicas{ws}",
+            "data": "synthetic", "config": dict(workload_desc(cfg), act_scale=args.act_scale,
+                                               parallelism=f"replicas{ws}",
                                                l2="inputs larger than L2: every step streams the active experts' "
                                                   "weights from HBM"),
             "roofline": roof,
@@ -410,6 +417,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--act-scale", default="e8m0", choices=sorted(ACT_SCALES),
+                    help="activation block scales: power-of-two E8M0 (default) or fp32 amax/448")
     ap.add_argument("--experts", type=int, default=None,
                     help="shrink the workload to this many experts (small profiling captures only)")
     ap.add_argument("--tokens", type=int, default=None,

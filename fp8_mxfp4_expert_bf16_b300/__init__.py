@@ -33,7 +33,11 @@ class MoEError(RuntimeError):
 class _Config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("num_experts", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("max_tokens", ctypes.c_int), ("score_func", ctypes.c_int),
-                ("device", ctypes.c_int)]
+                ("device", ctypes.c_int), ("act_scale_mode", ctypes.c_int)]
+
+
+ACT_SCALE_E8M0 = 0
+ACT_SCALE_F32 = 1
 
 
 _lib = None
@@ -68,6 +72,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_get_permutation": (S, [P, P]),
         "moe_get_act_quant": (S, [P, P, P]),
         "moe_get_inter_quant": (S, [P, P, P]),
+        "moe_get_act_scales_f32": (S, [P, P]),
+        "moe_get_inter_scales_f32": (S, [P, P]),
         "moe_get_expert_out": (S, [P, P]),
         "moe_set_profiling": (S, [P, I]),
         "moe_get_stage_times": (S, [P, P, I]),
@@ -115,12 +121,13 @@ class MoELayer:
     """
 
     def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, max_tokens: int,
-                 score_func: int = 0, device: int = 0):
+                 score_func: int = 0, device: int = 0, act_scale_mode: int = ACT_SCALE_E8M0):
         import torch  # noqa: F401  (device memory and streams)
         self.L = lib()
         self.H, self.I, self.E, self.k, self.max_tokens = hidden, inter, num_experts, top_k, max_tokens
         self.device = device
-        cfg = _Config(hidden, inter, num_experts, top_k, max_tokens, score_func, device)
+        self.act_scale_mode = act_scale_mode
+        cfg = _Config(hidden, inter, num_experts, top_k, max_tokens, score_func, device, act_scale_mode)
         h = ctypes.c_void_p()
         st = self.L.moe_init(ctypes.byref(cfg), ctypes.byref(h))
         if st != 0:
@@ -223,17 +230,39 @@ class MoELayer:
         return perm
 
     def act_quant(self):
+        """Q1 codes and block scales of the last forward: E8M0 bytes (u8), or
+        float32 scales for a handle in the fp32-scale mode."""
         q = np.empty((self.last_T, self.H), dtype=np.uint8)
-        s = np.empty((self.last_T, self.H // 128), dtype=np.uint8)
-        self._check(self.L.moe_get_act_quant(self.h, _ptr(q), _ptr(s)))
+        if self.act_scale_mode == ACT_SCALE_F32:
+            s = np.empty((self.last_T, self.H // 128), dtype=np.float32)
+            self._check(self.L.moe_get_act_quant(self.h, _ptr(q), None))
+            self._check(self.L.moe_get_act_scales_f32(self.h, _ptr(s)))
+        else:
+            s = np.empty((self.last_T, self.H // 128), dtype=np.uint8)
+            self._check(self.L.moe_get_act_quant(self.h, _ptr(q), _ptr(s)))
         return q, s
 
     def inter_quant(self):
+        """Q2 codes and block scales (perm order), as act_quant."""
         n = self.last_T * self.k
         q = np.empty((n, self.I), dtype=np.uint8)
-        s = np.empty((n, self.I // 128), dtype=np.uint8)
-        self._check(self.L.moe_get_inter_quant(self.h, _ptr(q), _ptr(s)))
+        if self.act_scale_mode == ACT_SCALE_F32:
+            s = np.empty((n, self.I // 128), dtype=np.float32)
+            self._check(self.L.moe_get_inter_quant(self.h, _ptr(q), None))
+            self._check(self.L.moe_get_inter_scales_f32(self.h, _ptr(s)))
+        else:
+            s = np.empty((n, self.I // 128), dtype=np.uint8)
+            self._check(self.L.moe_get_inter_quant(self.h, _ptr(q), _ptr(s)))
         return q, s
+
+    def block_scales_f32(self, which: str = "act"):
+        """Every block scale of Q1 ('act') or Q2 ('inter') as a float32 value."""
+        rows = self.last_T if which == "act" else self.last_T * self.k
+        width = self.H if which == "act" else self.I
+        s = np.empty((rows, width // 128), dtype=np.float32)
+        f = self.L.moe_get_act_scales_f32 if which == "act" else self.L.moe_get_inter_scales_f32
+        self._check(f(self.h, _ptr(s)))
+        return s
 
     def expert_out(self):
         out = np.empty((self.last_T * self.k, self.H), dtype=np.float32)

@@ -181,6 +181,8 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
         return fail(nullptr, MOE_ERR_SHAPE, "max_tokens=%d: must be in [1, 2^20]", c.max_tokens);
     if (c.score_func != MOE_SCORE_SIGMOID && c.score_func != MOE_SCORE_SOFTMAX)
         return fail(nullptr, MOE_ERR_INVALID_ARG, "score_func=%d", c.score_func);
+    if (c.act_scale_mode != MOE_ACT_SCALE_E8M0 && c.act_scale_mode != MOE_ACT_SCALE_F32)
+        return fail(nullptr, MOE_ERR_INVALID_ARG, "act_scale_mode=%d", c.act_scale_mode);
     if (cudaSetDevice(c.device) != cudaSuccess)
         return fail(nullptr, MOE_ERR_CUDA, "cudaSetDevice(%d) failed", c.device);
     cudaDeviceProp prop;
@@ -200,6 +202,7 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
     s.K = c.top_k;
     s.Tm = c.max_tokens;
     s.score_func = c.score_func;
+    s.act_f32 = c.act_scale_mode == MOE_ACT_SCALE_F32;
     s.KB1 = s.H / 128;
     s.KB2 = s.I / 128;
     s.NT1 = s.I / 128;
@@ -237,6 +240,10 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
     ALLOC(s.hq, (size_t)s.Rmax * s.I);
     ALLOC(s.hsf, sizeof(uint32_t) * (size_t)s.MTmax * s.KB2 * 128);
     ALLOC(s.obuf, sizeof(float) * (size_t)s.Rmax * s.H);
+    if (s.act_f32) {
+        ALLOC(s.asf32, sizeof(float) * (size_t)s.Rmax * s.KB1);
+        ALLOC(s.hsf32, sizeof(float) * (size_t)s.Rmax * s.KB2);
+    }
     ALLOC(s.err, sizeof(int32_t) * 4);
     ALLOC(h->xbuf, sizeof(uint16_t) * (size_t)s.Tm * s.H);
     ALLOC(h->ybuf, sizeof(uint16_t) * (size_t)s.Tm * s.H);
@@ -249,6 +256,9 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
               cudaMemset(s.hsf, 0, sizeof(uint32_t) * (size_t)s.MTmax * s.KB2 * 128) == cudaSuccess &&
               cudaMemset(s.err, 0, sizeof(int32_t) * 4) == cudaSuccess &&
               cudaMemset(s.n_mtiles, 0, sizeof(int32_t) * 4) == cudaSuccess;
+    if (ok && s.act_f32)
+        ok = cudaMemset(s.asf32, 0, sizeof(float) * (size_t)s.Rmax * s.KB1) == cudaSuccess &&
+             cudaMemset(s.hsf32, 0, sizeof(float) * (size_t)s.Rmax * s.KB2) == cudaSuccess;
     const uint32_t boxes[kNumABox] = {8, 16, 32, 64, 128};
     for (int i = 0; ok && i < kNumABox; ++i) {
         ok = make_map(&s.tm_aq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.aq, s.H, s.Rmax, s.H, 128, boxes[i]) &&
@@ -497,6 +507,9 @@ static moe_status get_quant(moe_handle* h, int which, uint8_t* q, uint8_t* sc)
 {
     moe_status r = getter_prologue(h);
     if (r != MOE_OK) return r;
+    if (sc && h->s.act_f32)
+        return fail(h, MOE_ERR_INVALID_ARG,
+                    "the handle keeps fp32 activation scales: pass scale = NULL and use the *_scales_f32 getter");
     const int T = h->last_T;
     const size_t rows = which == 0 ? (size_t)T : (size_t)T * h->s.K;
     const size_t width = which == 0 ? h->s.H : h->s.I;
@@ -514,6 +527,20 @@ static moe_status get_quant(moe_handle* h, int which, uint8_t* q, uint8_t* sc)
 }
 
 moe_status moe_get_act_quant(moe_handle* h, uint8_t* q, uint8_t* scale) { return get_quant(h, 0, q, scale); }
+
+static moe_status get_scales_f32(moe_handle* h, int which, float* out)
+{
+    moe_status r = getter_prologue(h);
+    if (r != MOE_OK) return r;
+    const int T = h->last_T;
+    const size_t rows = which == 0 ? (size_t)T : (size_t)T * h->s.K;
+    const size_t width = which == 0 ? h->s.H : h->s.I;
+    return with_tmp(h, sizeof(float) * rows * (width / 128), out,
+                    [&](void* d) { return launch_gather_scales_f32(h->s, T, which, static_cast<float*>(d), 0); });
+}
+
+moe_status moe_get_act_scales_f32(moe_handle* h, float* scale) { return get_scales_f32(h, 0, scale); }
+moe_status moe_get_inter_scales_f32(moe_handle* h, float* scale) { return get_scales_f32(h, 1, scale); }
 moe_status moe_get_inter_quant(moe_handle* h, uint8_t* q, uint8_t* scale) { return get_quant(h, 1, q, scale); }
 
 moe_status moe_get_expert_out(moe_handle* h, float* out)

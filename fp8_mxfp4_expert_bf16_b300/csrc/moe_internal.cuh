@@ -23,6 +23,7 @@ constexpr int kDevErrBounds = 2;
 
 struct DevState {
     int H, I, E, K, Tm, score_func;
+    int act_f32;         // activation blocks carry fp32 scales (amax / 448) instead of E8M0 ones
     int KB1, KB2;        // H/128, I/128: K-blocks of the two grouped GEMMs
     int NT1, NT2, BN2;   // n-tiles: G1 (I/128, 256 columns = gate 128 + up 128), G2 (H/BN2)
     int MTmax;           // max 128-row m-tiles: ceil(Tm*K/128) + E
@@ -59,6 +60,8 @@ struct DevState {
     uint32_t* asf;        // [MTmax][KB1][128] scale words in tcgen05.cp order
     uint8_t* hq;          // [Rmax][I]   e4m3 SwiGLU output
     uint32_t* hsf;        // [MTmax][KB2][128]
+    float* asf32;         // [Rmax][KB1] fp32 activation scales (fp32-scale mode only)
+    float* hsf32;         // [Rmax][KB2] fp32 SwiGLU-output scales (fp32-scale mode only)
     float* obuf;          // [Rmax][H]   expert outputs (fp32)
     int32_t* err;         // [4] error word, where, aux
 
@@ -114,6 +117,7 @@ cudaError_t launch_check_e8m0(const uint8_t* p, size_t n, int32_t* flag, cudaStr
 cudaError_t launch_unpad_perm(const DevState& s, int T, int32_t* out, cudaStream_t st);
 cudaError_t launch_gather_rows_u8(const DevState& s, int T, int which, uint8_t* q, uint8_t* sc, cudaStream_t st);
 cudaError_t launch_gather_obuf(const DevState& s, int T, float* out, cudaStream_t st);
+cudaError_t launch_gather_scales_f32(const DevState& s, int T, int which, float* out, cudaStream_t st);
 // router on the tensor cores (router_gemm.cu)
 cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, cudaStream_t st, int ksplit = 1);
 int router_split(int T, int H);

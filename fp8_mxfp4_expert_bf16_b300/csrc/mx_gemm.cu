@@ -81,6 +81,7 @@ constexpr uint32_t kBHalfTxBytes = 128 * 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;      // accumulator: 256 fp32 columns
 constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), SFB at +8 (8 cols)
+constexpr uint32_t kSFUnitCol = 352; // fp32-scale mode: a constant unit activation scale chunk (4 cols)
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, epilogue warps
 
@@ -103,6 +104,10 @@ struct GemmArgs {
     // down epilogue
     float* obuf;                 // [R][H]
     int H;
+    // fp32-scale mode: the activation rows' fp32 block scales [R][KB], and
+    // (gate/up) the output table for the SwiGLU rows' scales [R][I/128]
+    const float* as32;
+    float* hs32;
     int early_trigger;           // let the next kernel be scheduled right after the wait (else at the end)
     int32_t* err;
 };
@@ -115,10 +120,13 @@ struct PhaseCtl {
     uint64_t acc_empty;
     uint64_t drain;
     uint64_t red_full[2];
+    uint64_t pfull;               // fp32-scale mode: a K-step's partial product is in TMEM
+    uint64_t pempty;              // fp32-scale mode: every epilogue warp has read it
     float red[2][8][32];          // per-warp row amax halves, double-buffered by tile parity
 };
 
 struct GemmCtl {
+    uint32_t unit_sf[128];        // fp32-scale mode: E8M0 1.0 in every byte (a tcgen05.cp chunk)
     PhaseCtl<Shape<true>::kStages> light;
     PhaseCtl<Shape<false>::kStages> heavy;
     uint32_t tmem_base;
@@ -148,6 +156,8 @@ __device__ __forceinline__ void init_phase(PhaseCtl<kStages>& pc)
     mbar_init(smem_u32(&pc.red_full[0]), kEpiWarps);
     mbar_init(smem_u32(&pc.red_full[1]), kEpiWarps);
     mbar_init(smem_u32(&pc.drain), 1);
+    mbar_init(smem_u32(&pc.pfull), 1);
+    mbar_init(smem_u32(&pc.pempty), kEpiWarps);
 }
 
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
@@ -264,7 +274,7 @@ __device__ __forceinline__ void store_rows_transposed(uint32_t taddr, int live_r
 // role drains its own work before returning: the producer waits until its
 // copies have landed, the MMA issuer until its MMAs have completed, the
 // epilogue has read its last accumulator.
-template <int kMode, bool kLight>
+template <int kMode, bool kLight, bool kF32S>
 __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<Shape<kLight>::kStages>& pc,
                                            uint32_t tmem, const CUtensorMap* tmA0, const CUtensorMap* tmA1,
                                            const CUtensorMap* tmA2, const CUtensorMap* tmW, const GemmArgs& args,
@@ -305,7 +315,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 const int sel = rows <= S::kBox0 ? 0 : (rows <= S::kBox1 ? 1 : 2);
                 const CUtensorMap* tA = sel == 0 ? tmA0 : (sel == 1 ? tmA1 : tmA2);
                 const uint32_t a_bytes = (uint32_t)(sel == 0 ? S::kBox0 : (sel == 1 ? S::kBox1 : S::kBox2)) * 128u;
-                const uint32_t tx = a_bytes + args.halves * (kBHalfTxBytes + 512) + 512;
+                const uint32_t tx = a_bytes + args.halves * (kBHalfTxBytes + 512) + (kF32S ? 0u : 512u);
                 // first row of this tile's interleaved weight blocks
                 const size_t wrow0 = ((size_t)(e * NT + nt) * KB) * args.halves * kWBlockRowsPerHalf;
                 const uint32_t* sfa = args.sfa + (size_t)mt * KB * 128;
@@ -330,7 +340,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         uint8_t* st = smem + kb * kStageStride;
                         const uint32_t fb = smem_u32(&pc.full[kb]);
                         tma_load_2d(smem_u32(st), tA, fb, kb * kBK, mt * kBM);
-                        bulk_load(smem_u32(st + kSFAOff), sfa + (size_t)kb * 128, 512, fb);
+                        if constexpr (!kF32S) bulk_load(smem_u32(st + kSFAOff), sfa + (size_t)kb * 128, 512, fb);
                     }
                 }
                 for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -349,7 +359,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                     // the stage's weight rows (both halves) are one box; its scale chunks follow them
                     const size_t wrow = wrow0 + (size_t)kb * args.halves * kWBlockRowsPerHalf;
                     tma_load_2d(smem_u32(st + S::kBOff), tmW, fb, 0, (int)wrow);
-                    bulk_load(smem_u32(st + kSFAOff), sfa + (size_t)kb * 128, 512, fb);
+                    if constexpr (!kF32S) bulk_load(smem_u32(st + kSFAOff), sfa + (size_t)kb * 128, 512, fb);
                     bulk_load(smem_u32(st + kSFBOff), args.wq + (wrow + (size_t)args.halves * 128) * 64,
                               args.halves * 512, fb);
                     issued[s] = true;
@@ -368,6 +378,44 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
             const uint32_t idesc = idesc_mxf8f6f4(128, 128 * args.halves, kTypeE4M3, kTypeE2M1);
             int it = 0, tcount = 0;
             bool ok = true;
+            if constexpr (kF32S) {
+                // One partial product per K-step (unit activation scales, the
+                // weights' own E8M0 scales), handed to the epilogue, which folds
+                // the rows' fp32 scales in; the next K-step's MMAs wait until
+                // every epilogue warp has read it.
+                tmem_cp_32x128b_warpx4(tmem + kSFUnitCol, desc_sf_chunk(smem_u32(g->unit_sf)));
+                int ks = 0;
+                for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                    for (int kb = 0; kb < KB; ++kb, ++it, ++ks) {
+                        const int s = it % kStages;
+                        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+                        if (!mbar_wait(smem_u32(&pc.full[s]), ph, abrt)) {
+                            raise_error(g, args.err, 8);
+                            ok = false;
+                            break;
+                        }
+                        if (ks > 0 && !mbar_wait(smem_u32(&pc.pempty), (uint32_t)(ks - 1) & 1u, abrt)) {
+                            raise_error(g, args.err, 9);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t st = smem_u32(smem + s * kStageStride);
+                        const uint32_t sfb_t = tmem + kSFCol + 16u * s + 8u;
+                        tmem_cp_32x128b_warpx4(sfb_t, desc_sf_chunk(st + kSFBOff));
+                        if (args.halves == 2) tmem_cp_32x128b_warpx4(sfb_t + 4u, desc_sf_chunk(st + kSFBOff + 512));
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t ad = desc_kmajor_sw128(st + 32u * k);
+                            const uint64_t bd = desc_kmajor_sw128(st + S::kBOff + 32u * k);
+                            mma_mxf8f6f4(tmem + kAccCol, ad, bd, idesc_with_sf_id(idesc, k, k), tmem + kSFUnitCol,
+                                         sfb_t, k != 0 ? 1u : 0u);
+                        }
+                        tc_commit(smem_u32(&pc.empty[s]));
+                        tc_commit(smem_u32(&pc.pfull));
+                    }
+                }
+            } else
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
                 if (tcount > 0 && !mbar_wait(smem_u32(&pc.acc_empty), (uint32_t)(tcount - 1) & 1u, abrt)) {
                     raise_error(g, args.err, 3);
@@ -416,6 +464,106 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
         const int row = q * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         int tcount = 0;
+        if constexpr (kF32S) {
+            // fp32-scale mode: per K-step, this warp's 128 partial columns are
+            // read from TMEM and folded into fp32 registers with the row's
+            // scale (acc += s * partial, K-steps in order); warps without live
+            // rows still take part in each K-step's hand-off.
+            constexpr int kW = 128;
+            int ks = 0;
+            // the scales come from the previous kernel (quantisation, or the
+            // gate/up GEMM): wait for it before the first read
+            griddep_wait();
+            for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tcount) {
+                const int mt = list[tile / NT], nt = tile - (tile / NT) * NT;
+                const int rows = args.mtile_rows[mt];
+                const bool warp_live = q * 32 < rows;
+                const bool row_live = row < rows;
+                const int ncw = kMode == 0 ? 128 : 64 * args.halves;     // this warp's columns
+                // gate/up: gate columns [64 hw, +64) then up columns [128 + 64 hw, +64);
+                // down: columns [hw * ncw, +ncw)
+                const uint32_t c0 = kMode == 0 ? 64u * hw : (uint32_t)(hw * ncw);
+                const uint32_t c1 = kMode == 0 ? 128u + 64u * hw : c0 + 64u;
+                const float* srow = args.as32 + (size_t)(mt * kBM + row) * KB;
+                float acc[kW];
+#pragma unroll
+                for (int j = 0; j < kW; ++j) acc[j] = 0.0f;
+                float s_next = row_live ? srow[0] : 0.0f;
+                bool ok = true;
+                for (int kb = 0; kb < KB; ++kb, ++ks) {
+                    const float sc = s_next;
+                    if (kb + 1 < KB) s_next = row_live ? srow[kb + 1] : 0.0f;
+                    if (!mbar_wait(smem_u32(&pc.pfull), (uint32_t)ks & 1u, abrt)) {
+                        raise_error(g, args.err, 10);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (warp_live) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            if (32 * c < ncw) {
+                                uint32_t pv[32];
+                                tmem_ld32(tl + kAccCol + (c < 2 ? c0 + 32u * c : c1 + 32u * (c - 2)), pv);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(sc, __uint_as_float(pv[j]), acc[32 * c + j]);
+                            }
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&pc.pempty));
+                }
+                if (!ok) break;
+                if (kMode == 0) {
+                    // h = silu(g) * u on the promoted sums, then the fp32-scale
+                    // re-quantisation of the row's 128-wide block
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        const float gf = row_live ? acc[j] : 0.0f;
+                        const float uf = row_live ? acc[64 + j] : 0.0f;
+                        acc[j] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
+                    }
+                    float amax = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) amax = fmaxf(amax, fabsf(acc[j]));
+                    const int p = tcount & 1;
+                    pc.red[p][ew][lane] = amax;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&pc.red_full[p]));
+                    if (!mbar_wait(smem_u32(&pc.red_full[p]), (uint32_t)(tcount >> 1) & 1u, abrt)) {
+                        raise_error(g, args.err, 11);
+                        break;
+                    }
+                    amax = fmaxf(amax, pc.red[p][ew ^ 4][lane]);
+                    if (row_live) {
+                        const float s2 = __fdiv_rn(amax, 448.0f);
+                        uint4* dst =
+                            reinterpret_cast<uint4*>(args.hq + (size_t)(mt * kBM + row) * args.I + nt * 128 + 64 * hw);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                const float* hv = acc + 16 * v + 4 * w;
+                                w4[w] = amax > 0.0f ? e4m3x4(__fdiv_rn(hv[0], s2), __fdiv_rn(hv[1], s2),
+                                                             __fdiv_rn(hv[2], s2), __fdiv_rn(hv[3], s2))
+                                                    : 0u;
+                            }
+                            dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                        }
+                        if (hw == 0) args.hs32[(size_t)(mt * kBM + row) * (args.I / 128) + nt] = s2;
+                    }
+                } else if (row_live) {
+                    float4* d4 = reinterpret_cast<float4*>(args.obuf + (size_t)(mt * kBM + row) * args.H +
+                                                           (size_t)nt * (128 * args.halves) + c0);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (4 * j < ncw) d4[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                }
+            }
+        } else
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tcount) {
             const int mt = list[tile / NT], nt = tile - (tile / NT) * NT;
             const int rows = args.mtile_rows[mt];
@@ -506,7 +654,9 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
     }
 }
 
-template <int kMode>   // mode 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows
+// mode 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows; kF32S: the
+// activation blocks carry fp32 scales (promotion in the epilogue)
+template <int kMode, bool kF32S>
 __global__ void __launch_bounds__(kThreads, 1)
     k_mx_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
               const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
@@ -517,6 +667,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     GemmCtl* g = reinterpret_cast<GemmCtl*>(smem + kRingBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    if (kF32S) {
+        for (int i = threadIdx.x; i < 128; i += blockDim.x) g->unit_sf[i] = 0x7F7F7F7Fu;   // E8M0 1.0
+        fence_proxy_async_smem();   // generic-proxy writes above, read by tcgen05.cp
+    }
     if (threadIdx.x == 0) {
         init_phase(g->light);
         init_phase(g->heavy);
@@ -539,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = g->tmem_base;
     bool waited = false;   // the producer's wait for the previous kernel (producer thread only)
 
-    gemm_phase<kMode, true>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args, args.light_list,
+    gemm_phase<kMode, true, kF32S>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args, args.light_list,
                             *args.light_count, waited);
     // the heavy phase reuses the ring and the accumulator: every role of the
     // light phase has drained its own work
@@ -547,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (!*(volatile int*)&g->abort)
-        gemm_phase<kMode, false>(smem, g, g->heavy, tmem, &tmA2, &tmA3, &tmA4, &tmW, args, args.heavy_list,
+        gemm_phase<kMode, false, kF32S>(smem, g, g->heavy, tmem, &tmA2, &tmA3, &tmA4, &tmW, args, args.heavy_list,
                                  *args.heavy_count, waited);
     // a CTA without tiles still waits before it lets the next kernel start
     if (warp == 0 && lane == 0) {
@@ -565,8 +719,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t gemm_set_attributes()
 {
-    cudaError_t e = cudaFuncSetAttribute(k_mx_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_mx_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_mx_gemm<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_mx_gemm<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_mx_gemm<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_mx_gemm<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     return e;
 }
 
@@ -616,16 +775,27 @@ cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
 {
     GemmArgs a = gemm1_args(s);
     a.early_trigger = 1;   // the down GEMM follows
-    return launch_kernel(k_mx_gemm<0>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_aq[0], s.tm_aq[1],
-                         s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13, a);
+    if (s.act_f32) {
+        a.as32 = s.asf32;
+        a.hs32 = s.hsf32;
+        return launch_kernel(k_mx_gemm<0, true>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_aq[0],
+                             s.tm_aq[1], s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13, a);
+    }
+    return launch_kernel(k_mx_gemm<0, false>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_aq[0],
+                         s.tm_aq[1], s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13, a);
 }
 
 cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
 {
     GemmArgs a = gemm2_args(s);
     a.early_trigger = 0;   // the combine follows
-    return launch_kernel(k_mx_gemm<1>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_hq[0], s.tm_hq[1],
-                         s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2, a);
+    if (s.act_f32) {
+        a.as32 = s.hsf32;
+        return launch_kernel(k_mx_gemm<1, true>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_hq[0],
+                             s.tm_hq[1], s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2, a);
+    }
+    return launch_kernel(k_mx_gemm<1, false>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_hq[0],
+                         s.tm_hq[1], s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2, a);
 }
 
 }  // namespace moe

@@ -406,6 +406,34 @@ __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restric
     if (lane < K) asf[sf_word_index(my_row >> 7, b, KB, my_row & 127)] = (uint32_t)(ex + 127) * 0x01010101u;
 }
 
+// The fp32-scale variant: s = amax / 448 and codes e4m3(v / s), both fp32
+// divisions rounded to nearest (an all-zero block: s = 0, zero codes); s goes
+// to the fp32 scale table of every destination row.
+__global__ void __launch_bounds__(256) k_quant_scatter_f32s(const uint16_t* __restrict__ x,
+                                                            const int32_t* __restrict__ prow, uint8_t* __restrict__ aq,
+                                                            float* __restrict__ asf32, int T, int H, int K)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    const int KB = H / 128, lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (gw >= (long long)T * KB) return;
+    const int t = (int)(gw / KB), b = (int)(gw - (long long)t * KB);
+    const int my_row = lane < K ? prow[(size_t)t * K + lane] : 0;
+    const uint2 v = *reinterpret_cast<const uint2*>(x + (size_t)t * H + b * 128 + lane * 4);
+    const float f0 = bf16_lo(v.x), f1 = bf16_hi(v.x), f2 = bf16_lo(v.y), f3 = bf16_hi(v.y);
+    const float amax = warp_max(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+    const float sc = __fdiv_rn(amax, 448.0f);
+    const uint32_t word = amax > 0.0f ? e4m3x4(__fdiv_rn(f0, sc), __fdiv_rn(f1, sc), __fdiv_rn(f2, sc),
+                                               __fdiv_rn(f3, sc))
+                                      : 0u;
+    for (int j = 0; j < K; ++j) {
+        const int row = __shfl_sync(0xffffffffu, my_row, j);
+        *reinterpret_cast<uint32_t*>(aq + (size_t)row * H + b * 128 + lane * 4) = word;
+    }
+    if (lane < K) asf32[(size_t)my_row * KB + b] = sc;
+}
+
 // Small batches (T <= 256, one dispatch chunk): one block builds the expert
 // histogram and token bit-masks, the scan and m-tile lists, and the stable
 // ranks - the work of k_chunk_hist, k_scan and k_scatter_rows in a single
@@ -490,6 +518,9 @@ cudaError_t launch_dispatch_small(const DevState& s, int T, cudaStream_t st)
 cudaError_t launch_quant_scatter(const DevState& s, const uint16_t* x, int T, cudaStream_t st)
 {
     const long long warps = (long long)T * (s.H / 128);
+    if (s.act_f32)
+        return launch_kernel(k_quant_scatter_f32s, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, st, s.pdl, x,
+                             (const int32_t*)s.prow, s.aq, s.asf32, T, s.H, s.K);
     return launch_kernel(k_quant_scatter, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, st, s.pdl, x,
                          (const int32_t*)s.prow, s.aq, s.asf, T, s.H, s.K);
 }
@@ -703,6 +734,39 @@ __global__ void k_gather_q(const uint8_t* __restrict__ src, const uint32_t* __re
         if (q) q[(size_t)r * width + i] = src[(size_t)prw * width + i];
     for (int kb = threadIdx.x; kb < KB; kb += blockDim.x)
         if (sc) sc[(size_t)r * KB + kb] = (uint8_t)(sf[sf_word_index(prw >> 7, kb, KB, prw & 127)] & 0xFFu);
+}
+
+// Block scales of the rows of a getter as fp32 values: E8M0 bytes decoded
+// (2^(b-127)), or the fp32-scale table as stored.
+__global__ void k_gather_scales_f32(const uint32_t* __restrict__ sf, const float* __restrict__ sf32, const int32_t* prow,
+                                    const int32_t* offsets, const int32_t* mtile_off, int E, int K, int KB, int which,
+                                    float* __restrict__ out)
+{
+    const int r = blockIdx.x;
+    const int prw = (which == 0) ? prow[(size_t)r * K] : padded_row_of(offsets, mtile_off, E, r);
+    for (int kb = threadIdx.x; kb < KB; kb += blockDim.x) {
+        float v;
+        if (sf32) {
+            v = sf32[(size_t)prw * KB + kb];
+        } else {
+            const int b = (int)(sf[sf_word_index(prw >> 7, kb, KB, prw & 127)] & 0xFFu);
+            v = b == 0 ? 0x1p-127f : __int_as_float(b << 23);   // 2^(b - 127); byte 0 is 2^-127 (subnormal)
+        }
+        out[(size_t)r * KB + kb] = v;
+    }
+}
+
+cudaError_t launch_gather_scales_f32(const DevState& s, int T, int which, float* out, cudaStream_t st)
+{
+    const int rows = (which == 0) ? T : T * s.K;
+    if (rows == 0) return cudaSuccess;
+    if (which == 0)
+        k_gather_scales_f32<<<rows, 128, 0, st>>>(s.asf, s.act_f32 ? s.asf32 : nullptr, s.prow, s.offsets,
+                                                  s.mtile_off, s.E, s.K, s.H / 128, 0, out);
+    else
+        k_gather_scales_f32<<<rows, 128, 0, st>>>(s.hsf, s.act_f32 ? s.hsf32 : nullptr, s.prow, s.offsets,
+                                                  s.mtile_off, s.E, s.K, s.I / 128, 1, out);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gather_rows_u8(const DevState& s, int T, int which, uint8_t* q, uint8_t* sc, cudaStream_t st)

@@ -68,6 +68,18 @@ typedef struct moe_handle moe_handle;
 
 enum { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SOFTMAX = 1 };
 
+/* Activation scale of the 1 x 128 e4m3 blocks (both the layer input and the
+ * SwiGLU output).  The pages say only "block-wise e4m3" (vLLM recipe
+ * "XiaomiMiMo/MiMo-V2.6-Pro-RL", "Overview") and "dynamic activation
+ * scheme" (devupai "MiMo-V2.6-Flash", "Self-Hosting"):
+ *   MOE_ACT_SCALE_E8M0: a power-of-two scale per block, the smallest that
+ *     keeps the block's amax within 448 (the scale the block-scaled tensor
+ *     cores take directly; the default);
+ *   MOE_ACT_SCALE_F32: s = amax / 448 per block in fp32, codes e4m3 of the
+ *     fp32 quotient v / s (an all-zero block: s = 0, zero codes); the GEMMs
+ *     then fold s into fp32 partial sums per 128-wide K block. */
+enum { MOE_ACT_SCALE_E8M0 = 0, MOE_ACT_SCALE_F32 = 1 };
+
 typedef struct {
     int hidden;       /* H: multiple of 128, 128..16384 */
     int inter;        /* I: multiple of 128, 128..16384 */
@@ -76,6 +88,7 @@ typedef struct {
     int max_tokens;   /* workspace is sized for 0 <= T <= max_tokens (>= 1) */
     int score_func;   /* MOE_SCORE_SIGMOID (the pages' router) or MOE_SCORE_SOFTMAX */
     int device;       /* CUDA device ordinal; the device must be sm_103 */
+    int act_scale_mode; /* MOE_ACT_SCALE_E8M0 (0, default) or MOE_ACT_SCALE_F32 */
 } moe_config;
 
 /* Create a handle: checks the configuration and the device, allocates the
@@ -127,6 +140,10 @@ moe_status moe_forward_host(moe_handle* h, const uint16_t* x_host, int T, uint16
  *   act q    u8 [T][H] e4m3 codes of x, scale u8 [T][H/128] E8M0 bytes
  *   inter q  u8 [T*k][I] e4m3 codes of silu(g)*u in perm order,
  *            scale u8 [T*k][I/128]
+ *   (with MOE_ACT_SCALE_F32 the u8 scale outputs must be NULL: the scales
+ *   are fp32 and come from the two *_scales_f32 getters, which in either
+ *   mode return every block scale as its fp32 value, [T][H/128] and
+ *   [T*k][I/128])
  *   expert_out fp32 [T*k][H]: o of every (token, slot) row in perm order
  * Any output pointer may be NULL to skip it. */
 moe_status moe_get_logits(moe_handle* h, float* logits);
@@ -135,6 +152,8 @@ moe_status moe_get_expert_counts(moe_handle* h, int32_t* counts, int32_t* offset
 moe_status moe_get_permutation(moe_handle* h, int32_t* perm);
 moe_status moe_get_act_quant(moe_handle* h, uint8_t* q, uint8_t* scale);
 moe_status moe_get_inter_quant(moe_handle* h, uint8_t* q, uint8_t* scale);
+moe_status moe_get_act_scales_f32(moe_handle* h, float* scale);
+moe_status moe_get_inter_scales_f32(moe_handle* h, float* scale);
 moe_status moe_get_expert_out(moe_handle* h, float* out);
 
 /* Per-stage timing of subsequent forwards: CUDA events recorded between the
