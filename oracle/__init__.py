@@ -296,7 +296,21 @@ def silu(g: np.ndarray) -> np.ndarray:
     return g / (1.0 + np.exp(-g))
 
 
-def expert_ffn(a: np.ndarray, w13_q, w13_s, w2_q, w2_s, act_scale_mode: int = ACT_SCALE_E8M0):
+def fp8_block_decode(q: np.ndarray, s: np.ndarray, blk: int = 128) -> np.ndarray:
+    """Exact values of an expert matrix in the fp8 block format: e4m3 codes
+    q [R, K] times the fp32 scale of their blk x blk block, s [R/blk, K/blk].
+
+    [P5 "Why Are the V2.6 Files Half the Size of V2.5?": the V2.5 experts
+    are stored in FP8 (e4m3) with block scales; the 128 x 128 block size is
+    the one P2 "Overview" names for its block-wise FP8 computation.]
+    """
+    vals = e4m3_decode_array(q)
+    sc = np.repeat(np.repeat(s.astype(np.float64), blk, axis=-2), blk, axis=-1)
+    return vals * sc
+
+
+def expert_ffn(a: np.ndarray, w13_q, w13_s, w2_q, w2_s, act_scale_mode: int = ACT_SCALE_E8M0,
+               weight_format: str = "mxfp4"):
     """One expert's SwiGLU FFN on exact activation values a [n, H].
 
     [P5 "How Big Is Each Expert?": gate, up and down projections around a
@@ -307,13 +321,14 @@ def expert_ffn(a: np.ndarray, w13_q, w13_s, w2_q, w2_s, act_scale_mode: int = AC
     Returns (h fp64 [n, I], hq u8 [n, I], hs [n, I/128] (E8M0 bytes or fp32),
     o fp64 [n, H]).
     """
-    W13 = mxfp4_decode(w13_q, w13_s)
+    decode = fp8_block_decode if weight_format == "fp8" else mxfp4_decode
+    W13 = decode(w13_q, w13_s)
     I2 = W13.shape[0]
     I = I2 // 2
     gu = a @ W13.T
     h = silu(gu[:, :I]) * gu[:, I:]
     hq, hs = act_quant(h, 128, act_scale_mode)
-    W2 = mxfp4_decode(w2_q, w2_s)
+    W2 = decode(w2_q, w2_s)
     o = act_dequant(hq, hs, 128) @ W2.T
     return h, hq, hs, o
 
@@ -337,7 +352,7 @@ class Forward:
 
 def forward(x_bf16, router_w_bf16, w13_q, w13_s, w2_q, w2_s, k: int,
             score_func: int = SCORE_SIGMOID, logit_bias=None, sel_bias=None,
-            tokens=None, act_scale_mode: int = ACT_SCALE_E8M0) -> Forward:
+            tokens=None, act_scale_mode: int = ACT_SCALE_E8M0, weight_format: str = "mxfp4") -> Forward:
     """The whole layer: route, dispatch, quantise, experts, combine.
 
     Routing, counts, offsets and the permutation cover every token; the
@@ -352,7 +367,7 @@ def forward(x_bf16, router_w_bf16, w13_q, w13_s, w2_q, w2_s, k: int,
     n = toks.size
     aq, as_ = act_quant(bf16_to_f64(x_bf16[toks]), 128, act_scale_mode)
     a = act_dequant(aq, as_, 128)
-    I = w2_q.shape[2] * 2
+    I = w2_q.shape[2] * (1 if weight_format == "fp8" else 2)
     hq = np.zeros((n, k, I), dtype=np.uint8)
     hs = np.zeros((n, k, I // 128), dtype=np.float32 if act_scale_mode == ACT_SCALE_F32 else np.uint8)
     h = np.zeros((n, k, I), dtype=np.float64)
@@ -360,7 +375,8 @@ def forward(x_bf16, router_w_bf16, w13_q, w13_s, w2_q, w2_s, k: int,
     sel = r.ids[toks]
     for e in np.unique(sel):
         rows, slots = np.nonzero(sel == e)
-        h_e, hq_e, hs_e, o_e = expert_ffn(a[rows], w13_q[e], w13_s[e], w2_q[e], w2_s[e], act_scale_mode)
+        h_e, hq_e, hs_e, o_e = expert_ffn(a[rows], w13_q[e], w13_s[e], w2_q[e], w2_s[e], act_scale_mode,
+                                          weight_format)
         h[rows, slots] = h_e
         hq[rows, slots] = hq_e
         hs[rows, slots] = hs_e

@@ -52,6 +52,7 @@ def _L():
         lib.syn_normal_f32.argtypes = [u64, u64, f, sz, p, p, i]
         lib.syn_mxfp4_experts.argtypes = [u64, u64, i, i, i, f, p, p, p, i]
         lib.syn_expert_f32.argtypes = [u64, u64, i, i, i, f, p, p, i]
+        lib.syn_fp8_experts.argtypes = [u64, u64, i, i, i, f, p, p, p, i]
         from scipy.special import ndtri
         n = 4096
         pts = np.arange(n + 1, dtype=np.float64) / n
@@ -82,6 +83,15 @@ def mxfp4_experts(seed: int, stream_base: int, E: int, rows: int, K: int, sigma:
     scale = np.empty((E, rows, K // 32), dtype=np.uint8)
     _L().syn_mxfp4_experts(seed, stream_base, E, rows, K, sigma, _p(packed), _p(scale), _p(_tab), _tab.size - 1)
     return packed, scale
+
+
+def fp8_experts(seed: int, stream_base: int, E: int, rows: int, K: int, sigma: float):
+    """The same draws as ``mxfp4_experts`` stored as e4m3 codes u8 [E, rows, K]
+    with one fp32 scale (amax / 448) per 128 x 128 block, f32 [E, rows/128, K/128]."""
+    q = np.empty((E, rows, K), dtype=np.uint8)
+    s = np.empty((E, rows // 128, K // 128), dtype=np.float32)
+    _L().syn_fp8_experts(seed, stream_base, E, rows, K, sigma, _p(q), _p(s), _p(_tab), _tab.size - 1)
+    return q, s
 
 
 def expert_f32(seed: int, stream_base: int, E: int, rows: int, K: int, sigma: float) -> np.ndarray:
@@ -128,11 +138,12 @@ class Inputs:
     router_w: np.ndarray     # u16 bf16 [E, H]
     logit_bias: np.ndarray   # f32 [E]
     sel_bias: np.ndarray     # f32 [E] (zero: the correction bias of a freshly initialised router)
-    w13_q: np.ndarray        # u8 [E, 2I, H/2]  gate rows [0, I), up rows [I, 2I)
-    w13_s: np.ndarray        # u8 [E, 2I, H/32]
-    w2_q: np.ndarray         # u8 [E, H, I/2]
-    w2_s: np.ndarray         # u8 [E, H, I/32]
+    w13_q: np.ndarray        # mxfp4: u8 [E, 2I, H/2] (gate rows [0, I), up rows [I, 2I)); fp8: u8 e4m3 [E, 2I, H]
+    w13_s: np.ndarray        # mxfp4: u8 E8M0 [E, 2I, H/32]; fp8: f32 [E, 2I/128, H/128]
+    w2_q: np.ndarray         # mxfp4: u8 [E, H, I/2]; fp8: u8 e4m3 [E, H, I]
+    w2_s: np.ndarray         # mxfp4: u8 [E, H, I/32]; fp8: f32 [E, H/128, I/128]
     extra: dict = field(default_factory=dict)
+    weight_format: str = "mxfp4"   # "mxfp4" or "fp8" (e4m3 + fp32 scale per 128 x 128 block)
 
 
 def logit_bias(cfg: Config) -> np.ndarray:
@@ -155,9 +166,10 @@ def logit_bias(cfg: Config) -> np.ndarray:
     raise ValueError(cfg.bias)
 
 
-def make_inputs(cfg: Config | str, T: int | None = None, x_only: bool = False) -> Inputs:
+def make_inputs(cfg: Config | str, T: int | None = None, x_only: bool = False, weights: str = "mxfp4") -> Inputs:
     """Draw one workload: x ~ bf16(N(0,1)), Wr ~ bf16(N(0, 0.02^2)),
-    expert weights fp32 N(0, 0.02^2) stored as MXFP4."""
+    expert weights fp32 N(0, 0.02^2) stored as MXFP4 (or, with
+    weights="fp8", as e4m3 with an fp32 scale per 128 x 128 block)."""
     if isinstance(cfg, str):
         cfg = CONFIGS[cfg]
     T = cfg.T if T is None else T
@@ -166,18 +178,23 @@ def make_inputs(cfg: Config | str, T: int | None = None, x_only: bool = False) -
     if x_only:
         return Inputs(cfg, x, None, None, None, None, None, None, None)
     wr = normal_bf16(s, _S_WR, 0.02, (cfg.E, cfg.H))
-    w13_q, w13_s = mxfp4_experts(s, _S_W13, cfg.E, 2 * cfg.I, cfg.H, 0.02)
-    w2_q, w2_s = mxfp4_experts(s, _S_W2, cfg.E, cfg.H, cfg.I, 0.02)
+    store = fp8_experts if weights == "fp8" else mxfp4_experts
+    w13_q, w13_s = store(s, _S_W13, cfg.E, 2 * cfg.I, cfg.H, 0.02)
+    w2_q, w2_s = store(s, _S_W2, cfg.E, cfg.H, cfg.I, 0.02)
     return Inputs(cfg, x, wr, logit_bias(cfg), np.zeros(cfg.E, dtype=np.float32),
-                  w13_q, w13_s, w2_q, w2_s)
+                  w13_q, w13_s, w2_q, w2_s, weight_format=weights)
 
 
-def custom_inputs(T, H, E, I, k, seed, bias="none", score_func=0) -> Inputs:
+def custom_inputs(T, H, E, I, k, seed, bias="none", score_func=0, weights="mxfp4") -> Inputs:
     """A workload of any shape (edge cases in the tests)."""
-    return make_inputs(Config(f"custom-{T}-{H}-{E}-{I}-{k}", T, H, E, I, k, seed, bias, score_func))
+    return make_inputs(Config(f"custom-{T}-{H}-{E}-{I}-{k}", T, H, E, I, k, seed, bias, score_func),
+                       weights=weights)
 
 
-def expert_weight_bytes(H: int, I: int) -> int:
-    """Bytes of one expert in MXFP4: 3*H*I weights at 4 bits plus one scale
-    byte per 32 weights (4.25 bits per weight)."""
+def expert_weight_bytes(H: int, I: int, weights: str = "mxfp4") -> int:
+    """Bytes of one expert: MXFP4, 3*H*I weights at 4 bits plus one scale
+    byte per 32 weights (4.25 bits per weight); fp8, one byte per weight plus
+    a 4-byte scale per 128 x 128 block."""
+    if weights == "fp8":
+        return 3 * H * I + 4 * (3 * H * I // (128 * 128))
     return 3 * H * I // 2 + 3 * H * I // 32

@@ -14,7 +14,9 @@
  * Expert weights are drawn in fp32 and stored as MXFP4 with the OCP MX v1.0
  * rule (shared exponent floor(log2(amax)) - 2 per 32 values, E2M1 codes by
  * round-to-nearest with ties to the even code, saturating at 6), packed two
- * codes per byte with the first element in the low nibble.
+ * codes per byte with the first element in the low nibble - or, for the fp8
+ * expert format, as e4m3 codes with one fp32 scale (amax / 448) per 128 x
+ * 128 block.
  */
 #include <math.h>
 #include <stdint.h>
@@ -140,6 +142,58 @@ void syn_mxfp4_experts(uint64_t seed, uint64_t stream_base, int E, int rows, int
                     buf[c] = sigma * normal_from(draw(key, (uint64_t)r * K + c0 + c), tab, n_tab);
                 mxfp4_row(buf, n, packed + (size_t)er * (K / 2) + c0 / 2, scale + (size_t)er * (K / 32) + c0 / 32);
             }
+        }
+    }
+}
+
+/* e4m3 (e4m3fn: bias 7, no infinities, 448 the largest finite value) code of
+ * a finite fp32 value, round to nearest with ties to even, saturating at 448.
+ * Used only to store synthetic fp8 expert weights. */
+static uint8_t e4m3_code(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80u : 0u;
+    float a = fabsf(v);
+    if (a >= 464.0f) return sign | 0x7Eu;   /* 464 rounds up past 448: saturate */
+    if (a < 0.015625f) {                    /* below 2^-6: steps of 2^-9 */
+        int m = (int)nearbyintf(a * 512.0f);
+        return sign | (uint8_t)m;           /* m == 8 is the smallest normal, code 8 */
+    }
+    int p;
+    (void)frexpf(a, &p);                    /* a = f * 2^p, f in [0.5, 1): exponent p - 1 */
+    int e = p - 1;
+    int m = (int)nearbyintf(ldexpf(a, 3 - e));   /* 8..16 */
+    if (m == 16) { e += 1; m = 8; }
+    if (e > 8 || (e == 8 && m > 14)) return sign | 0x7Eu;
+    return sign | (uint8_t)(((e + 7) << 3) | (m - 8));
+}
+
+/* Expert weight tensor [E][rows][K] drawn as syn_mxfp4_experts draws it and
+ * stored in the fp8 block format: per 128 x 128 block an fp32 scale
+ * amax / 448 and e4m3 codes of w / scale; q [E][rows][K], scale
+ * [E][rows/128][K/128] (rows and K multiples of 128). */
+void syn_fp8_experts(uint64_t seed, uint64_t stream_base, int E, int rows, int K, float sigma, uint8_t* q,
+                     float* scale, const float* tab, int n_tab)
+{
+    const int RB = rows / 128, KB = K / 128;
+#pragma omp parallel for schedule(static)
+    for (long long eb = 0; eb < (long long)E * RB; ++eb) {
+        int e = (int)(eb / RB), rb = (int)(eb % RB);
+        uint64_t key = stream_key(seed, stream_base + (uint64_t)e);
+        static __thread float blk[128 * 128];
+        for (int kb = 0; kb < KB; ++kb) {
+            float amax = 0.0f;
+            for (int r = 0; r < 128; ++r)
+                for (int c = 0; c < 128; ++c) {
+                    float w = sigma * normal_from(draw(key, (uint64_t)(rb * 128 + r) * K + kb * 128 + c), tab, n_tab);
+                    blk[r * 128 + c] = w;
+                    if (fabsf(w) > amax) amax = fabsf(w);
+                }
+            float sc = amax / 448.0f;
+            scale[((size_t)e * RB + rb) * KB + kb] = sc;
+            for (int r = 0; r < 128; ++r)
+                for (int c = 0; c < 128; ++c)
+                    q[((size_t)e * rows + rb * 128 + r) * K + kb * 128 + c] =
+                        amax > 0.0f ? e4m3_code(blk[r * 128 + c] / sc) : 0;
         }
     }
 }
