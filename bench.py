@@ -201,7 +201,8 @@ def oracle_sample(inp, budget_s=12.0, max_tokens=None, act_scale_mode=0):
     done = 0
     for t in order:
         oracle.forward(inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, c.k, c.score_func,
-                       inp.logit_bias, inp.sel_bias, tokens=[int(t)], act_scale_mode=act_scale_mode)
+                       inp.logit_bias, inp.sel_bias, tokens=[int(t)], act_scale_mode=act_scale_mode,
+                       weight_format=inp.weight_format)
         done += 1
         if time.perf_counter() - t0 >= budget_s or (max_tokens and done >= max_tokens):
             break
@@ -222,7 +223,7 @@ def run_reference(args, cfg):
     ws, rank, local = dist_env()
     if rank != 0:
         return 0
-    inp = synth.make_inputs(cfg)
+    inp = synth.make_inputs(cfg, weights=args.weights)
     tokens = 0
     elapsed = 0.0
     for _ in range(args.warmup):
@@ -241,7 +242,7 @@ def run_reference(args, cfg):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * elapsed / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(workload_desc(cfg), act_scale=args.act_scale),
+        "config": dict(workload_desc(cfg), act_scale=args.act_scale, weights=args.weights),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{tokens} tokens of the {cfg.name} batch, one oracle call per token "
                                    f"(routing of all {cfg.T} tokens + that token's {cfg.k} expert FFNs, fp64)"},
@@ -263,11 +264,12 @@ def run_gpu(args, cfg):
         tdist.init_process_group("nccl")
     device = local
     torch.cuda.set_device(device)
-    inp = synth.make_inputs(cfg)
+    inp = synth.make_inputs(cfg, weights=args.weights)
     c = cfg
     act_mode = ACT_SCALES[args.act_scale]
     layer = moe.MoELayer(c.H, c.I, c.E, c.k, c.T, c.score_func, device=device, act_scale_mode=act_mode)
-    layer.load_weights(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
+    load = layer.load_weights_fp8 if args.weights == "fp8" else layer.load_weights
+    load(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
     x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).to(f"cuda:{device}")
     y = torch.empty_like(x)
     stream = torch.cuda.Stream(device)
@@ -287,8 +289,12 @@ def run_gpu(args, cfg):
     counts, _ = layer.expert_counts()
     active = int((counts > 0).sum())
     rows = int(counts.sum())
-    ebytes13 = 2 * c.I * c.H // 2 + 2 * c.I * c.H // 32
-    ebytes2 = c.H * c.I // 2 + c.H * c.I // 32
+    if args.weights == "fp8":   # e4m3 bytes + a 4-byte scale per 128 x 128 block
+        ebytes13 = 2 * c.I * c.H + 4 * (2 * c.I // 128) * (c.H // 128)
+        ebytes2 = c.H * c.I + 4 * (c.H // 128) * (c.I // 128)
+    else:                       # E2M1 nibbles + one E8M0 byte per 32
+        ebytes13 = 2 * c.I * c.H // 2 + 2 * c.I * c.H // 32
+        ebytes2 = c.H * c.I // 2 + c.H * c.I // 32
     g1_bytes = active * ebytes13
     g2_bytes = active * ebytes2
     g1_flops = 2.0 * rows * (2 * c.I) * c.H
@@ -383,7 +389,7 @@ def run_gpu(args, cfg):
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e2m1 (fp32 accumulate)",
-            "data": "synthetic", "config": dict(workload_desc(cfg), act_scale=args.act_scale,
+            "data": "synthetic", "config": dict(workload_desc(cfg), act_scale=args.act_scale, weights=args.weights,
                                                parallelism=f"replicas{ws}",
                                                l2="inputs larger than L2: every step streams the active experts' "
                                                   "weights from HBM"),
@@ -417,6 +423,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", default="mxfp4", choices=["mxfp4", "fp8"],
+                    help="expert format: MXFP4 (default) or e4m3 with an fp32 scale per 128 x 128 block")
     ap.add_argument("--act-scale", default="e8m0", choices=sorted(ACT_SCALES),
                     help="activation block scales: power-of-two E8M0 (default) or fp32 amax/448")
     ap.add_argument("--experts", type=int, default=None,

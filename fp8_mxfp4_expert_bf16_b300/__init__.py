@@ -64,6 +64,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_init": (S, [ctypes.POINTER(_Config), ctypes.POINTER(P)]),
         "moe_destroy": (S, [P]),
         "moe_load_weights": (S, [P, P, P, P, P, P, P, P]),
+        "moe_load_weights_fp8": (S, [P, P, P, P, P, P, P, P]),
         "moe_forward": (S, [P, P, I, P, P]),
         "moe_forward_host": (S, [P, P, I, P, P]),
         "moe_get_logits": (S, [P, P]),
@@ -169,6 +170,18 @@ class MoELayer:
             assert b is None or tuple(b.shape) == (E,)
         self._check(self.L.moe_load_weights(self.h, _ptr(router_w), _ptr(logit_bias), _ptr(sel_bias),
                                             _ptr(w13_q), _ptr(w13_s), _ptr(w2_q), _ptr(w2_s)))
+
+    def load_weights_fp8(self, router_w, logit_bias, sel_bias, w13, w13_scale, w2, w2_scale):
+        """Experts in the fp8 block format: e4m3 codes u8 [E, 2I, H] / [E, H, I]
+        with fp32 scales per 128 x 128 block [E, 2I/128, H/128] / [E, H/128, I/128]."""
+        H, I, E = self.H, self.I, self.E
+        for a, shape in [(router_w, (E, H)), (w13, (E, 2 * I, H)), (w13_scale, (E, 2 * I // 128, H // 128)),
+                         (w2, (E, H, I)), (w2_scale, (E, H // 128, I // 128))]:
+            assert tuple(a.shape) == shape, (tuple(a.shape), shape)
+        for b in (logit_bias, sel_bias):
+            assert b is None or tuple(b.shape) == (E,)
+        self._check(self.L.moe_load_weights_fp8(self.h, _ptr(router_w), _ptr(logit_bias), _ptr(sel_bias),
+                                                _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale)))
 
     def forward(self, x, y=None, stream=None):
         """x: cuda bf16 [T, H] -> y: cuda bf16 [T, H] (enqueued on the stream, no sync)."""

@@ -356,6 +356,93 @@ moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float
     s.cb = d_cb;
     s.w13q = static_cast<const uint8_t*>(d_13);
     s.w2q = static_cast<const uint8_t*>(d_2);
+    s.w_fp8 = 0;
+    s.ws13 = s.ws2 = nullptr;
+    h->loaded = true;
+    h->last_T = -1;
+    return MOE_OK;
+}
+
+moe_status moe_load_weights_fp8(moe_handle* h, const uint16_t* router_w, const float* logit_bias,
+                                const float* sel_bias, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                const float* w2_scale)
+{
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_load_weights_fp8: handle is NULL");
+    if (!router_w || !w13 || !w13_scale || !w2 || !w2_scale)
+        return fail(h, MOE_ERR_INVALID_ARG, "moe_load_weights_fp8: a required weight pointer is NULL");
+    DevState& s = h->s;
+    CUDA_TRY(h, cudaSetDevice(h->cfg.device));
+    h->loaded = false;
+    for (void*& p : h->w_alloc)
+        if (p) {
+            cudaFree(p);
+            p = nullptr;
+        }
+    const size_t E = s.E, H = s.H, I = s.I;
+    const size_t n_wr = E * H * 2, n_13 = E * 2 * I * H, n_2 = E * H * I;
+    const size_t n_13s = E * (2 * I / 128) * (H / 128), n_2s = E * (H / 128) * (I / 128);
+    const int halves2 = s.BN2 / 128;
+    // tile-major blocks of 128-byte rows (e4m3, K = 128 per row)
+    const uint64_t rows13 = (uint64_t)E * s.NT1 * s.KB1 * 2 * 128;
+    const uint64_t rows2 = (uint64_t)E * s.NT2 * s.KB2 * halves2 * 128;
+    void *d_wr, *d_b, *d_13, *d_2, *d_s13, *d_s2, *d_tmp;
+    CUDA_TRY(h, cudaMalloc(&d_wr, n_wr));
+    h->w_alloc[0] = d_wr;
+    CUDA_TRY(h, cudaMalloc(&d_b, 2 * E * sizeof(float)));
+    h->w_alloc[1] = d_b;
+    CUDA_TRY(h, cudaMalloc(&d_13, rows13 * 128));
+    h->w_alloc[2] = d_13;
+    CUDA_TRY(h, cudaMalloc(&d_2, rows2 * 128));
+    h->w_alloc[3] = d_2;
+    CUDA_TRY(h, cudaMalloc(&d_s13, n_13s * sizeof(float)));
+    h->w_alloc[4] = d_s13;
+    CUDA_TRY(h, cudaMalloc(&d_s2, n_2s * sizeof(float)));
+    h->w_alloc[5] = d_s2;
+    CUDA_TRY(h, cudaMalloc(&d_tmp, (n_13 > n_2 ? n_13 : n_2) + 256));
+    h->w_alloc[6] = d_tmp;
+    float* d_lb = static_cast<float*>(d_b);
+    float* d_cb = d_lb + E;
+    uint8_t* tmp = static_cast<uint8_t*>(d_tmp);
+    CUDA_TRY(h, cudaMemcpy(d_wr, router_w, n_wr, cudaMemcpyDefault));
+    CUDA_TRY(h, cudaMemset(d_b, 0, 2 * E * sizeof(float)));
+    if (logit_bias) CUDA_TRY(h, cudaMemcpy(d_lb, logit_bias, E * sizeof(float), cudaMemcpyDefault));
+    if (sel_bias) CUDA_TRY(h, cudaMemcpy(d_cb, sel_bias, E * sizeof(float), cudaMemcpyDefault));
+    int32_t* flag = s.err + 3;
+    CUDA_TRY(h, cudaMemset(flag, 0, sizeof(int32_t)));
+    CUDA_TRY(h, cudaMemcpy(tmp, w13, n_13, cudaMemcpyDefault));
+    CUDA_TRY(h, launch_check_fp8(tmp, n_13, nullptr, 0, flag, 0));
+    CUDA_TRY(h, launch_repack_w8(tmp, static_cast<uint8_t*>(d_13), s.E, s.KB1, s.NT1, 2, 2 * s.I, 0, s.I / 128, 0));
+    CUDA_TRY(h, cudaDeviceSynchronize());
+    CUDA_TRY(h, cudaMemcpy(tmp, w2, n_2, cudaMemcpyDefault));
+    CUDA_TRY(h, launch_check_fp8(tmp, n_2, nullptr, 0, flag, 0));
+    CUDA_TRY(h, launch_repack_w8(tmp, static_cast<uint8_t*>(d_2), s.E, s.KB2, s.NT2, halves2, s.H, 1, s.I / 128, 0));
+    CUDA_TRY(h, cudaDeviceSynchronize());
+    CUDA_TRY(h, cudaMemcpy(d_s13, w13_scale, n_13s * sizeof(float), cudaMemcpyDefault));
+    CUDA_TRY(h, cudaMemcpy(d_s2, w2_scale, n_2s * sizeof(float), cudaMemcpyDefault));
+    CUDA_TRY(h, launch_check_fp8(nullptr, 0, static_cast<const float*>(d_s13), n_13s, flag, 0));
+    CUDA_TRY(h, launch_check_fp8(nullptr, 0, static_cast<const float*>(d_s2), n_2s, flag, 0));
+    int32_t bad = 0;
+    CUDA_TRY(h, cudaMemcpy(&bad, flag, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    cudaFree(d_tmp);
+    h->w_alloc[6] = nullptr;
+    if (bad) {
+        CUDA_TRY(h, cudaMemset(flag, 0, sizeof(int32_t)));
+        return fail(h, MOE_ERR_INVALID_ARG,
+                    "moe_load_weights_fp8: an e4m3 NaN code or a negative / non-finite block scale");
+    }
+    if (!make_map(&s.tm_w13, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_13, 128, rows13, 128, 128, 256) ||
+        !make_map(&s.tm_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_2, 128, rows2, 128, 128, 128 * halves2) ||
+        !make_map(&s.tm_wr64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_wr, H, E, H * 2, 64, 64) ||
+        !make_map(&s.tm_wr128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_wr, H, E, H * 2, 64, 128))
+        return fail(h, MOE_ERR_CUDA, "moe_load_weights_fp8: cuTensorMapEncodeTiled failed for the weights");
+    s.wr = static_cast<const uint16_t*>(d_wr);
+    s.lb = d_lb;
+    s.cb = d_cb;
+    s.w13q = static_cast<const uint8_t*>(d_13);
+    s.w2q = static_cast<const uint8_t*>(d_2);
+    s.ws13 = static_cast<const float*>(d_s13);
+    s.ws2 = static_cast<const float*>(d_s2);
+    s.w_fp8 = 1;
     h->loaded = true;
     h->last_T = -1;
     return MOE_OK;

@@ -24,6 +24,7 @@ constexpr int kDevErrBounds = 2;
 struct DevState {
     int H, I, E, K, Tm, score_func;
     int act_f32;         // activation blocks carry fp32 scales (amax / 448) instead of E8M0 ones
+    int w_fp8 = 0;       // experts in the fp8 block format (e4m3 + fp32 scale per 128 x 128) instead of MXFP4
     int KB1, KB2;        // H/128, I/128: K-blocks of the two grouped GEMMs
     int NT1, NT2, BN2;   // n-tiles: G1 (I/128, 256 columns = gate 128 + up 128), G2 (H/BN2)
     int MTmax;           // max 128-row m-tiles: ceil(Tm*K/128) + E
@@ -39,6 +40,9 @@ struct DevState {
     // scale chunks in tcgen05.cp order
     const uint8_t* w13q = nullptr;
     const uint8_t* w2q = nullptr;
+    // fp8 block format: the fp32 block scales [E][R/128][K/128] of each projection
+    const float* ws13 = nullptr;
+    const float* ws2 = nullptr;
 
     // workspace
     float* logits;        // [Tm][E]
@@ -113,6 +117,9 @@ cudaError_t launch_repack_sf(const uint8_t* src, uint8_t* dst, int E, int KB, in
 cudaError_t launch_repack_w(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
                             int mode, int I128, cudaStream_t st);
 cudaError_t launch_check_e8m0(const uint8_t* p, size_t n, int32_t* flag, cudaStream_t st);
+cudaError_t launch_repack_w8(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
+                             int mode, int I128, cudaStream_t st);
+cudaError_t launch_check_fp8(const uint8_t* q, size_t n, const float* s, size_t ns, int32_t* flag, cudaStream_t st);
 // getter helpers (route.cu)
 cudaError_t launch_unpad_perm(const DevState& s, int T, int32_t* out, cudaStream_t st);
 cudaError_t launch_gather_rows_u8(const DevState& s, int T, int which, uint8_t* q, uint8_t* sc, cudaStream_t st);

@@ -81,7 +81,7 @@ constexpr uint32_t kBHalfTxBytes = 128 * 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;      // accumulator: 256 fp32 columns
 constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), SFB at +8 (8 cols)
-constexpr uint32_t kSFUnitCol = 352; // fp32-scale mode: a constant unit activation scale chunk (4 cols)
+constexpr uint32_t kSFUnitCol = 352; // promotion modes: a constant unit scale chunk, twice (8 cols)
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, epilogue warps
 
@@ -108,6 +108,8 @@ struct GemmArgs {
     // (gate/up) the output table for the SwiGLU rows' scales [R][I/128]
     const float* as32;
     float* hs32;
+    // fp8 expert format: the projection's fp32 block scales [E][R/128][KB]
+    const float* ws;
     int early_trigger;           // let the next kernel be scheduled right after the wait (else at the end)
     int32_t* err;
 };
@@ -274,7 +276,7 @@ __device__ __forceinline__ void store_rows_transposed(uint32_t taddr, int live_r
 // role drains its own work before returning: the producer waits until its
 // copies have landed, the MMA issuer until its MMAs have completed, the
 // epilogue has read its last accumulator.
-template <int kMode, bool kLight, bool kF32S>
+template <int kMode, bool kLight, bool kF32S, bool kW8>
 __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<Shape<kLight>::kStages>& pc,
                                            uint32_t tmem, const CUtensorMap* tmA0, const CUtensorMap* tmA1,
                                            const CUtensorMap* tmA2, const CUtensorMap* tmW, const GemmArgs& args,
@@ -315,9 +317,14 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 const int sel = rows <= S::kBox0 ? 0 : (rows <= S::kBox1 ? 1 : 2);
                 const CUtensorMap* tA = sel == 0 ? tmA0 : (sel == 1 ? tmA1 : tmA2);
                 const uint32_t a_bytes = (uint32_t)(sel == 0 ? S::kBox0 : (sel == 1 ? S::kBox1 : S::kBox2)) * 128u;
-                const uint32_t tx = a_bytes + args.halves * (kBHalfTxBytes + 512) + (kF32S ? 0u : 512u);
+                // weight bytes of a stage: E2M1 rows (8 KB per 128 rows) + their scale chunks,
+                // or e4m3 rows (16 KB per 128 rows, block scales applied in the epilogue)
+                const uint32_t tx = a_bytes +
+                                    (kW8 ? (uint32_t)args.halves * 16384u : args.halves * (kBHalfTxBytes + 512)) +
+                                    (kF32S ? 0u : 512u);
+                constexpr int kRowsHalf = kW8 ? 128 : kWBlockRowsPerHalf;
                 // first row of this tile's interleaved weight blocks
-                const size_t wrow0 = ((size_t)(e * NT + nt) * KB) * args.halves * kWBlockRowsPerHalf;
+                const size_t wrow0 = ((size_t)(e * NT + nt) * KB) * args.halves * kRowsHalf;
                 const uint32_t* sfa = args.sfa + (size_t)mt * KB * 128;
                 if (!waited) {
                     // Before the wait: the weight tile and its scales for the
@@ -328,10 +335,11 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         uint8_t* st = smem + kb * kStageStride;
                         const uint32_t fb = smem_u32(&pc.full[kb]);
                         mbar_arrive_expect_tx(fb, tx);
-                        const size_t wrow = wrow0 + (size_t)kb * args.halves * kWBlockRowsPerHalf;
+                        const size_t wrow = wrow0 + (size_t)kb * args.halves * kRowsHalf;
                         tma_load_2d(smem_u32(st + S::kBOff), tmW, fb, 0, (int)wrow);
-                        bulk_load(smem_u32(st + kSFBOff), args.wq + (wrow + (size_t)args.halves * 128) * 64,
-                                  args.halves * 512, fb);
+                        if constexpr (!kW8)
+                            bulk_load(smem_u32(st + kSFBOff), args.wq + (wrow + (size_t)args.halves * 128) * 64,
+                                      args.halves * 512, fb);
                         issued[kb] = true;
                         last_phase[kb] = 0;
                     }
@@ -357,11 +365,12 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                     mbar_arrive_expect_tx(fb, tx);
                     tma_load_2d(smem_u32(st), tA, fb, kb * kBK, mt * kBM);
                     // the stage's weight rows (both halves) are one box; its scale chunks follow them
-                    const size_t wrow = wrow0 + (size_t)kb * args.halves * kWBlockRowsPerHalf;
+                    const size_t wrow = wrow0 + (size_t)kb * args.halves * kRowsHalf;
                     tma_load_2d(smem_u32(st + S::kBOff), tmW, fb, 0, (int)wrow);
                     if constexpr (!kF32S) bulk_load(smem_u32(st + kSFAOff), sfa + (size_t)kb * 128, 512, fb);
-                    bulk_load(smem_u32(st + kSFBOff), args.wq + (wrow + (size_t)args.halves * 128) * 64,
-                              args.halves * 512, fb);
+                    if constexpr (!kW8)
+                        bulk_load(smem_u32(st + kSFBOff), args.wq + (wrow + (size_t)args.halves * 128) * 64,
+                                  args.halves * 512, fb);
                     issued[s] = true;
                     last_phase[s] = ph;
                 }
@@ -375,15 +384,17 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = idesc_mxf8f6f4(128, 128 * args.halves, kTypeE4M3, kTypeE2M1);
+            const uint32_t idesc = idesc_mxf8f6f4(128, 128 * args.halves, kTypeE4M3, kW8 ? kTypeE4M3 : kTypeE2M1);
             int it = 0, tcount = 0;
             bool ok = true;
-            if constexpr (kF32S) {
-                // One partial product per K-step (unit activation scales, the
-                // weights' own E8M0 scales), handed to the epilogue, which folds
-                // the rows' fp32 scales in; the next K-step's MMAs wait until
-                // every epilogue warp has read it.
+            if constexpr (kF32S || kW8) {
+                // One partial product per K-step, handed to the epilogue, which
+                // folds the fp32 scales in (the rows' activation scales and / or
+                // the weights' block scales; in the MMA those are unit E8M0
+                // chunks); the next K-step's MMAs wait until every epilogue
+                // warp has read it.
                 tmem_cp_32x128b_warpx4(tmem + kSFUnitCol, desc_sf_chunk(smem_u32(g->unit_sf)));
+                tmem_cp_32x128b_warpx4(tmem + kSFUnitCol + 4u, desc_sf_chunk(smem_u32(g->unit_sf)));
                 int ks = 0;
                 for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                     for (int kb = 0; kb < KB; ++kb, ++it, ++ks) {
@@ -401,15 +412,23 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         }
                         tc_fence_after();
                         const uint32_t st = smem_u32(smem + s * kStageStride);
-                        const uint32_t sfb_t = tmem + kSFCol + 16u * s + 8u;
-                        tmem_cp_32x128b_warpx4(sfb_t, desc_sf_chunk(st + kSFBOff));
-                        if (args.halves == 2) tmem_cp_32x128b_warpx4(sfb_t + 4u, desc_sf_chunk(st + kSFBOff + 512));
+                        uint32_t sfa_t = tmem + kSFUnitCol, sfb_t = tmem + kSFUnitCol;
+                        if constexpr (!kF32S) {
+                            sfa_t = tmem + kSFCol + 16u * s;
+                            tmem_cp_32x128b_warpx4(sfa_t, desc_sf_chunk(st + kSFAOff));
+                        }
+                        if constexpr (!kW8) {
+                            sfb_t = tmem + kSFCol + 16u * s + 8u;
+                            tmem_cp_32x128b_warpx4(sfb_t, desc_sf_chunk(st + kSFBOff));
+                            if (args.halves == 2)
+                                tmem_cp_32x128b_warpx4(sfb_t + 4u, desc_sf_chunk(st + kSFBOff + 512));
+                        }
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const uint64_t ad = desc_kmajor_sw128(st + 32u * k);
                             const uint64_t bd = desc_kmajor_sw128(st + S::kBOff + 32u * k);
-                            mma_mxf8f6f4(tmem + kAccCol, ad, bd, idesc_with_sf_id(idesc, k, k), tmem + kSFUnitCol,
-                                         sfb_t, k != 0 ? 1u : 0u);
+                            mma_mxf8f6f4(tmem + kAccCol, ad, bd, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
+                                         k != 0 ? 1u : 0u);
                         }
                         tc_commit(smem_u32(&pc.empty[s]));
                         tc_commit(smem_u32(&pc.pfull));
@@ -464,16 +483,17 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
         const int row = q * 32 + lane;
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         int tcount = 0;
-        if constexpr (kF32S) {
-            // fp32-scale mode: per K-step, this warp's 128 partial columns are
-            // read from TMEM and folded into fp32 registers with the row's
-            // scale (acc += s * partial, K-steps in order); warps without live
-            // rows still take part in each K-step's hand-off.
+        if constexpr (kF32S || kW8) {
+            // promotion modes: per K-step, this warp's 128 partial columns are
+            // read from TMEM and folded into fp32 registers, acc += s * partial
+            // in K order, s = the row's fp32 activation scale and / or the
+            // fp32 scale of the weight block the columns belong to; warps
+            // without live rows still take part in each K-step's hand-off.
             constexpr int kW = 128;
             int ks = 0;
-            // the scales come from the previous kernel (quantisation, or the
-            // gate/up GEMM): wait for it before the first read
-            griddep_wait();
+            // activation scales come from the previous kernel (quantisation,
+            // or the gate/up GEMM): wait for it before the first read
+            if (kF32S) griddep_wait();
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tcount) {
                 const int mt = list[tile / NT], nt = tile - (tile / NT) * NT;
                 const int rows = args.mtile_rows[mt];
@@ -484,15 +504,34 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 // down: columns [hw * ncw, +ncw)
                 const uint32_t c0 = kMode == 0 ? 64u * hw : (uint32_t)(hw * ncw);
                 const uint32_t c1 = kMode == 0 ? 128u + 64u * hw : c0 + 64u;
-                const float* srow = args.as32 + (size_t)(mt * kBM + row) * KB;
+                const float* srow = kF32S ? args.as32 + (size_t)(mt * kBM + row) * KB : nullptr;
+                // weight blocks of this warp's two column groups: gate / up rows of
+                // the n-tile (gate/up), or the tile's 128-feature block (down)
+                const float* wsa = nullptr;
+                const float* wsb = nullptr;
+                if constexpr (kW8) {
+                    const int e = args.mtile_expert[mt];
+                    const int RB = kMode == 0 ? 2 * (args.I / 128) : args.H / 128;
+                    const int rba = kMode == 0 ? nt : nt * args.halves + (args.halves == 2 ? hw : 0);
+                    const int rbb = kMode == 0 ? args.I / 128 + nt : rba;
+                    wsa = args.ws + ((size_t)e * RB + rba) * KB;
+                    wsb = args.ws + ((size_t)e * RB + rbb) * KB;
+                }
                 float acc[kW];
 #pragma unroll
                 for (int j = 0; j < kW; ++j) acc[j] = 0.0f;
-                float s_next = row_live ? srow[0] : 0.0f;
+                float s_next = kF32S ? (row_live ? srow[0] : 0.0f) : 1.0f;
+                float wa_next = kW8 ? wsa[0] : 1.0f, wb_next = kW8 ? wsb[0] : 1.0f;
                 bool ok = true;
                 for (int kb = 0; kb < KB; ++kb, ++ks) {
-                    const float sc = s_next;
-                    if (kb + 1 < KB) s_next = row_live ? srow[kb + 1] : 0.0f;
+                    const float sc_a = s_next * wa_next, sc_b = s_next * wb_next;
+                    if (kb + 1 < KB) {
+                        if constexpr (kF32S) s_next = row_live ? srow[kb + 1] : 0.0f;
+                        if constexpr (kW8) {
+                            wa_next = wsa[kb + 1];
+                            wb_next = wsb[kb + 1];
+                        }
+                    }
                     if (!mbar_wait(smem_u32(&pc.pfull), (uint32_t)ks & 1u, abrt)) {
                         raise_error(g, args.err, 10);
                         ok = false;
@@ -506,6 +545,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                                 uint32_t pv[32];
                                 tmem_ld32(tl + kAccCol + (c < 2 ? c0 + 32u * c : c1 + 32u * (c - 2)), pv);
                                 tmem_ld_wait();
+                                const float sc = c < 2 ? sc_a : sc_b;
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(sc, __uint_as_float(pv[j]), acc[32 * c + j]);
                             }
@@ -516,7 +556,46 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                     if (lane == 0) mbar_arrive(smem_u32(&pc.pempty));
                 }
                 if (!ok) break;
-                if (kMode == 0) {
+                if (kMode == 0 && !kF32S) {
+                    // h = silu(g) * u on the promoted sums, then the power-of-two
+                    // re-quantisation of the row's 128-wide block
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        const float gf = row_live ? acc[j] : 0.0f;
+                        const float uf = row_live ? acc[64 + j] : 0.0f;
+                        acc[j] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
+                    }
+                    float amax = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) amax = fmaxf(amax, fabsf(acc[j]));
+                    const int p = tcount & 1;
+                    pc.red[p][ew][lane] = amax;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&pc.red_full[p]));
+                    if (!mbar_wait(smem_u32(&pc.red_full[p]), (uint32_t)(tcount >> 1) & 1u, abrt)) {
+                        raise_error(g, args.err, 12);
+                        break;
+                    }
+                    amax = fmaxf(amax, pc.red[p][ew ^ 4][lane]);
+                    if (row_live) {
+                        const int ex = act_block_exponent(amax);
+                        const float inv = __int_as_float((127 - ex) << 23);
+                        uint4* dst =
+                            reinterpret_cast<uint4*>(args.hq + (size_t)(mt * kBM + row) * args.I + nt * 128 + 64 * hw);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float* hv = acc + 16 * v;
+                            uint4 w;
+                            w.x = e4m3x4(hv[0] * inv, hv[1] * inv, hv[2] * inv, hv[3] * inv);
+                            w.y = e4m3x4(hv[4] * inv, hv[5] * inv, hv[6] * inv, hv[7] * inv);
+                            w.z = e4m3x4(hv[8] * inv, hv[9] * inv, hv[10] * inv, hv[11] * inv);
+                            w.w = e4m3x4(hv[12] * inv, hv[13] * inv, hv[14] * inv, hv[15] * inv);
+                            dst[v] = w;
+                        }
+                        if (hw == 0)
+                            args.hsf[sf_word_index(mt, nt, args.I / 128, row)] = (uint32_t)(ex + 127) * 0x01010101u;
+                    }
+                } else if (kMode == 0) {
                     // h = silu(g) * u on the promoted sums, then the fp32-scale
                     // re-quantisation of the row's 128-wide block
 #pragma unroll
@@ -655,8 +734,9 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
 }
 
 // mode 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows; kF32S: the
-// activation blocks carry fp32 scales (promotion in the epilogue)
-template <int kMode, bool kF32S>
+// activation blocks carry fp32 scales, kW8: the experts are e4m3 with fp32
+// 128 x 128 block scales (either one: promotion in the epilogue)
+template <int kMode, bool kF32S, bool kW8>
 __global__ void __launch_bounds__(kThreads, 1)
     k_mx_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
               const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
@@ -667,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     GemmCtl* g = reinterpret_cast<GemmCtl*>(smem + kRingBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (kF32S) {
+    if (kF32S || kW8) {
         for (int i = threadIdx.x; i < 128; i += blockDim.x) g->unit_sf[i] = 0x7F7F7F7Fu;   // E8M0 1.0
         fence_proxy_async_smem();   // generic-proxy writes above, read by tcgen05.cp
     }
@@ -693,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = g->tmem_base;
     bool waited = false;   // the producer's wait for the previous kernel (producer thread only)
 
-    gemm_phase<kMode, true, kF32S>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args, args.light_list,
+    gemm_phase<kMode, true, kF32S, kW8>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args, args.light_list,
                             *args.light_count, waited);
     // the heavy phase reuses the ring and the accumulator: every role of the
     // light phase has drained its own work
@@ -701,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (!*(volatile int*)&g->abort)
-        gemm_phase<kMode, false, kF32S>(smem, g, g->heavy, tmem, &tmA2, &tmA3, &tmA4, &tmW, args, args.heavy_list,
+        gemm_phase<kMode, false, kF32S, kW8>(smem, g, g->heavy, tmem, &tmA2, &tmA3, &tmA4, &tmW, args, args.heavy_list,
                                  *args.heavy_count, waited);
     // a CTA without tiles still waits before it lets the next kernel start
     if (warp == 0 && lane == 0) {
@@ -719,13 +799,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t gemm_set_attributes()
 {
-    cudaError_t e = cudaFuncSetAttribute(k_mx_gemm<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_mx_gemm<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_mx_gemm<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_mx_gemm<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const void* ks[] = {(const void*)k_mx_gemm<0, false, false>, (const void*)k_mx_gemm<1, false, false>,
+                        (const void*)k_mx_gemm<0, true, false>,  (const void*)k_mx_gemm<1, true, false>,
+                        (const void*)k_mx_gemm<0, false, true>,  (const void*)k_mx_gemm<1, false, true>,
+                        (const void*)k_mx_gemm<0, true, true>,   (const void*)k_mx_gemm<1, true, true>};
+    cudaError_t e = cudaSuccess;
+    for (const void* k : ks)
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     return e;
 }
 
@@ -769,33 +849,45 @@ static GemmArgs gemm2_args(const DevState& s)
     return a;
 }
 
+template <int kMode, bool kF32S, bool kW8>
+static cudaError_t launch_variant(const DevState& s, cudaStream_t st, const GemmArgs& a, const CUtensorMap* tA,
+                                  const CUtensorMap& tW)
+{
+    return launch_kernel(k_mx_gemm<kMode, kF32S, kW8>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, tA[0],
+                         tA[1], tA[2], tA[3], tA[4], tW, a);
+}
+
+template <int kMode>
+static cudaError_t launch_mode(const DevState& s, cudaStream_t st, const GemmArgs& a, const CUtensorMap* tA,
+                               const CUtensorMap& tW)
+{
+    if (s.w_fp8) {
+        return s.act_f32 ? launch_variant<kMode, true, true>(s, st, a, tA, tW)
+                         : launch_variant<kMode, false, true>(s, st, a, tA, tW);
+    }
+    return s.act_f32 ? launch_variant<kMode, true, false>(s, st, a, tA, tW)
+                     : launch_variant<kMode, false, false>(s, st, a, tA, tW);
+}
+
 // Light m-tiles (activation boxes of 8 / 16 rows: maps 0, 1), then heavy
 // m-tiles (32 / 64 / 128 rows: maps 2..4), in one launch.
 cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
 {
     GemmArgs a = gemm1_args(s);
     a.early_trigger = 1;   // the down GEMM follows
-    if (s.act_f32) {
-        a.as32 = s.asf32;
-        a.hs32 = s.hsf32;
-        return launch_kernel(k_mx_gemm<0, true>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_aq[0],
-                             s.tm_aq[1], s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13, a);
-    }
-    return launch_kernel(k_mx_gemm<0, false>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_aq[0],
-                         s.tm_aq[1], s.tm_aq[2], s.tm_aq[3], s.tm_aq[4], s.tm_w13, a);
+    a.as32 = s.asf32;
+    a.hs32 = s.hsf32;
+    a.ws = s.ws13;
+    return launch_mode<0>(s, st, a, s.tm_aq, s.tm_w13);
 }
 
 cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
 {
     GemmArgs a = gemm2_args(s);
     a.early_trigger = 0;   // the combine follows
-    if (s.act_f32) {
-        a.as32 = s.hsf32;
-        return launch_kernel(k_mx_gemm<1, true>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_hq[0],
-                             s.tm_hq[1], s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2, a);
-    }
-    return launch_kernel(k_mx_gemm<1, false>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, s.tm_hq[0],
-                         s.tm_hq[1], s.tm_hq[2], s.tm_hq[3], s.tm_hq[4], s.tm_w2, a);
+    a.as32 = s.hsf32;
+    a.ws = s.ws2;
+    return launch_mode<1>(s, st, a, s.tm_hq, s.tm_w2);
 }
 
 }  // namespace moe

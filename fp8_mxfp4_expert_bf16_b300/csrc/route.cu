@@ -677,6 +677,58 @@ cudaError_t launch_repack_w(const uint8_t* src, uint8_t* dst, int E, int KB, int
     return cudaGetLastError();
 }
 
+// fp8 expert format: canonical e4m3 [E][R][K] -> tile-major blocks
+// [E][NT][KB] of halves * 128 rows x 128 bytes (one GEMM stage's weight
+// rows, the same n-tile grouping as above; no scale rows: the fp32 block
+// scales stay in their own table).  One thread per 16 bytes.
+__global__ void k_repack_w8(const uint4* __restrict__ src, uint4* __restrict__ dst, int E, int KB, int NT, int halves,
+                            int rows_total, int mode, int I128)
+{
+    const size_t n = (size_t)E * rows_total * KB * 8;   // 16-byte pieces
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int q = (int)(i & 7);                 // 16-byte piece within the 128-byte row slice
+        const int kb = (int)((i >> 3) % KB);
+        const size_t er = (i >> 3) / KB;
+        const int r = (int)(er % rows_total);
+        const int e = (int)(er / rows_total);
+        int nt, half, rr;
+        tile_of_row(r, mode, halves, I128, nt, half, rr);
+        const size_t row_t = ((((size_t)e * NT + nt) * KB + kb) * halves + half) * 128 + rr;
+        dst[row_t * 8 + q] = src[i];
+    }
+}
+
+cudaError_t launch_repack_w8(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
+                             int mode, int I128, cudaStream_t st)
+{
+    k_repack_w8<<<4736, 256, 0, st>>>(reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), E, KB, NT,
+                                      halves, rows_total, mode, I128);
+    return cudaGetLastError();
+}
+
+// Invalid fp8 expert input: an e4m3 NaN code (0x7F / 0xFF), or a block scale
+// that is negative, infinite or NaN.
+__global__ void k_check_fp8(const uint8_t* __restrict__ q, size_t n, const float* __restrict__ s, size_t ns,
+                            int32_t* flag)
+{
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        if ((q[i] & 0x7Fu) == 0x7Fu) {
+            atomicOr(flag, 1);
+            break;
+        }
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < ns; i += (size_t)gridDim.x * blockDim.x)
+        if (!(s[i] >= 0.0f) || isinf(s[i])) {
+            atomicOr(flag, 1);
+            break;
+        }
+}
+
+cudaError_t launch_check_fp8(const uint8_t* q, size_t n, const float* s, size_t ns, int32_t* flag, cudaStream_t st)
+{
+    k_check_fp8<<<1184, 256, 0, st>>>(q, n, s, ns, flag);
+    return cudaGetLastError();
+}
+
 __global__ void k_check_e8m0(const uint8_t* __restrict__ p, size_t n, int32_t* flag)
 {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)

@@ -116,6 +116,23 @@ moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float
                             const float* sel_bias, const uint8_t* w13_q, const uint8_t* w13_s,
                             const uint8_t* w2_q, const uint8_t* w2_s);
 
+/* The same with the experts in the fp8 block format of the V2.5 files
+ * ("MiMo V2.6 Pro and Flash architecture teardown", section "Why Are the
+ * V2.6 Files Half the Size of V2.5?": FP8 experts; 128 x 128 blocks as in
+ * the vLLM recipe's "block-wise FP8"): e4m3 codes with one fp32 scale per
+ * 128 x 128 block, the weight being e4m3(q) * scale (exactly, no
+ * requantisation).
+ *   w13        u8 e4m3 [E][2I][H] (gate rows [0, I), up rows [I, 2I))
+ *   w13_scale  fp32 [E][2I/128][H/128]
+ *   w2         u8 e4m3 [E][H][I]
+ *   w2_scale   fp32 [E][H/128][I/128]
+ * An e4m3 NaN code (0x7F, 0xFF) or a negative / non-finite scale fails with
+ * MOE_ERR_INVALID_ARG and leaves the handle without weights.  The GEMMs then
+ * fold the block scales into fp32 partial sums per 128-wide K block. */
+moe_status moe_load_weights_fp8(moe_handle* h, const uint16_t* router_w, const float* logit_bias,
+                                const float* sel_bias, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                const float* w2_scale);
+
 /* y = layer(x) for T tokens: x bf16 [T][H] and y bf16 [T][H] are device
  * pointers (x and y must not overlap).  Enqueued on `stream`; returns without
  * waiting for the GPU and without reading anything back, so it can be

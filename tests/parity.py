@@ -59,7 +59,8 @@ def make_layer(inp, max_tokens=None, score_func=None, act_scale_mode=0):
     c = inp.cfg
     layer = moe.MoELayer(c.H, c.I, c.E, c.k, max_tokens or inp.x.shape[0],
                          c.score_func if score_func is None else score_func, act_scale_mode=act_scale_mode)
-    layer.load_weights(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
+    load = layer.load_weights_fp8 if getattr(inp, "weight_format", "mxfp4") == "fp8" else layer.load_weights
+    load(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
     return layer
 
 
@@ -175,7 +176,8 @@ def full_check(layer, inp, tokens=None, check_intermediates=True):
     y_g = run_layer(layer, inp)
     f = oracle.forward(inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, c.k, c.score_func,
                        inp.logit_bias, inp.sel_bias, tokens=tokens,
-                       act_scale_mode=getattr(layer, "act_scale_mode", 0))
+                       act_scale_mode=getattr(layer, "act_scale_mode", 0),
+                       weight_format=getattr(inp, "weight_format", "mxfp4"))
     toks = f.tokens
     ids_g, gates_g = layer.routing()
     same, same_order = check_routing(f.route, ids_g, gates_g, c.k)
