@@ -118,10 +118,9 @@ moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float
 
 /* The same with the experts in the fp8 block format of the V2.5 files
  * ("MiMo V2.6 Pro and Flash architecture teardown", section "Why Are the
- * V2.6 Files Half the Size of V2.5?": FP8 experts; 128 x 128 blocks as in
- * the vLLM recipe's "block-wise FP8"): e4m3 codes with one fp32 scale per
- * 128 x 128 block, the weight being e4m3(q) * scale (exactly, no
- * requantisation).
+ * V2.6 Files Half the Size of V2.5?", the V2.5 / V2.6 table, row "Routed
+ * experts": FP8 E4M3 with one F32 scale per 128 x 128 block): the weight is
+ * e4m3(q) * scale of its block (exactly, no requantisation).
  *   w13        u8 e4m3 [E][2I][H] (gate rows [0, I), up rows [I, 2I))
  *   w13_scale  fp32 [E][2I/128][H/128]
  *   w2         u8 e4m3 [E][H][I]

@@ -300,9 +300,9 @@ def fp8_block_decode(q: np.ndarray, s: np.ndarray, blk: int = 128) -> np.ndarray
     """Exact values of an expert matrix in the fp8 block format: e4m3 codes
     q [R, K] times the fp32 scale of their blk x blk block, s [R/blk, K/blk].
 
-    [P5 "Why Are the V2.6 Files Half the Size of V2.5?": the V2.5 experts
-    are stored in FP8 (e4m3) with block scales; the 128 x 128 block size is
-    the one P2 "Overview" names for its block-wise FP8 computation.]
+    [P5 "Why Are the V2.6 Files Half the Size of V2.5?", the V2.5 / V2.6
+    table, row "Routed experts": V2.5 stores them as FP8 E4M3 with one F32
+    scale per 128 x 128 block.]
     """
     vals = e4m3_decode_array(q)
     sc = np.repeat(np.repeat(s.astype(np.float64), blk, axis=-2), blk, axis=-1)
