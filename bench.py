@@ -190,6 +190,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device: str) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's);
+    x itself when torch.distributed is not initialised."""
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    if tdist.is_available() and tdist.is_initialized():
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank: int, seconds_max: float, world: int) -> float:
+    """Tokens per second of all ranks together: every replica processes its
+    own batch, the job ends with its slowest rank."""
+    return world * tokens_per_rank / seconds_max
+
+
 def oracle_sample(inp, budget_s=12.0, max_tokens=None, act_scale_mode=0):
     """Time the CPU oracle token by token on the workload (routing of the
     whole batch included in every call) until the time budget is spent."""
@@ -336,11 +353,8 @@ def run_gpu(args, cfg):
     layer.set_profiling(False)
     layer.check_device_error()
 
-    t_local = torch.tensor([ms_total], dtype=torch.float64, device=f"cuda:{device}")
-    if dist:
-        tdist.all_reduce(t_local, op=tdist.ReduceOp.MAX)
-    ms_max = float(t_local.item())
-    value = ws * c.T * args.steps / (ms_max / 1000.0)
+    ms_max = max_over_ranks(ms_total, f"cuda:{device}")
+    value = whole_job_rate(c.T * args.steps, ms_max / 1000.0, ws)
 
     # end to end through the host-buffer entry point (pinned host memory)
     xh = torch.from_numpy(inp.x.view(np.int16)).pin_memory()
@@ -352,10 +366,7 @@ def run_gpu(args, cfg):
     for _ in range(args.steps):
         layer.forward_host(xh, yh, stream)
     el = time.perf_counter() - t0
-    t_e2e = torch.tensor([el], dtype=torch.float64, device=f"cuda:{device}")
-    if dist:
-        tdist.all_reduce(t_e2e, op=tdist.ReduceOp.MAX)
-    e2e_value = ws * c.T * args.steps / float(t_e2e.item())
+    e2e_value = whole_job_rate(c.T * args.steps, max_over_ranks(el, f"cuda:{device}"), ws)
 
     g1_ms = stage["gemm1_gate_up"]
     g2_ms = stage["gemm2_down"]
