@@ -81,6 +81,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_stage_count": (I, []),
         "moe_stage_name": (ctypes.c_char_p, [I]),
         "moe_check_device_error": (S, [P]),
+        "moe_selftest_wait_timeout": (S, [P, ctypes.c_uint]),
         "moe_last_launch_count": (I, [P]),
         "moe_last_error": (ctypes.c_char_p, [P]),
         "moe_status_string": (ctypes.c_char_p, [I]),

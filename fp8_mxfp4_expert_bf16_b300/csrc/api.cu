@@ -13,6 +13,7 @@
 
 #include "../../include/moe_mx.h"
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 using namespace moe;
 
@@ -537,6 +538,44 @@ moe_status moe_forward_host(moe_handle* h, const uint16_t* x_host, int T, uint16
 }
 
 int moe_last_launch_count(moe_handle* h) { return h ? h->last_launches : 0; }
+
+}   // extern "C"
+
+namespace moe {
+// The kernels' timeout path, on purpose: one thread waits on a barrier that
+// nothing completes, gives up after limit_ns, and records the timeout in the
+// error word exactly as a GEMM or router wait would (site 99).
+__global__ void k_wait_probe(int32_t* err, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait_for(smem_u32(&bar), 0u, &abort_flag, limit_ns)) {
+        if (atomicCAS(err, 0, kDevErrTimeout) == 0) {
+            err[1] = 99;
+            err[2] = blockIdx.x;
+        }
+    }
+}
+}  // namespace moe
+
+extern "C" {
+
+moe_status moe_selftest_wait_timeout(moe_handle* h, unsigned int limit_us)
+{
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_selftest_wait_timeout: handle is NULL");
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(h, MOE_ERR_INVALID_ARG, "moe_selftest_wait_timeout: limit_us=%u outside [1, 10^6]", limit_us);
+    CUDA_TRY(h, cudaSetDevice(h->cfg.device));
+    moe::k_wait_probe<<<1, 32>>>(h->s.err, (uint64_t)limit_us * 1000ull);
+    CUDA_TRY(h, cudaGetLastError());
+    return MOE_OK;
+}
 
 moe_status moe_check_device_error(moe_handle* h)
 {

@@ -65,7 +65,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 
 // Wait until the phase with the given parity has completed.  Returns false
 // if *abort became non-zero or the time limit passed first.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort)
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                              uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -74,8 +75,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const v
         for (int i = 0; i < 16; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort)
+{
+    return mbar_wait_for(bar, parity, abort, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -187,6 +187,16 @@ const char* moe_stage_name(int i);
  * kernel (MOE_ERR_TIMEOUT from a bounded wait, MOE_ERR_DEVICE otherwise). */
 moe_status moe_check_device_error(moe_handle* h);
 
+/* Self-test of the kernels' bounded waits (the pages have no counterpart;
+ * it checks the library's own failure detection without harming the GPU):
+ * launches one small kernel on the legacy default stream whose thread waits
+ * on a barrier that nothing completes; after limit_us microseconds
+ * (1 .. 1,000,000) the wait gives up, records MOE_ERR_TIMEOUT in the
+ * handle's device error word (site 99) as any kernel wait would, and the
+ * kernel exits normally.  The next moe_check_device_error (or getter)
+ * reports MOE_ERR_TIMEOUT and clears the word; the context stays usable. */
+moe_status moe_selftest_wait_timeout(moe_handle* h, unsigned int limit_us);
+
 /* Number of kernels the last forward launched. */
 int moe_last_launch_count(moe_handle* h);
 

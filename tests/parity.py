@@ -169,6 +169,36 @@ def check_q2(layer, f, perm, tokens, same, ids_g):
     return frac
 
 
+DOWN_TF_REL = 1e-5
+
+
+def check_down_teacher_forced(layer, inp, perm, toks, sel, o_g):
+    """The down GEMM alone: the oracle recomputes each row's expert output in
+    fp64 from the GPU's own Q2 codes and scales (so Q2 rounding differences
+    drop out); the GPU's fp32 accumulation must agree to DOWN_TF_REL."""
+    hq_g, hs_g = layer.inter_quant()
+    ids_g, _ = layer.routing()
+    c = inp.cfg
+    fp8 = getattr(inp, "weight_format", "mxfp4") == "fp8"
+    num = den = 0.0
+    W2 = {}
+    for i in sel:
+        t = toks[i]
+        for j in range(c.k):
+            e = int(ids_g[t, j])
+            if e not in W2:
+                W2[e] = (oracle.fp8_block_decode(inp.w2_q[e], inp.w2_s[e]) if fp8
+                         else oracle.mxfp4_decode(inp.w2_q[e], inp.w2_s[e]))
+            row = perm[t * c.k + j]
+            h = oracle.act_dequant(hq_g[row:row + 1], hs_g[row:row + 1])
+            o = (h @ W2[e].T)[0]
+            num += float(np.sum((o_g[row].astype(np.float64) - o) ** 2))
+            den += float(np.sum(o * o))
+    rel = np.sqrt(num / max(den, 1e-300))
+    assert rel <= DOWN_TF_REL, f"down GEMM vs fp64 on its own inputs: rel L2 {rel:.3e}"
+    return float(rel)
+
+
 def full_check(layer, inp, tokens=None, check_intermediates=True):
     """Run the GPU layer on all of inp.x; compare routing/dispatch for all
     tokens and everything else on ``tokens`` (default all)."""
@@ -196,6 +226,7 @@ def full_check(layer, inp, tokens=None, check_intermediates=True):
         o_rel = np.linalg.norm(og - oo) / np.linalg.norm(oo)
         assert o_rel <= Y_REL_L2, f"expert output rel L2 {o_rel:.3e}"
         stats["expert_out_rel_l2"] = float(o_rel)
+        stats["down_teacher_forced_rel_l2"] = check_down_teacher_forced(layer, inp, perm, toks, sel, o_g)
     rel, mx = check_y(y_g[toks], f.y, same[toks])
     stats.update(rel_l2=rel, max_abs_over_rms=mx)
     return stats, y_g, f

@@ -43,6 +43,23 @@ def test_shapes_full_parity(shape):
     print(shape, stats)
 
 
+@pytest.mark.parametrize("shape", [(64, 512, 16, 256, 8), (300, 512, 16, 256, 8), (77, 1024, 40, 384, 6)])
+def test_structural_invariants(shape):
+    T, H, E, I, k = shape
+    inp = synth.custom_inputs(T, H, E, I, k, seed=700 + T)
+    layer = make_layer(inp)
+    run_layer(layer, inp)
+    ids, gates = layer.routing()
+    counts, offsets = layer.expert_counts()
+    perm = layer.permutation()
+    assert np.allclose(gates.sum(axis=1), 1.0, atol=1e-6)
+    assert (gates > 0).all()
+    assert all(len(set(r.tolist())) == k for r in ids) and ((0 <= ids) & (ids < E)).all()
+    assert counts.sum() == T * k and np.array_equal(counts, np.bincount(ids.reshape(-1), minlength=E))
+    assert offsets[0] == 0 and offsets[E] == T * k and (np.diff(offsets) >= 0).all()
+    assert np.array_equal(np.sort(perm), np.arange(T * k))
+
+
 def test_forward_host_matches_device_and_is_deterministic():
     import torch
     inp = synth.make_inputs("toy")

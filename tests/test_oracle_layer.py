@@ -245,3 +245,23 @@ def test_generator_is_deterministic_and_seeded():
     assert abs(x.mean()) < 0.02 and abs(x.std() - 1) < 0.02
     c = synth.make_inputs(synth.Config("s1", 64, 512, 16, 256, 8, 1, "none"))
     assert not np.array_equal(a.x, c.x)
+
+
+def test_forward_structural_invariants():
+    """Gates sum to 1, k distinct experts per token, counts sum to T*k,
+    offsets are the exclusive scan ending at T*k, the permutation is a
+    bijection that lists each expert's (token, slot) pairs contiguously."""
+    inp = synth.custom_inputs(37, 256, 12, 128, 5, seed=41, bias="normal:1.0")
+    T, k, E = 37, 5, 12
+    f = oracle.forward(inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, k,
+                       logit_bias=inp.logit_bias)
+    r = f.route
+    assert np.allclose(r.gates.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    assert all(len(set(row.tolist())) == k for row in r.ids)
+    assert f.counts.sum() == T * k
+    assert f.offsets[0] == 0 and f.offsets[E] == T * k and (np.diff(f.offsets) >= 0).all()
+    assert np.array_equal(np.sort(f.perm), np.arange(T * k))
+    flat = r.ids.reshape(-1)
+    for e in range(E):
+        rows = f.perm[flat == e]
+        assert np.array_equal(np.sort(rows), np.arange(f.offsets[e], f.offsets[e + 1]))
