@@ -434,38 +434,58 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         tc_commit(smem_u32(&pc.pfull));
                     }
                 }
-            } else
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
-                if (tcount > 0 && !mbar_wait(smem_u32(&pc.acc_empty), (uint32_t)(tcount - 1) & 1u, abrt)) {
-                    raise_error(g, args.err, 3);
-                    break;
-                }
-                tc_fence_after();
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % kStages;
-                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                    if (!mbar_wait(smem_u32(&pc.full[s]), ph, abrt)) {
-                        raise_error(g, args.err, 4);
-                        ok = false;
+            } else {
+                // The tensor pipe holds only a few MMAs ahead, so the issue
+                // path between two MMAs is kept to a handful of instructions
+                // (it shares its SM sub-partition with two epilogue warps):
+                // all descriptors of stage 0 are built once, a stage's are
+                // those plus a fixed offset (the start-address field counts
+                // 16-byte units and never carries: shared addresses stay
+                // below 2^18 bytes), and the ring position is stepped, not
+                // divided out of the iteration count.
+                const uint32_t s0 = smem_u32(smem);
+                const uint64_t ad0 = desc_kmajor_sw128(s0), bd0 = desc_kmajor_sw128(s0 + S::kBOff);
+                const uint64_t sfad0 = desc_sf_chunk(s0 + kSFAOff), sfbd0 = desc_sf_chunk(s0 + kSFBOff);
+                const uint32_t id1 = idesc_with_sf_id(idesc, 1, 1), id2 = idesc_with_sf_id(idesc, 2, 2),
+                               id3 = idesc_with_sf_id(idesc, 3, 3);
+                const uint32_t full0 = smem_u32(&pc.full[0]), empty0 = smem_u32(&pc.empty[0]);
+                const uint32_t acc = tmem + kAccCol;
+                const bool two = args.halves == 2;
+                int s = 0;
+                uint32_t ph = 0, doff = 0;
+                for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
+                    if (tcount > 0 && !mbar_wait(smem_u32(&pc.acc_empty), (uint32_t)(tcount - 1) & 1u, abrt)) {
+                        raise_error(g, args.err, 3);
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t st = smem_u32(smem + s * kStageStride);
-                    const uint32_t sfa_t = tmem + kSFCol + 16u * s;
-                    const uint32_t sfb_t = sfa_t + 8u;
-                    tmem_cp_32x128b_warpx4(sfa_t, desc_sf_chunk(st + kSFAOff));
-                    tmem_cp_32x128b_warpx4(sfb_t, desc_sf_chunk(st + kSFBOff));
-                    if (args.halves == 2) tmem_cp_32x128b_warpx4(sfb_t + 4u, desc_sf_chunk(st + kSFBOff + 512));
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t ad = desc_kmajor_sw128(st + 32u * k);
-                        const uint64_t bd = desc_kmajor_sw128(st + S::kBOff + 32u * k);
-                        mma_mxf8f6f4(tmem + kAccCol, ad, bd, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
-                                     (kb | k) != 0 ? 1u : 0u);
+                    for (int kb = 0; kb < KB; ++kb) {
+                        if (!mbar_wait(full0 + 8u * s, ph, abrt)) {
+                            raise_error(g, args.err, 4);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sfa_t = tmem + kSFCol + 16u * s;
+                        const uint64_t ad = ad0 + doff, bd = bd0 + doff;
+                        tmem_cp_32x128b_warpx4(sfa_t, sfad0 + doff);
+                        tmem_cp_32x128b_warpx4(sfa_t + 8u, sfbd0 + doff);
+                        if (two) tmem_cp_32x128b_warpx4(sfa_t + 12u, sfbd0 + doff + (512 >> 4));
+                        mma_mxf8f6f4(acc, ad, bd, idesc, sfa_t, sfa_t + 8u, kb != 0 ? 1u : 0u);
+                        mma_mxf8f6f4(acc, ad + 2, bd + 2, id1, sfa_t, sfa_t + 8u, 1u);
+                        mma_mxf8f6f4(acc, ad + 4, bd + 4, id2, sfa_t, sfa_t + 8u, 1u);
+                        mma_mxf8f6f4(acc, ad + 6, bd + 6, id3, sfa_t, sfa_t + 8u, 1u);
+                        tc_commit(empty0 + 8u * s);
+                        if (++s == kStages) {
+                            s = 0;
+                            ph ^= 1u;
+                            doff = 0;
+                        } else {
+                            doff += kStageStride >> 4;
+                        }
                     }
-                    tc_commit(smem_u32(&pc.empty[s]));
+                    if (ok) tc_commit(smem_u32(&pc.acc_full));
                 }
-                if (ok) tc_commit(smem_u32(&pc.acc_full));
             }
             // all MMAs of this thread complete before the ring or TMEM is reused
             int zero = 0;
