@@ -382,8 +382,10 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                     raise_error(g, args.err, 2);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+        // ------------------------------------------------ MMA issuer
+        // The default path runs its loop on the whole warp (one elected lane
+        // issues each tcgen05 operation); the promotion path on lane 0.
+        if ((kF32S || kW8) ? lane == 0 : true) {
             const uint32_t idesc = idesc_mxf8f6f4(128, 128 * args.halves, kTypeE4M3, kW8 ? kTypeE4M3 : kTypeE2M1);
             int it = 0, tcount = 0;
             bool ok = true;
@@ -454,28 +456,29 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 int s = 0;
                 uint32_t ph = 0, doff = 0;
                 for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
-                    if (tcount > 0 && !mbar_wait(smem_u32(&pc.acc_empty), (uint32_t)(tcount - 1) & 1u, abrt)) {
-                        raise_error(g, args.err, 3);
+                    if (tcount > 0 &&
+                        !__all_sync(~0u, mbar_wait(smem_u32(&pc.acc_empty), (uint32_t)(tcount - 1) & 1u, abrt))) {
+                        if (lane == 0) raise_error(g, args.err, 3);
                         break;
                     }
                     tc_fence_after();
                     for (int kb = 0; kb < KB; ++kb) {
-                        if (!mbar_wait(full0 + 8u * s, ph, abrt)) {
-                            raise_error(g, args.err, 4);
+                        if (!__all_sync(~0u, mbar_wait(full0 + 8u * s, ph, abrt))) {
+                            if (lane == 0) raise_error(g, args.err, 4);
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint32_t sfa_t = tmem + kSFCol + 16u * s;
                         const uint64_t ad = ad0 + doff, bd = bd0 + doff;
-                        tmem_cp_32x128b_warpx4(sfa_t, sfad0 + doff);
-                        tmem_cp_32x128b_warpx4(sfa_t + 8u, sfbd0 + doff);
-                        if (two) tmem_cp_32x128b_warpx4(sfa_t + 12u, sfbd0 + doff + (512 >> 4));
-                        mma_mxf8f6f4(acc, ad, bd, idesc, sfa_t, sfa_t + 8u, kb != 0 ? 1u : 0u);
-                        mma_mxf8f6f4(acc, ad + 2, bd + 2, id1, sfa_t, sfa_t + 8u, 1u);
-                        mma_mxf8f6f4(acc, ad + 4, bd + 4, id2, sfa_t, sfa_t + 8u, 1u);
-                        mma_mxf8f6f4(acc, ad + 6, bd + 6, id3, sfa_t, sfa_t + 8u, 1u);
-                        tc_commit(empty0 + 8u * s);
+                        tmem_cp_32x128b_warpx4_elect(sfa_t, sfad0 + doff);
+                        tmem_cp_32x128b_warpx4_elect(sfa_t + 8u, sfbd0 + doff);
+                        if (two) tmem_cp_32x128b_warpx4_elect(sfa_t + 12u, sfbd0 + doff + (512 >> 4));
+                        mma_mxf8f6f4_elect(acc, ad, bd, idesc, sfa_t, sfa_t + 8u, kb != 0 ? 1u : 0u);
+                        mma_mxf8f6f4_elect(acc, ad + 2, bd + 2, id1, sfa_t, sfa_t + 8u, 1u);
+                        mma_mxf8f6f4_elect(acc, ad + 4, bd + 4, id2, sfa_t, sfa_t + 8u, 1u);
+                        mma_mxf8f6f4_elect(acc, ad + 6, bd + 6, id3, sfa_t, sfa_t + 8u, 1u);
+                        tc_commit_elect(empty0 + 8u * s);
                         if (++s == kStages) {
                             s = 0;
                             ph ^= 1u;
@@ -484,13 +487,16 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                             doff += kStageStride >> 4;
                         }
                     }
-                    if (ok) tc_commit(smem_u32(&pc.acc_full));
+                    if (ok) tc_commit_elect(smem_u32(&pc.acc_full));
                 }
             }
-            // all MMAs of this thread complete before the ring or TMEM is reused
+            // all MMAs of this warp complete before the ring or TMEM is reused
             int zero = 0;
-            tc_commit(smem_u32(&pc.drain));
-            if (!mbar_wait(smem_u32(&pc.drain), 0u, &zero)) raise_error(g, args.err, 5);
+            if constexpr (kF32S || kW8)
+                tc_commit(smem_u32(&pc.drain));
+            else
+                tc_commit_elect(smem_u32(&pc.drain));
+            if (!mbar_wait(smem_u32(&pc.drain), 0u, &zero) && lane == 0) raise_error(g, args.err, 5);
         }
     } else {
         // ---------------------------------------------------- epilogue
