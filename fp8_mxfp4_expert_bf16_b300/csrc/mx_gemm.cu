@@ -383,78 +383,81 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        // The default path runs its loop on the whole warp (one elected lane
-        // issues each tcgen05 operation); the promotion path on lane 0.
-        if ((kF32S || kW8) ? lane == 0 : true) {
+        // The loops run on the whole warp (one elected lane issues each
+        // tcgen05 operation), which keeps their control flow and descriptors
+        // warp-uniform.  The tensor pipe holds only a few MMAs ahead, so the
+        // issue path between two MMAs is kept to a handful of instructions
+        // (the warp shares its SM sub-partition with two epilogue warps):
+        // all descriptors of stage 0 are built once, a stage's are those
+        // plus a fixed offset (the start-address field counts 16-byte units
+        // and never carries: shared addresses stay below 2^18 bytes), and
+        // the ring position is stepped, not divided out of a counter.
+        {
             const uint32_t idesc = idesc_mxf8f6f4(128, 128 * args.halves, kTypeE4M3, kW8 ? kTypeE4M3 : kTypeE2M1);
-            int it = 0, tcount = 0;
+            const uint32_t s0 = smem_u32(smem);
+            const uint64_t ad0 = desc_kmajor_sw128(s0), bd0 = desc_kmajor_sw128(s0 + S::kBOff);
+            const uint64_t sfad0 = desc_sf_chunk(s0 + kSFAOff), sfbd0 = desc_sf_chunk(s0 + kSFBOff);
+            const uint32_t id1 = idesc_with_sf_id(idesc, 1, 1), id2 = idesc_with_sf_id(idesc, 2, 2),
+                           id3 = idesc_with_sf_id(idesc, 3, 3);
+            const uint32_t full0 = smem_u32(&pc.full[0]), empty0 = smem_u32(&pc.empty[0]);
+            const uint32_t acc = tmem + kAccCol;
+            const bool two = args.halves == 2;
+            int s = 0, tcount = 0;
+            uint32_t ph = 0, doff = 0;
             bool ok = true;
+            auto advance = [&]() {
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                    doff = 0;
+                } else {
+                    doff += kStageStride >> 4;
+                }
+            };
             if constexpr (kF32S || kW8) {
                 // One partial product per K-step, handed to the epilogue, which
                 // folds the fp32 scales in (the rows' activation scales and / or
                 // the weights' block scales; in the MMA those are unit E8M0
                 // chunks); the next K-step's MMAs wait until every epilogue
                 // warp has read it.
-                tmem_cp_32x128b_warpx4(tmem + kSFUnitCol, desc_sf_chunk(smem_u32(g->unit_sf)));
-                tmem_cp_32x128b_warpx4(tmem + kSFUnitCol + 4u, desc_sf_chunk(smem_u32(g->unit_sf)));
+                const uint64_t unit = desc_sf_chunk(smem_u32(g->unit_sf));
+                tmem_cp_32x128b_warpx4_elect(tmem + kSFUnitCol, unit);
+                tmem_cp_32x128b_warpx4_elect(tmem + kSFUnitCol + 4u, unit);
                 int ks = 0;
                 for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                    for (int kb = 0; kb < KB; ++kb, ++it, ++ks) {
-                        const int s = it % kStages;
-                        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                        if (!mbar_wait(smem_u32(&pc.full[s]), ph, abrt)) {
-                            raise_error(g, args.err, 8);
+                    for (int kb = 0; kb < KB; ++kb, ++ks) {
+                        if (!__all_sync(~0u, mbar_wait(full0 + 8u * s, ph, abrt))) {
+                            if (lane == 0) raise_error(g, args.err, 8);
                             ok = false;
                             break;
                         }
-                        if (ks > 0 && !mbar_wait(smem_u32(&pc.pempty), (uint32_t)(ks - 1) & 1u, abrt)) {
-                            raise_error(g, args.err, 9);
+                        if (ks > 0 && !__all_sync(~0u, mbar_wait(smem_u32(&pc.pempty), (uint32_t)(ks - 1) & 1u, abrt))) {
+                            if (lane == 0) raise_error(g, args.err, 9);
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t st = smem_u32(smem + s * kStageStride);
                         uint32_t sfa_t = tmem + kSFUnitCol, sfb_t = tmem + kSFUnitCol;
                         if constexpr (!kF32S) {
                             sfa_t = tmem + kSFCol + 16u * s;
-                            tmem_cp_32x128b_warpx4(sfa_t, desc_sf_chunk(st + kSFAOff));
+                            tmem_cp_32x128b_warpx4_elect(sfa_t, sfad0 + doff);
                         }
                         if constexpr (!kW8) {
                             sfb_t = tmem + kSFCol + 16u * s + 8u;
-                            tmem_cp_32x128b_warpx4(sfb_t, desc_sf_chunk(st + kSFBOff));
-                            if (args.halves == 2)
-                                tmem_cp_32x128b_warpx4(sfb_t + 4u, desc_sf_chunk(st + kSFBOff + 512));
+                            tmem_cp_32x128b_warpx4_elect(sfb_t, sfbd0 + doff);
+                            if (two) tmem_cp_32x128b_warpx4_elect(sfb_t + 4u, sfbd0 + doff + (512 >> 4));
                         }
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t ad = desc_kmajor_sw128(st + 32u * k);
-                            const uint64_t bd = desc_kmajor_sw128(st + S::kBOff + 32u * k);
-                            mma_mxf8f6f4(tmem + kAccCol, ad, bd, idesc_with_sf_id(idesc, k, k), sfa_t, sfb_t,
-                                         k != 0 ? 1u : 0u);
-                        }
-                        tc_commit(smem_u32(&pc.empty[s]));
-                        tc_commit(smem_u32(&pc.pfull));
+                        const uint64_t ad = ad0 + doff, bd = bd0 + doff;
+                        mma_mxf8f6f4_elect(acc, ad, bd, idesc, sfa_t, sfb_t, 0u);
+                        mma_mxf8f6f4_elect(acc, ad + 2, bd + 2, id1, sfa_t, sfb_t, 1u);
+                        mma_mxf8f6f4_elect(acc, ad + 4, bd + 4, id2, sfa_t, sfb_t, 1u);
+                        mma_mxf8f6f4_elect(acc, ad + 6, bd + 6, id3, sfa_t, sfb_t, 1u);
+                        tc_commit_elect(empty0 + 8u * s);
+                        tc_commit_elect(smem_u32(&pc.pfull));
+                        advance();
                     }
                 }
             } else {
-                // The tensor pipe holds only a few MMAs ahead, so the issue
-                // path between two MMAs is kept to a handful of instructions
-                // (it shares its SM sub-partition with two epilogue warps):
-                // all descriptors of stage 0 are built once, a stage's are
-                // those plus a fixed offset (the start-address field counts
-                // 16-byte units and never carries: shared addresses stay
-                // below 2^18 bytes), and the ring position is stepped, not
-                // divided out of the iteration count.
-                const uint32_t s0 = smem_u32(smem);
-                const uint64_t ad0 = desc_kmajor_sw128(s0), bd0 = desc_kmajor_sw128(s0 + S::kBOff);
-                const uint64_t sfad0 = desc_sf_chunk(s0 + kSFAOff), sfbd0 = desc_sf_chunk(s0 + kSFBOff);
-                const uint32_t id1 = idesc_with_sf_id(idesc, 1, 1), id2 = idesc_with_sf_id(idesc, 2, 2),
-                               id3 = idesc_with_sf_id(idesc, 3, 3);
-                const uint32_t full0 = smem_u32(&pc.full[0]), empty0 = smem_u32(&pc.empty[0]);
-                const uint32_t acc = tmem + kAccCol;
-                const bool two = args.halves == 2;
-                int s = 0;
-                uint32_t ph = 0, doff = 0;
                 for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++tcount) {
                     if (tcount > 0 &&
                         !__all_sync(~0u, mbar_wait(smem_u32(&pc.acc_empty), (uint32_t)(tcount - 1) & 1u, abrt))) {
@@ -479,23 +482,14 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         mma_mxf8f6f4_elect(acc, ad + 4, bd + 4, id2, sfa_t, sfa_t + 8u, 1u);
                         mma_mxf8f6f4_elect(acc, ad + 6, bd + 6, id3, sfa_t, sfa_t + 8u, 1u);
                         tc_commit_elect(empty0 + 8u * s);
-                        if (++s == kStages) {
-                            s = 0;
-                            ph ^= 1u;
-                            doff = 0;
-                        } else {
-                            doff += kStageStride >> 4;
-                        }
+                        advance();
                     }
                     if (ok) tc_commit_elect(smem_u32(&pc.acc_full));
                 }
             }
             // all MMAs of this warp complete before the ring or TMEM is reused
             int zero = 0;
-            if constexpr (kF32S || kW8)
-                tc_commit(smem_u32(&pc.drain));
-            else
-                tc_commit_elect(smem_u32(&pc.drain));
+            tc_commit_elect(smem_u32(&pc.drain));
             if (!mbar_wait(smem_u32(&pc.drain), 0u, &zero) && lane == 0) raise_error(g, args.err, 5);
         }
     } else {
