@@ -78,11 +78,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
     return fn;
 }
 
-// 2-D tensor map over a row-major [rows][inner] tensor, 128-byte swizzle
-// unless stated otherwise.
+// 2-D tensor map over a row-major [rows][inner] tensor, 128-byte swizzle.
 static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t rows,
-                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
-                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows)
 {
     auto enc = get_encode();
     if (!enc) return false;
@@ -90,7 +88,7 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, void* base, uint64_
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(m, dt, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+    CUresult r = enc(m, dt, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -234,11 +232,9 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
     ALLOC(s.mtile_off, sizeof(int32_t) * (s.E + 1));
     ALLOC(s.mtile_expert, sizeof(int32_t) * s.MTmax);
     ALLOC(s.mtile_rows, sizeof(int32_t) * s.MTmax);
-    ALLOC(s.n_mtiles, sizeof(int32_t) * 8);
+    ALLOC(s.n_mtiles, sizeof(int32_t) * 4);
     ALLOC(s.light_list, sizeof(int32_t) * s.MTmax);
     ALLOC(s.heavy_list, sizeof(int32_t) * s.MTmax);
-    ALLOC(s.pairs, sizeof(int2) * s.MTmax);
-    ALLOC(s.solo_list, sizeof(int32_t) * s.MTmax);
     ALLOC(s.prow, sizeof(int32_t) * s.Tm * s.K);
     ALLOC(s.aq, (size_t)s.Rmax * s.H);
     ALLOC(s.asf, sizeof(uint32_t) * (size_t)s.MTmax * s.KB1 * 128);
@@ -260,7 +256,7 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
               cudaMemset(s.hq, 0, (size_t)s.Rmax * s.I) == cudaSuccess &&
               cudaMemset(s.hsf, 0, sizeof(uint32_t) * (size_t)s.MTmax * s.KB2 * 128) == cudaSuccess &&
               cudaMemset(s.err, 0, sizeof(int32_t) * 4) == cudaSuccess &&
-              cudaMemset(s.n_mtiles, 0, sizeof(int32_t) * 8) == cudaSuccess;
+              cudaMemset(s.n_mtiles, 0, sizeof(int32_t) * 4) == cudaSuccess;
     if (ok && s.act_f32)
         ok = cudaMemset(s.asf32, 0, sizeof(float) * (size_t)s.Rmax * s.KB1) == cudaSuccess &&
              cudaMemset(s.hsf32, 0, sizeof(float) * (size_t)s.Rmax * s.KB2) == cudaSuccess;
@@ -269,16 +265,8 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
         ok = make_map(&s.tm_aq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.aq, s.H, s.Rmax, s.H, 128, boxes[i]) &&
              make_map(&s.tm_hq[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hq, s.I, s.Rmax, s.I, 128, boxes[i]);
     }
-    // activation scale chunks (per m-tile and K-step, 512 B) as rows of 128 B,
-    // four to a box (SM-pair GEMM)
-    if (ok)
-        ok = make_map(&s.tm_asf, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.asf, 128, (uint64_t)s.MTmax * s.KB1 * 4, 128, 128, 4,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
-             make_map(&s.tm_hsf, CU_TENSOR_MAP_DATA_TYPE_UINT8, s.hsf, 128, (uint64_t)s.MTmax * s.KB2 * 4, 128, 128, 4,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
     if (ok)
         ok = gemm_set_attributes() == cudaSuccess && router_set_attributes() == cudaSuccess;
-    if (ok) s.pair_grid = gemm_pair_grid(s.num_sms);
     if (ok) ok = cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         moe_destroy(h);
@@ -359,15 +347,8 @@ moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float
         return fail(h, MOE_ERR_INVALID_ARG, "moe_load_weights: an expert scale byte is 0xFF (E8M0 NaN)");
     }
     // interleaved blocks as 2-D tensors of 64-byte rows; a box covers one stage's weight rows
-    // (SM-pair GEMM: one half's 128 rows per box, and a stage's scale rows
-    // as plain 64-byte rows)
     if (!make_map(&s.tm_w13, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, d_13, 128, rows13, 64, 128, 256) ||
         !make_map(&s.tm_w2, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, d_2, 128, rows2, 64, 128, 128 * halves2) ||
-        !make_map(&s.tm_w13h, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, d_13, 128, rows13, 64, 128, 128) ||
-        !make_map(&s.tm_w2h, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, d_2, 128, rows2, 64, 128, 128) ||
-        !make_map(&s.tm_w13sf, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_13, 64, rows13, 64, 64, 16, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&s.tm_w2sf, CU_TENSOR_MAP_DATA_TYPE_UINT8, d_2, 64, rows2, 64, 64, 8 * halves2,
-                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map(&s.tm_wr64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_wr, H, E, H * 2, 64, 64) ||
         !make_map(&s.tm_wr128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d_wr, H, E, H * 2, 64, 128))
         return fail(h, MOE_ERR_CUDA, "moe_load_weights: cuTensorMapEncodeTiled failed for the weights");
@@ -522,12 +503,11 @@ moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, voi
         CUDA_TRY(h, launch_dispatch(s, x, T, st, &n));
     }
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[3], st));
-    // batches beyond one dispatch chunk (MXFP4 experts, power-of-two
-    // activation scales): heavy m-tiles in pairs on the SM-pair kernel
-    const bool pairs = T > kChunk && s.pair_grid > 0 && !s.act_f32 && !s.w_fp8;
-    CUDA_TRY(h, launch_gemm1(s, st, pairs, &n));
+    CUDA_TRY(h, launch_gemm1(s, st));   // light then heavy m-tiles, one launch
+    ++n;
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[4], st));
-    CUDA_TRY(h, launch_gemm2(s, st, pairs && s.BN2 == 256, &n));
+    CUDA_TRY(h, launch_gemm2(s, st));
+    ++n;
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[5], st));
     CUDA_TRY(h, launch_combine(s, y, T, st));
     ++n;

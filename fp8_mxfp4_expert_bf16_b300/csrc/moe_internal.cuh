@@ -56,12 +56,9 @@ struct DevState {
     int32_t* mtile_off;   // [E+1] exclusive scan of ceil(count/128)
     int32_t* mtile_expert;// [MTmax]
     int32_t* mtile_rows;  // [MTmax] valid rows of each m-tile (1..128)
-    int32_t* n_mtiles;    // [8]: all m-tiles, light m-tiles (<= kLightRows valid rows), heavy m-tiles,
-                          // heavy m-tile pairs, 0, heavy m-tiles left over from the pairs
+    int32_t* n_mtiles;    // [4]: all m-tiles, light m-tiles (<= kLightRows valid rows), heavy m-tiles
     int32_t* light_list;  // [MTmax] m-tiles with at most kLightRows valid rows (light GEMM shape)
     int32_t* heavy_list;  // [MTmax] the other m-tiles (128-row GEMMs)
-    int2* pairs;          // [MTmax] heavy m-tiles of one expert in consecutive pairs, for the SM-pair GEMM
-    int32_t* solo_list;   // [MTmax] an expert's odd heavy m-tile left over from the pairs
     int32_t* prow;        // [Tm*K] padded row of each (token, slot)
     uint8_t* aq;          // [Rmax][H]   e4m3 activations, expert-contiguous padded rows
     uint32_t* asf;        // [MTmax][KB1][128] scale words in tcgen05.cp order
@@ -75,10 +72,6 @@ struct DevState {
     // tensor maps (host copies, passed by value to the GEMM kernels)
     CUtensorMap tm_aq[kNumABox], tm_hq[kNumABox], tm_w13, tm_w2;
     CUtensorMap tm_wr64, tm_wr128;   // router weights, 64 / 128-row boxes
-    // SM-pair GEMM: half weight tiles (128 code rows), weight scale rows of a
-    // stage (16 rows of 64 B), activation scale chunks (four 128-byte rows)
-    CUtensorMap tm_w13h, tm_w2h, tm_w13sf, tm_w2sf, tm_asf, tm_hsf;
-    int pair_grid = 0;   // CTAs of the SM-pair GEMM (two per co-resident cluster); 0 = not used
     int num_sms;
     bool pdl = true;     // launch the forward's kernels with programmatic stream serialisation
 };
@@ -137,11 +130,8 @@ cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, c
 int router_split(int T, int H);
 cudaError_t router_set_attributes();
 // grouped GEMMs (mx_gemm.cu)
-// With `pairs`, heavy m-tiles of experts with two or more of them run on the
-// SM-pair kernel (a second launch); each call adds its launches to *nlaunch.
-cudaError_t launch_gemm1(const DevState& s, cudaStream_t st, bool pairs, int* nlaunch);
-cudaError_t launch_gemm2(const DevState& s, cudaStream_t st, bool pairs, int* nlaunch);
+cudaError_t launch_gemm1(const DevState& s, cudaStream_t st);
+cudaError_t launch_gemm2(const DevState& s, cudaStream_t st);
 cudaError_t gemm_set_attributes();
-int gemm_pair_grid(int num_sms);   // CTAs of the SM-pair kernel that can be co-resident (even), 0 if none
 
 }  // namespace moe

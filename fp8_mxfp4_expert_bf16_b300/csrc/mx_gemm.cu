@@ -112,9 +112,6 @@ struct GemmArgs {
     const float* ws;
     int early_trigger;           // let the next kernel be scheduled right after the wait (else at the end)
     int32_t* err;
-    // SM-pair kernel: heavy m-tiles of one expert in pairs, and their number
-    const int2* pairs;
-    const int32_t* pair_count;
 };
 
 template <int kStages>
@@ -140,29 +137,13 @@ struct GemmCtl {
 constexpr int kSmemBytes = kRingBytes + (int)sizeof(GemmCtl) + 1024;   // + alignment of the ring to 1 KB
 static_assert(kSmemBytes <= 232448, "shared memory");
 
-__device__ __forceinline__ void raise_error_flag(int* abort_flag, int32_t* err, int where)
+__device__ __forceinline__ void raise_error(GemmCtl* g, int32_t* err, int where)
 {
     if (atomicCAS(err, 0, kDevErrTimeout) == 0) {
         err[1] = where;
         err[2] = blockIdx.x;
     }
-    *(volatile int*)abort_flag = 1;
-}
-
-__device__ __forceinline__ void raise_error(GemmCtl* g, int32_t* err, int where)
-{
-    raise_error_flag(&g->abort, err, where);
-}
-
-// The epilogue's release of the accumulator: an arrive on this CTA's barrier,
-// or (kRemote) on a barrier given by its cluster-window address.
-template <bool kRemote>
-__device__ __forceinline__ void acc_release(uint32_t bar)
-{
-    if constexpr (kRemote)
-        mbar_arrive_cluster(bar);
-    else
-        mbar_arrive(bar);
+    *(volatile int*)&g->abort = 1;
 }
 
 template <int kStages>
@@ -223,7 +204,6 @@ __device__ __forceinline__ void producer_wait_once(bool& waited, int early_trigg
 // go to registers, the accumulator is released (arrive on `acc_empty`), then
 // each live lane stores its own row.  With so few rows the stores are short
 // and the accumulator is held only for the TMEM reads.
-template <bool kRemote = false>
 __device__ __forceinline__ void store_rows_direct(uint32_t taddr, int ncols, int live_rows, float* dst0,
                                                   size_t row_stride, uint32_t acc_empty, int lane)
 {
@@ -236,7 +216,7 @@ __device__ __forceinline__ void store_rows_direct(uint32_t taddr, int ncols, int
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) acc_release<kRemote>(acc_empty);
+    if (lane == 0) mbar_arrive(acc_empty);
     if (lane < live_rows) {
         float4* d4 = reinterpret_cast<float4*>(dst0 + (size_t)lane * row_stride);
 #pragma unroll
@@ -256,7 +236,7 @@ __device__ __forceinline__ void store_rows_direct(uint32_t taddr, int ncols, int
 // `acc_empty`) as soon as the last block has been read.  dst0 is row 0 of
 // the warp's 32 rows, `live_rows` how many of them are valid, rows
 // `row_stride` floats apart.
-template <int kCols, bool kRemote = false>
+template <int kCols>
 __device__ __forceinline__ void store_rows_transposed(uint32_t taddr, int live_rows, float* dst0, size_t row_stride,
                                                       uint32_t acc_empty, int lane)
 {
@@ -270,7 +250,7 @@ __device__ __forceinline__ void store_rows_transposed(uint32_t taddr, int live_r
         if (b == kCols / 32 - 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) acc_release<kRemote>(acc_empty);
+            if (lane == 0) mbar_arrive(acc_empty);
         }
         if (live_rows <= 0) continue;
 #pragma unroll
@@ -290,108 +270,6 @@ __device__ __forceinline__ void store_rows_transposed(uint32_t taddr, int live_r
         for (int j = 0; j < 32; ++j)
             if (j < live_rows) dst0[(size_t)j * row_stride + 32 * b + lane] = __uint_as_float(a[j]);
     }
-}
-
-// Default-mode epilogue of one tile for this epilogue warp (gate/up:
-// SwiGLU and the e4m3 re-quantisation of the row's 128-wide block; down: the
-// fp32 rows).  The accumulator is released by an arrive on `acc_empty`: this
-// CTA's barrier, or with kRemote the cluster address of the MMA-issuing
-// CTA's barrier (an SM pair).  Returns false after a wait has timed out.
-template <int kMode, bool kLight, bool kRemote, int kStages>
-__device__ __forceinline__ bool epilogue_tile(PhaseCtl<kStages>& pc, const GemmArgs& args, uint32_t tmem, int mt,
-                                              int nt, int rows, int tcount, const volatile int* abrt,
-                                              uint32_t acc_empty, int* abort_flag)
-{
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ew = warp - 2;                      // 0..7
-    const int q = warp & 3;                       // this warp's TMEM lane quarter
-    const int hw = ew >> 2;                       // which half of the columns
-    const int row = q * 32 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-        if (!mbar_wait(smem_u32(&pc.acc_full), (uint32_t)tcount & 1u, abrt)) {
-            raise_error_flag(abort_flag, args.err, 6);
-            return false;
-        }
-        tc_fence_after();
-        // Rows at or past `rows` hold padding or stale shared memory (any bit
-        // pattern): no arithmetic touches them, and a warp whose 32 rows are
-        // all invalid skips its TMEM loads entirely.
-        const bool warp_live = q * 32 < rows;
-        const bool row_live = row < rows;
-        if (kMode == 0) {
-            // this warp: middle columns [64 hw, 64 hw + 64) of the tile's 128
-            float h[64];
-            if (warp_live) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t gg[16], u[16];
-                    tmem_ld16(tl + kAccCol + 64u * hw + 16u * c, gg);
-                    tmem_ld16(tl + kAccCol + 128u + 64u * hw + 16u * c, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        // invalid rows are replaced by zeros before any arithmetic;
-                        // silu(g) = g / (1 + e^-g) with the fast exponential and
-                        // division intrinsics (a few ulp of fp32)
-                        const float gf = row_live ? __uint_as_float(gg[j]) : 0.0f;
-                        const float uf = row_live ? __uint_as_float(u[j]) : 0.0f;
-                        h[16 * c + j] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 64; ++j) h[j] = 0.0f;
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) acc_release<kRemote>(acc_empty);
-            // the row's amax over all 128 columns: combine with the partner warp
-            float amax = 0.f;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) amax = fmaxf(amax, fabsf(h[j]));
-            const int p = tcount & 1;
-            pc.red[p][ew][lane] = amax;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&pc.red_full[p]));
-            if (!mbar_wait(smem_u32(&pc.red_full[p]), (uint32_t)(tcount >> 1) & 1u, abrt)) {
-                raise_error_flag(abort_flag, args.err, 7);
-                return false;
-            }
-            amax = fmaxf(amax, pc.red[p][ew ^ 4][lane]);
-            if (row_live) {
-                const int ex = act_block_exponent(amax);
-                const float inv = __int_as_float((127 - ex) << 23);
-                uint4* dst =
-                    reinterpret_cast<uint4*>(args.hq + (size_t)(mt * kBM + row) * args.I + nt * 128 + 64 * hw);
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint4 w;
-                    w.x = e4m3x4(h[16 * v + 0] * inv, h[16 * v + 1] * inv, h[16 * v + 2] * inv, h[16 * v + 3] * inv);
-                    w.y = e4m3x4(h[16 * v + 4] * inv, h[16 * v + 5] * inv, h[16 * v + 6] * inv, h[16 * v + 7] * inv);
-                    w.z = e4m3x4(h[16 * v + 8] * inv, h[16 * v + 9] * inv, h[16 * v + 10] * inv, h[16 * v + 11] * inv);
-                    w.w = e4m3x4(h[16 * v + 12] * inv, h[16 * v + 13] * inv, h[16 * v + 14] * inv, h[16 * v + 15] * inv);
-                    dst[v] = w;
-                }
-                if (hw == 0)
-                    args.hsf[sf_word_index(mt, nt, args.I / 128, row)] = (uint32_t)(ex + 127) * 0x01010101u;
-            }
-        } else {
-            // this warp: output columns [hw * ncols / 2, (hw + 1) * ncols / 2).  The
-            // whole slice is read into registers first and the accumulator released,
-            // so the next tile's MMAs run while the rows are stored.
-            const int ncols = 128 * args.halves, half_cols = ncols / 2;
-            float* dst0 =
-                args.obuf + (size_t)(mt * kBM + q * 32) * args.H + (size_t)nt * ncols + hw * half_cols;
-            const int live = warp_live ? min(32, rows - q * 32) : 0;
-            const uint32_t taddr = tl + kAccCol + (uint32_t)(hw * half_cols);
-            if (kLight)
-                store_rows_direct<kRemote>(taddr, half_cols, live, dst0, (size_t)args.H, acc_empty, lane);
-            else if (half_cols == 128)
-                store_rows_transposed<128, kRemote>(taddr, live, dst0, (size_t)args.H, acc_empty, lane);
-            else
-                store_rows_transposed<64, kRemote>(taddr, live, dst0, (size_t)args.H, acc_empty, lane);
-        }
-    return true;
 }
 
 // One phase (the light or the heavy m-tile list) of the grouped GEMM.  Every
@@ -787,9 +665,90 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
         } else
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++tcount) {
             const int mt = list[tile / NT], nt = tile - (tile / NT) * NT;
-            if (!epilogue_tile<kMode, kLight, false>(pc, args, tmem, mt, nt, args.mtile_rows[mt], tcount, abrt,
-                                                     smem_u32(&pc.acc_empty), &g->abort))
+            const int rows = args.mtile_rows[mt];
+            if (!mbar_wait(smem_u32(&pc.acc_full), (uint32_t)tcount & 1u, abrt)) {
+                raise_error(g, args.err, 6);
                 break;
+            }
+            tc_fence_after();
+            // Rows at or past `rows` hold padding or stale shared memory (any bit
+            // pattern): no arithmetic touches them, and a warp whose 32 rows are
+            // all invalid skips its TMEM loads entirely.
+            const bool warp_live = q * 32 < rows;
+            const bool row_live = row < rows;
+            if (kMode == 0) {
+                // this warp: middle columns [64 hw, 64 hw + 64) of the tile's 128
+                float h[64];
+                if (warp_live) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t gg[16], u[16];
+                        tmem_ld16(tl + kAccCol + 64u * hw + 16u * c, gg);
+                        tmem_ld16(tl + kAccCol + 128u + 64u * hw + 16u * c, u);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            // invalid rows are replaced by zeros before any arithmetic;
+                            // silu(g) = g / (1 + e^-g) with the fast exponential and
+                            // division intrinsics (a few ulp of fp32)
+                            const float gf = row_live ? __uint_as_float(gg[j]) : 0.0f;
+                            const float uf = row_live ? __uint_as_float(u[j]) : 0.0f;
+                            h[16 * c + j] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) h[j] = 0.0f;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&pc.acc_empty));
+                // the row's amax over all 128 columns: combine with the partner warp
+                float amax = 0.f;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) amax = fmaxf(amax, fabsf(h[j]));
+                const int p = tcount & 1;
+                pc.red[p][ew][lane] = amax;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&pc.red_full[p]));
+                if (!mbar_wait(smem_u32(&pc.red_full[p]), (uint32_t)(tcount >> 1) & 1u, abrt)) {
+                    raise_error(g, args.err, 7);
+                    break;
+                }
+                amax = fmaxf(amax, pc.red[p][ew ^ 4][lane]);
+                if (row_live) {
+                    const int ex = act_block_exponent(amax);
+                    const float inv = __int_as_float((127 - ex) << 23);
+                    uint4* dst =
+                        reinterpret_cast<uint4*>(args.hq + (size_t)(mt * kBM + row) * args.I + nt * 128 + 64 * hw);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 w;
+                        w.x = e4m3x4(h[16 * v + 0] * inv, h[16 * v + 1] * inv, h[16 * v + 2] * inv, h[16 * v + 3] * inv);
+                        w.y = e4m3x4(h[16 * v + 4] * inv, h[16 * v + 5] * inv, h[16 * v + 6] * inv, h[16 * v + 7] * inv);
+                        w.z = e4m3x4(h[16 * v + 8] * inv, h[16 * v + 9] * inv, h[16 * v + 10] * inv, h[16 * v + 11] * inv);
+                        w.w = e4m3x4(h[16 * v + 12] * inv, h[16 * v + 13] * inv, h[16 * v + 14] * inv, h[16 * v + 15] * inv);
+                        dst[v] = w;
+                    }
+                    if (hw == 0)
+                        args.hsf[sf_word_index(mt, nt, args.I / 128, row)] = (uint32_t)(ex + 127) * 0x01010101u;
+                }
+            } else {
+                // this warp: output columns [hw * ncols / 2, (hw + 1) * ncols / 2).  The
+                // whole slice is read into registers first and the accumulator released,
+                // so the next tile's MMAs run while the rows are stored.
+                const int ncols = 128 * args.halves, half_cols = ncols / 2;
+                float* dst0 =
+                    args.obuf + (size_t)(mt * kBM + q * 32) * args.H + (size_t)nt * ncols + hw * half_cols;
+                const int live = warp_live ? min(32, rows - q * 32) : 0;
+                const uint32_t taddr = tl + kAccCol + (uint32_t)(hw * half_cols);
+                if (kLight)
+                    store_rows_direct(taddr, half_cols, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
+                else if (half_cols == 128)
+                    store_rows_transposed<128>(taddr, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
+                else
+                    store_rows_transposed<64>(taddr, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
+            }
         }
     }
 }
@@ -858,254 +817,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// ------------------------------------------------------------------------
-// SM-pair grouped GEMM for heavy m-tiles (clusters of two CTAs, tcgen05
-// cta_group::2).  A cluster takes two heavy m-tiles of one expert (one entry
-// of the pair list) against one 256-wide n-tile: the even CTA holds the first
-// m-tile's 128 activation rows and weight rows 0..127 of the n-tile, the odd
-// CTA the second m-tile's rows and weight rows 128..255; the even CTA's MMA
-// warp issues M = 256 MMAs that read both CTAs' shared memory, and each CTA's
-// TMEM accumulates its own m-tile against all 256 weight rows.  Per SM a
-// stage then holds half a weight tile (16 KB of shared memory instead of
-// 32 KB; in global memory each half is read once per 256 rows instead of
-// once per 128), so the stage's shared-memory traffic (copies in, MMA
-// operand reads out) drops by a third and the ring grows to 6 stages.
-// Every copy of both CTAs completes on the even CTA's stage barrier (armed
-// by the even CTA with both CTAs' byte counts; a copy may land before the
-// arming, the barrier's transaction count then goes negative and the phase
-// still needs the arming arrival); MMA completion is multicast to both
-// CTAs' barriers; each CTA's epilogue drains its own TMEM and arrives on the
-// even CTA's accumulator-free barrier.  Each CTA holds the activation
-// scales of its own rows and the weight scales of all 256 rows (the pair
-// form of tcgen05.cp copies each CTA's own chunk into its own TMEM).
-struct PairShape {
-    static constexpr int kStages = 6;
-    static constexpr int kABytes = kBM * 128;               // 128 activation rows x 128 B
-    static constexpr int kBOff = kABytes;
-    static constexpr int kSFAOff = kBOff + 128 * 128;       // half weight tile: 128 rows x 128 B (16-byte slots)
-    static constexpr int kSFBOff = kSFAOff + 512;           // activation scales of this CTA's rows
-    static constexpr int kStageStride = ((kSFBOff + 1024 + 1023) / 1024) * 1024;   // + weight scales, 256 rows
-    static constexpr int kRingBytes = kStages * kStageStride;
-};
-
-struct PairCtl {
-    PhaseCtl<PairShape::kStages> pc;   // full: used on the even CTA (both CTAs' copies); acc_empty: even CTA,
-                                       // both CTAs' epilogue warps; empty, acc_full, drain: both, multicast
-    uint32_t tmem_base;
-    int abort;
-};
-constexpr int kPairSmemBytes = PairShape::kRingBytes + (int)sizeof(PairCtl) + 1024;
-static_assert(kPairSmemBytes <= 232448, "shared memory");
-
-// activation box bytes of an m-tile with `rows` valid rows (32, 64 or 128-row box)
-__device__ __forceinline__ uint32_t pair_a_bytes(int rows)
-{
-    return rows <= 32 ? 32u * 128u : (rows <= 64 ? 64u * 128u : 128u * 128u);
-}
-
-template <int kMode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    k_mx_gemm_pair(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmWh,
-                   const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                   const GemmArgs args)
-{
-    using S = PairShape;
-    constexpr int kStages = S::kStages, kStageStride = S::kStageStride;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    PairCtl* ctl = reinterpret_cast<PairCtl*>(smem + S::kRingBytes);
-    PhaseCtl<kStages>& pc = ctl->pc;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const bool even = rank == 0;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&pc.full[s]), 1);
-            mbar_init(smem_u32(&pc.empty[s]), 1);
-        }
-        mbar_init(smem_u32(&pc.acc_full), 1);
-        mbar_init(smem_u32(&pc.acc_empty), 2 * kEpiWarps);
-        mbar_init(smem_u32(&pc.drain), 1);
-        mbar_init(smem_u32(&pc.red_full[0]), kEpiWarps);
-        mbar_init(smem_u32(&pc.red_full[1]), kEpiWarps);
-        ctl->abort = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&tmA0);
-        tma_prefetch_desc(&tmA1);
-        tma_prefetch_desc(&tmA2);
-        tma_prefetch_desc(&tmWh);
-        tma_prefetch_desc(&tmSFA);
-        tma_prefetch_desc(&tmSFB);
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
-        tmem_relinquish_pair();
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();   // both CTAs' barriers are initialised before any copy or arrive targets them
-    tc_fence_after();
-    const uint32_t tmem = ctl->tmem_base;
-    const volatile int* abrt = &ctl->abort;
-    const int NT = args.NT, KB = args.KB;
-    const int total = (*args.pair_count) * NT;
-    const int cid = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
-    bool waited = false;
-
-    if (warp == 0) {
-        if (lane == 0 && cid < total) {
-            // ------------------------------------------------ TMA producer (both CTAs)
-            const uint32_t full0 = mapa_shared(smem_u32(&pc.full[0]), 0);   // the even CTA's stage barriers
-            uint32_t last_phase[kStages];
-            bool issued[kStages];
-            for (int s = 0; s < kStages; ++s) issued[s] = false, last_phase[s] = 0;
-            int it = 0, pre = 0;
-            bool ok = true;
-            for (int tile = cid; tile < total && ok; tile += ncl) {
-                const int p = tile / NT, nt = tile - p * NT;
-                const int2 pr = args.pairs[p];
-                const int e = args.mtile_expert[pr.x];
-                const int rows0 = args.mtile_rows[pr.x], rows1 = args.mtile_rows[pr.y];
-                const int my_mt = even ? pr.x : pr.y;
-                const int my_rows = even ? rows0 : rows1;
-                const CUtensorMap* tA = my_rows <= 32 ? &tmA0 : (my_rows <= 64 ? &tmA1 : &tmA2);
-                // both CTAs' bytes of one stage: activation boxes and their scale
-                // chunks, half weight tiles (8 KB of codes each), all weight scales twice
-                const uint32_t tx = pair_a_bytes(rows0) + pair_a_bytes(rows1) + 2u * 512u + 2u * (kBHalfTxBytes + 1024u);
-                const int wrow0 = (int)(((size_t)(e * NT + nt) * KB) * 2 * kWBlockRowsPerHalf);
-                if (!waited) {
-                    // before the wait: this CTA's weight half and the weight scales of the first stages
-                    pre = KB < kStages ? KB : kStages;
-                    for (int kb = 0; kb < pre; ++kb) {
-                        uint8_t* st = smem + kb * kStageStride;
-                        if (even) mbar_arrive_expect_tx(smem_u32(&pc.full[kb]), tx);
-                        const uint32_t fb = full0 + 8u * kb;
-                        const int wrow = wrow0 + kb * 2 * kWBlockRowsPerHalf;
-                        tma_load_2d_pair(smem_u32(st + S::kBOff), &tmWh, fb, 0, wrow + 128 * (int)rank);
-                        tma_load_2d_pair(smem_u32(st + S::kSFBOff), &tmSFB, fb, 0, wrow + 256);
-                        issued[kb] = true;
-                        last_phase[kb] = 0;
-                    }
-                    producer_wait_once(waited, args.early_trigger);
-                    for (int kb = 0; kb < pre; ++kb) {
-                        uint8_t* st = smem + kb * kStageStride;
-                        const uint32_t fb = full0 + 8u * kb;
-                        tma_load_2d_pair(smem_u32(st), tA, fb, kb * kBK, my_mt * kBM);
-                        tma_load_2d_pair(smem_u32(st + S::kSFAOff), &tmSFA, fb, 0, (my_mt * KB + kb) * 4);
-                    }
-                }
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    if (it < pre) continue;   // issued around the wait
-                    const int s = it % kStages;
-                    const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-                    if (!mbar_wait(smem_u32(&pc.empty[s]), ph ^ 1u, abrt)) {
-                        raise_error_flag(&ctl->abort, args.err, 21);
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* st = smem + s * kStageStride;
-                    if (even) mbar_arrive_expect_tx(smem_u32(&pc.full[s]), tx);
-                    const uint32_t fb = full0 + 8u * s;
-                    const int wrow = wrow0 + kb * 2 * kWBlockRowsPerHalf;
-                    tma_load_2d_pair(smem_u32(st), tA, fb, kb * kBK, my_mt * kBM);
-                    tma_load_2d_pair(smem_u32(st + S::kSFAOff), &tmSFA, fb, 0, (my_mt * KB + kb) * 4);
-                    tma_load_2d_pair(smem_u32(st + S::kBOff), &tmWh, fb, 0, wrow + 128 * (int)rank);
-                    tma_load_2d_pair(smem_u32(st + S::kSFBOff), &tmSFB, fb, 0, wrow + 256);
-                    issued[s] = true;
-                    last_phase[s] = ph;
-                }
-            }
-            // the even CTA's stage barriers count both CTAs' copies: once they
-            // have completed, nothing is in flight into either CTA
-            int zero = 0;
-            if (even)
-                for (int s = 0; s < kStages; ++s)
-                    if (issued[s] && !mbar_wait(smem_u32(&pc.full[s]), last_phase[s], &zero))
-                        raise_error_flag(&ctl->abort, args.err, 22);
-        }
-    } else if (warp == 1) {
-        if (even) {
-            // -------------------------------------------- MMA issuer (even CTA, whole warp)
-            const uint32_t idesc = idesc_mxf8f6f4(256, 256, kTypeE4M3, kTypeE2M1);
-            const uint32_t s0 = smem_u32(smem);
-            const uint64_t ad0 = desc_kmajor_sw128(s0), bd0 = desc_kmajor_sw128(s0 + S::kBOff);
-            const uint64_t sfad0 = desc_sf_chunk(s0 + S::kSFAOff), sfbd0 = desc_sf_chunk(s0 + S::kSFBOff);
-            const uint32_t id1 = idesc_with_sf_id(idesc, 1, 1), id2 = idesc_with_sf_id(idesc, 2, 2),
-                           id3 = idesc_with_sf_id(idesc, 3, 3);
-            const uint32_t full0 = smem_u32(&pc.full[0]), empty0 = smem_u32(&pc.empty[0]);
-            const uint32_t acc = tmem + kAccCol;
-            int s = 0, tcount = 0;
-            uint32_t ph = 0, doff = 0;
-            bool ok = true;
-            for (int tile = cid; tile < total && ok; tile += ncl, ++tcount) {
-                if (tcount > 0 &&
-                    !__all_sync(~0u, mbar_wait(smem_u32(&pc.acc_empty), (uint32_t)(tcount - 1) & 1u, abrt))) {
-                    if (lane == 0) raise_error_flag(&ctl->abort, args.err, 23);
-                    break;
-                }
-                tc_fence_after();
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!__all_sync(~0u, mbar_wait(full0 + 8u * s, ph, abrt))) {
-                        if (lane == 0) raise_error_flag(&ctl->abort, args.err, 24);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sfa_t = tmem + kSFCol + 16u * s;
-                    const uint64_t ad = ad0 + doff, bd = bd0 + doff;
-                    tmem_cp_32x128b_warpx4_pair_elect(sfa_t, sfad0 + doff);
-                    tmem_cp_32x128b_warpx4_pair_elect(sfa_t + 8u, sfbd0 + doff);
-                    tmem_cp_32x128b_warpx4_pair_elect(sfa_t + 12u, sfbd0 + doff + (512 >> 4));
-                    mma_mxf8f6f4_pair_elect(acc, ad, bd, idesc, sfa_t, sfa_t + 8u, kb != 0 ? 1u : 0u);
-                    mma_mxf8f6f4_pair_elect(acc, ad + 2, bd + 2, id1, sfa_t, sfa_t + 8u, 1u);
-                    mma_mxf8f6f4_pair_elect(acc, ad + 4, bd + 4, id2, sfa_t, sfa_t + 8u, 1u);
-                    mma_mxf8f6f4_pair_elect(acc, ad + 6, bd + 6, id3, sfa_t, sfa_t + 8u, 1u);
-                    tc_commit_pair_elect(empty0 + 8u * s, 0x3);
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1u;
-                        doff = 0;
-                    } else {
-                        doff += kStageStride >> 4;
-                    }
-                }
-                if (ok) tc_commit_pair_elect(smem_u32(&pc.acc_full), 0x3);
-            }
-            tc_commit_pair_elect(smem_u32(&pc.drain), 0x3);
-        }
-        // both CTAs: every MMA has completed before the ring or TMEM is released
-        int zero = 0;
-        if (!mbar_wait(smem_u32(&pc.drain), 0u, &zero) && lane == 0) raise_error_flag(&ctl->abort, args.err, 25);
-    } else {
-        // ---------------------------------------------------- epilogue (both CTAs)
-        const uint32_t acc_empty_even = mapa_shared(smem_u32(&pc.acc_empty), 0);
-        int tcount = 0;
-        for (int tile = cid; tile < total; tile += ncl, ++tcount) {
-            const int p = tile / NT, nt = tile - p * NT;
-            const int2 pr = args.pairs[p];
-            const int mt = even ? pr.x : pr.y;
-            if (!epilogue_tile<kMode, false, true>(pc, args, tmem, mt, nt, args.mtile_rows[mt], tcount, abrt,
-                                                   acc_empty_even, &ctl->abort))
-                break;
-        }
-    }
-
-    // a CTA without tiles still waits before it lets the next kernel start
-    if (warp == 0 && lane == 0) {
-        producer_wait_once(waited, args.early_trigger);
-        griddep_launch_dependents();
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();   // no copy, MMA or arrive of either CTA targets the other after this
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc_pair(tmem, kTmemCols);
-    }
-}
-
 cudaError_t gemm_set_attributes()
 {
     const void* ks[] = {(const void*)k_mx_gemm<0, false, false>, (const void*)k_mx_gemm<1, false, false>,
@@ -1115,37 +826,7 @@ cudaError_t gemm_set_attributes()
     cudaError_t e = cudaSuccess;
     for (const void* k : ks)
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_mx_gemm_pair<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_mx_gemm_pair<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
     return e;
-}
-
-// CTAs of the SM-pair kernel that can be resident at once (two per cluster;
-// at most one CTA per SM), 0 if none.
-int gemm_pair_grid(int num_sms)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_sms & ~1);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kPairSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0, n2 = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_mx_gemm_pair<0>, &cfg) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n2, k_mx_gemm_pair<1>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    if (n2 < n) n = n2;
-    if (2 * n > num_sms) n = num_sms / 2;
-    return 2 * n;
 }
 
 static GemmArgs common_args(const DevState& s)
@@ -1157,8 +838,6 @@ static GemmArgs common_args(const DevState& s)
     a.light_count = s.n_mtiles + 1;
     a.heavy_list = s.heavy_list;
     a.heavy_count = s.n_mtiles + 2;
-    a.pairs = s.pairs;
-    a.pair_count = s.n_mtiles + 3;
     a.err = s.err;
     return a;
 }
@@ -1210,45 +889,25 @@ static cudaError_t launch_mode(const DevState& s, cudaStream_t st, const GemmArg
                      : launch_variant<kMode, false, false>(s, st, a, tA, tW);
 }
 
-// Single-SM kernel: light m-tiles (activation boxes of 8 / 16 rows: maps 0,
-// 1), then heavy m-tiles (32 / 64 / 128 rows: maps 2..4), in one launch.
-// With `pairs` its heavy list holds only the m-tiles left over from the
-// pairs, and the SM-pair kernel follows for the pairs.
-cudaError_t launch_gemm1(const DevState& s, cudaStream_t st, bool pairs, int* nlaunch)
+// Light m-tiles (activation boxes of 8 / 16 rows: maps 0, 1), then heavy
+// m-tiles (32 / 64 / 128 rows: maps 2..4), in one launch.
+cudaError_t launch_gemm1(const DevState& s, cudaStream_t st)
 {
     GemmArgs a = gemm1_args(s);
-    a.early_trigger = 1;   // the down GEMM, or the pair kernel, follows
+    a.early_trigger = 1;   // the down GEMM follows
     a.as32 = s.asf32;
     a.hs32 = s.hsf32;
     a.ws = s.ws13;
-    if (pairs) a.heavy_list = s.solo_list, a.heavy_count = s.n_mtiles + 5;
-    cudaError_t e = launch_mode<0>(s, st, a, s.tm_aq, s.tm_w13);
-    ++*nlaunch;
-    if (e != cudaSuccess || !pairs) return e;
-    GemmArgs b = gemm1_args(s);
-    b.early_trigger = 1;
-    e = launch_kernel(k_mx_gemm_pair<0>, dim3(s.pair_grid), dim3(kThreads), kPairSmemBytes, st, s.pdl, s.tm_aq[2],
-                      s.tm_aq[3], s.tm_aq[4], s.tm_w13h, s.tm_asf, s.tm_w13sf, b);
-    ++*nlaunch;
-    return e;
+    return launch_mode<0>(s, st, a, s.tm_aq, s.tm_w13);
 }
 
-cudaError_t launch_gemm2(const DevState& s, cudaStream_t st, bool pairs, int* nlaunch)
+cudaError_t launch_gemm2(const DevState& s, cudaStream_t st)
 {
     GemmArgs a = gemm2_args(s);
-    a.early_trigger = pairs ? 1 : 0;   // the pair kernel, or the combine, follows
+    a.early_trigger = 0;   // the combine follows
     a.as32 = s.hsf32;
     a.ws = s.ws2;
-    if (pairs) a.heavy_list = s.solo_list, a.heavy_count = s.n_mtiles + 5;
-    cudaError_t e = launch_mode<1>(s, st, a, s.tm_hq, s.tm_w2);
-    ++*nlaunch;
-    if (e != cudaSuccess || !pairs) return e;
-    GemmArgs b = gemm2_args(s);
-    b.early_trigger = 0;   // the combine follows
-    e = launch_kernel(k_mx_gemm_pair<1>, dim3(s.pair_grid), dim3(kThreads), kPairSmemBytes, st, s.pdl, s.tm_hq[2],
-                      s.tm_hq[3], s.tm_hq[4], s.tm_w2h, s.tm_hsf, s.tm_w2sf, b);
-    ++*nlaunch;
-    return e;
+    return launch_mode<1>(s, st, a, s.tm_hq, s.tm_w2);
 }
 
 }  // namespace moe

@@ -231,110 +231,6 @@ __device__ __forceinline__ void tc_commit_elect(uint32_t bar)
         : "memory");
 }
 
-// ---------------------------------------------- clusters of two CTAs (an SM pair)
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of both CTAs: release this CTA's prior shared-memory writes
-// and wait for the peer's.
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address, in the cluster's shared window, of the same shared-memory offset
-// in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-// Arrive on an mbarrier given by its cluster-window address (this CTA's or the peer's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// 2-D tiled copy into this CTA's shared memory whose completion is counted
-// on an mbarrier of either CTA of the pair (cluster-window address).  The
-// innermost coordinate c0 times the element size is a multiple of 16 bytes.
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
-                                                 int c1)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
-        "[%2];" ::"r"(dst),
-        "l"(map), "r"(bar_cluster), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-// TMEM allocation of an SM pair: both CTAs execute it (one warp each) and
-// receive the same column range in their own Tensor Memory.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot_smem, uint32_t ncols)
-{
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish_pair()
-{
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
-{
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// SM-pair forms, issued from the whole converged MMA warp of the pair's
-// even CTA (one elected lane issues).  M = 256 block-scaled MMA: A rows
-// 0..127 come from the even CTA's tile, 128..255 from the odd CTA's (same
-// shared-memory offset); B's first N/2 rows from the even CTA, the rest from
-// the odd one; each CTA's TMEM receives its own 128 rows x N accumulator and
-// holds the A scales of its own rows and the B scales of all N rows.
-__device__ __forceinline__ void mma_mxf8f6f4_pair_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                                        uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
-}
-
-// Each CTA of the pair copies the chunk at this shared-memory offset of its
-// own shared memory into its own TMEM.
-__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair_elect(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile(
-        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
-        "l"(sdesc)
-        : "memory");
-}
-
-// Arrive on the mbarrier at offset `bar` in every CTA of `mask` once the
-// pair's previously issued tcgen05 operations have completed.
-__device__ __forceinline__ void tc_commit_pair_elect(uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
-            bar),
-        "h"(mask)
-        : "memory");
-}
-
 // Arrive on `bar` once all previously issued tcgen05 async operations of
 // this thread have completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar)

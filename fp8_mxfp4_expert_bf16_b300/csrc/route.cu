@@ -280,18 +280,14 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot)
 // expert counts, exclusive scans (offsets, m-tile offsets) and the m-tile
 // lists: every 128-row m-tile with its expert and valid rows, and the split
 // into light m-tiles (at most kLightRows valid rows: only an expert's last
-// m-tile can be one) and heavy m-tiles, each list in m-tile order; the
-// heavy m-tiles of each expert also in consecutive pairs for the SM-pair
-// GEMM, with an odd one left over in a list of its own (it then runs on the
-// single-SM GEMM).
+// m-tile can be one) and heavy m-tiles, each list in m-tile order.
 __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict__ chunk_hist,
                                                       int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
                                                       int32_t* __restrict__ offsets, int32_t* __restrict__ mtile_off,
                                                       int32_t* __restrict__ mtile_expert,
                                                       int32_t* __restrict__ mtile_rows, int32_t* __restrict__ n_mtiles,
                                                       int32_t* __restrict__ light_list,
-                                                      int32_t* __restrict__ heavy_list, int2* __restrict__ pairs,
-                                                      int32_t* __restrict__ solo_list, int nchunk, int E)
+                                                      int32_t* __restrict__ heavy_list, int nchunk, int E)
 {
     griddep_wait();
     griddep_launch_dependents();
@@ -314,10 +310,6 @@ __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict_
     const int ex_mt = block_exclusive_scan<kMaxExperts>(mt, warp_tot);
     const int ex_light = block_exclusive_scan<kMaxExperts>(light, warp_tot);
     const int ex_heavy = block_exclusive_scan<kMaxExperts>(heavy, warp_tot);
-    const int npair = heavy / 2;
-    const int solo = heavy & 1;
-    const int ex_pair = block_exclusive_scan<kMaxExperts>(npair, warp_tot);
-    const int ex_solo = block_exclusive_scan<kMaxExperts>(solo, warp_tot);
     if (e < E) {
         offsets[e] = ex_cnt;
         mtile_off[e] = ex_mt;
@@ -326,8 +318,6 @@ __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict_
             mtile_rows[ex_mt + m] = min(kBM, run - kBM * m);
         }
         for (int m = 0; m < heavy; ++m) heavy_list[ex_heavy + m] = ex_mt + m;
-        for (int j = 0; j < npair; ++j) pairs[ex_pair + j] = make_int2(ex_mt + 2 * j, ex_mt + 2 * j + 1);
-        if (solo) solo_list[ex_solo] = ex_mt + heavy - 1;
         if (light) light_list[ex_light] = ex_mt + mt - 1;
         if (e == E - 1) {
             offsets[E] = ex_cnt + run;
@@ -335,8 +325,6 @@ __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict_
             n_mtiles[0] = ex_mt + mt;
             n_mtiles[1] = ex_light + light;
             n_mtiles[2] = ex_heavy + heavy;
-            n_mtiles[3] = ex_pair + npair;
-            n_mtiles[5] = ex_solo + solo;
         }
     }
 }
@@ -545,7 +533,7 @@ cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStr
     if (e == cudaSuccess)
         e = launch_kernel(k_scan, dim3(1), dim3(kMaxExperts), 0, st, s.pdl, (const int32_t*)s.chunk_hist, s.chunk_base,
                           s.counts, s.offsets, s.mtile_off, s.mtile_expert, s.mtile_rows, s.n_mtiles, s.light_list,
-                          s.heavy_list, s.pairs, s.solo_list, nchunk, s.E);
+                          s.heavy_list, nchunk, s.E);
     if (e == cudaSuccess)
         e = launch_kernel(k_scatter_rows, dim3(nchunk), dim3(kChunk), 0, st, s.pdl, (const int32_t*)s.ids,
                           (const int32_t*)s.chunk_base, (const int32_t*)s.mtile_off, s.prow, T, s.E, s.K);
