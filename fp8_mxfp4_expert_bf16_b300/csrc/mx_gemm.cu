@@ -82,6 +82,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;      // accumulator: 256 fp32 columns
 constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), SFB at +8 (8 cols)
 constexpr uint32_t kSFUnitCol = 352; // promotion modes: a constant unit scale chunk, twice (8 cols)
+constexpr uint32_t kStashCol = 384;  // gate/up epilogue: the tile's up columns parked here (128 cols)
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, epilogue warps
 
@@ -679,6 +680,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
             if (kMode == 0) {
                 // this warp: middle columns [64 hw, 64 hw + 64) of the tile's 128
                 float h[64];
+                const uint32_t stash = tl + kStashCol + 64u * hw;
                 if (warp_live) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -686,12 +688,24 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         tmem_ld16(tl + kAccCol + 64u * hw + 16u * c, gg);
                         tmem_ld16(tl + kAccCol + 128u + 64u * hw + 16u * c, u);
                         tmem_ld_wait();
+                        tmem_st16(stash + 16u * c, u);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) h[16 * c + j] = __uint_as_float(gg[j]);
+                        tmem_st_wait();
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&pc.acc_empty));
+                if (warp_live) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t u[16];
+                        tmem_ld16(stash + 16u * c, u);
+                        tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            // invalid rows are replaced by zeros before any arithmetic;
-                            // silu(g) = g / (1 + e^-g) with the fast exponential and
-                            // division intrinsics (a few ulp of fp32)
-                            const float gf = row_live ? __uint_as_float(gg[j]) : 0.0f;
+                            const float gf = row_live ? h[16 * c + j] : 0.0f;
                             const float uf = row_live ? __uint_as_float(u[j]) : 0.0f;
                             h[16 * c + j] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
                         }
@@ -700,9 +714,6 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
 #pragma unroll
                     for (int j = 0; j < 64; ++j) h[j] = 0.0f;
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&pc.acc_empty));
                 // the row's amax over all 128 columns: combine with the partner warp
                 float amax = 0.f;
 #pragma unroll
