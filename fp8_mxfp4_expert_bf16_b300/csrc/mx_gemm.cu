@@ -82,6 +82,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;      // accumulator: 256 fp32 columns
 constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), SFB at +8 (8 cols)
 constexpr uint32_t kSFUnitCol = 352; // promotion modes: a constant unit scale chunk, twice (8 cols)
+constexpr uint32_t kStashHeavyCol = 320;  // down epilogue, heavy phase: 3 x 32 columns per warp parked here
 constexpr uint32_t kStashCol = 384;  // gate/up epilogue: the tile's up columns parked here (128 cols)
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, epilogue warps
@@ -238,17 +239,27 @@ __device__ __forceinline__ void store_rows_direct(uint32_t taddr, int ncols, int
 // the warp's 32 rows, `live_rows` how many of them are valid, rows
 // `row_stride` floats apart.
 template <int kCols>
-__device__ __forceinline__ void store_rows_transposed(uint32_t taddr, int live_rows, float* dst0, size_t row_stride,
-                                                      uint32_t acc_empty, int lane)
+__device__ __forceinline__ void store_rows_transposed(uint32_t taddr, uint32_t stash, int live_rows, float* dst0,
+                                                      size_t row_stride, uint32_t acc_empty, int lane)
 {
+    if (live_rows > 0) {
+#pragma unroll 1
+        for (int b = 1; b < kCols / 32; ++b) {
+            uint32_t a[32];
+            tmem_ld32(taddr + 32u * b, a);
+            tmem_ld_wait();
+            tmem_st32(stash + 32u * (b - 1), a);
+            tmem_st_wait();
+        }
+    }
 #pragma unroll 1
     for (int b = 0; b < kCols / 32; ++b) {
         uint32_t a[32];
         if (live_rows > 0) {
-            tmem_ld32(taddr + 32u * b, a);
+            tmem_ld32(b == 0 ? taddr : stash + 32u * (b - 1), a);
             tmem_ld_wait();
         }
-        if (b == kCols / 32 - 1) {
+        if (b == 0) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
@@ -756,9 +767,11 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 if (kLight)
                     store_rows_direct(taddr, half_cols, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
                 else if (half_cols == 128)
-                    store_rows_transposed<128>(taddr, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
+                    store_rows_transposed<128>(taddr, tl + kStashHeavyCol + 96u * hw, live, dst0, (size_t)args.H,
+                                               smem_u32(&pc.acc_empty), lane);
                 else
-                    store_rows_transposed<64>(taddr, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
+                    store_rows_transposed<64>(taddr, tl + kStashHeavyCol + 96u * hw, live, dst0, (size_t)args.H,
+                                              smem_u32(&pc.acc_empty), lane);
             }
         }
     }
