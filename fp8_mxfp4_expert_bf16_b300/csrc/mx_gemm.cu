@@ -23,12 +23,17 @@
 //               kind::mxf8f6f4) and both scale-factor chunks;
 //   warp 1      TMEM owner and MMA issuer: copies the scale chunks into
 //               TMEM (tcgen05.cp) and issues 4 block-scaled 128x256x32 MMAs
-//               per stage into one fp32 accumulator in TMEM;
+//               per stage into one fp32 accumulator in TMEM; the whole warp
+//               runs the loop and one elected lane issues each operation;
 //   warps 2-9   epilogue (two warps per TMEM lane quarter, each half of the
 //               columns): TMEM -> registers; gate/up: h = silu(g) * u and
 //               re-quantisation of h to e4m3 per 1 x 128 block (the two
 //               warps of a row combine their amax through shared memory);
-//               down: fp32 rows to the expert-output buffer.
+//               down: fp32 rows to the expert-output buffer.  The single
+//               accumulator (TMEM also holds the scale chunks, so it cannot
+//               be double-buffered) is released early by parking columns in
+//               the TMEM columns the phase leaves free: the up half (gate/up)
+//               or three of each warp's four column blocks (down, heavy).
 // Programmatic dependent launch: the kernel may start while the previous
 // kernel of the forward (which writes the activations) is still running.
 // Before waiting for it, the producer streams what does not depend on it:
@@ -84,6 +89,10 @@ constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), 
 constexpr uint32_t kSFUnitCol = 352; // promotion modes: a constant unit scale chunk, twice (8 cols)
 constexpr uint32_t kStashHeavyCol = 320;  // down epilogue, heavy phase: 3 x 32 columns per warp parked here
 constexpr uint32_t kStashCol = 384;  // gate/up epilogue: the tile's up columns parked here (128 cols)
+static_assert(kSFCol + 16 * Shape<false>::kStages <= kStashHeavyCol && kStashHeavyCol + 2 * 96 <= kTmemCols,
+              "heavy-phase down stash overlaps the heavy ring's scale chunks");
+static_assert(kSFCol + 16 * Shape<true>::kStages <= kStashCol && kStashCol + 128 <= kTmemCols,
+              "gate/up stash overlaps the light ring's scale chunks");
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, epilogue warps
 
@@ -230,14 +239,16 @@ __device__ __forceinline__ void store_rows_direct(uint32_t taddr, int ncols, int
 }
 
 // Down-GEMM epilogue of one warp, heavy m-tiles: kCols (64 or 128) fp32
-// accumulator columns of its 32 TMEM lanes (rows), 32 columns at a time: read into
-// registers, transposed across the warp with a five-step butterfly of
-// shuffles so that lane l holds column l of all 32 rows, and stored one row
-// per instruction (32 lanes x 4 B = one full 128-byte line, instead of 32
-// rows' 16-byte pieces).  The accumulator is released (arrive on
-// `acc_empty`) as soon as the last block has been read.  dst0 is row 0 of
-// the warp's 32 rows, `live_rows` how many of them are valid, rows
-// `row_stride` floats apart.
+// accumulator columns of its 32 TMEM lanes (rows), in blocks of 32 columns.
+// Blocks 1.. are first copied to `stash` (TMEM columns outside the
+// accumulator, through registers), block 0 is read, and the accumulator is
+// released (arrive on `acc_empty`).  Then each block, from registers or
+// read back from the stash, is transposed across the warp with a five-step
+// butterfly of shuffles so that lane l holds column l of all 32 rows, and
+// stored one row per instruction (32 lanes x 4 B = one full 128-byte line,
+// instead of 32 rows' 16-byte pieces).  dst0 is row 0 of the warp's 32
+// rows, `live_rows` how many of them are valid, rows `row_stride` floats
+// apart.
 template <int kCols>
 __device__ __forceinline__ void store_rows_transposed(uint32_t taddr, uint32_t stash, int live_rows, float* dst0,
                                                       size_t row_stride, uint32_t acc_empty, int lane)
