@@ -350,18 +350,39 @@ class Forward:
     y: np.ndarray           # u16 [n, H] bf16 output
 
 
+def route_with_ids(r: Route, ids: np.ndarray) -> Route:
+    """The same router output with a given selection ``ids`` [T, k] in place
+    of the oracle's own top-k: gates = the given experts' scores / their sum.
+
+    Where two keys are closer than the rounding of a device's fp32 logits,
+    both selections are correct (the device tests accept either); the layer's
+    later steps are then checked against this variant fed the device's
+    choice.  The keys and margins stay the oracle's.
+    """
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    assert ids.shape == r.ids.shape
+    sel = np.take_along_axis(r.scores, ids.astype(np.int64), axis=1)
+    gates = sel / sel.sum(axis=1, keepdims=True)
+    return Route(ids, gates, r.logits, r.scores, r.keys, r.margin)
+
+
 def forward(x_bf16, router_w_bf16, w13_q, w13_s, w2_q, w2_s, k: int,
             score_func: int = SCORE_SIGMOID, logit_bias=None, sel_bias=None,
-            tokens=None, act_scale_mode: int = ACT_SCALE_E8M0, weight_format: str = "mxfp4") -> Forward:
+            tokens=None, act_scale_mode: int = ACT_SCALE_E8M0, weight_format: str = "mxfp4",
+            ids=None) -> Forward:
     """The whole layer: route, dispatch, quantise, experts, combine.
 
     Routing, counts, offsets and the permutation cover every token; the
     expert FFNs and the output are computed for ``tokens`` (default: all).
     y[t] = bf16_rne( sum_j gate[t, j] * o[t, j] ), the sum in fp64.
+    ``ids`` (optional, int [T, k]) replaces the top-k selection for every
+    later step (see ``route_with_ids``).
     """
     T, H = x_bf16.shape
     E = router_w_bf16.shape[0]
     r = route(x_bf16, router_w_bf16, k, score_func, logit_bias, sel_bias)
+    if ids is not None:
+        r = route_with_ids(r, ids)
     counts, offsets, perm = dispatch(r.ids, E)
     toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     n = toks.size
@@ -384,3 +405,35 @@ def forward(x_bf16, router_w_bf16, w13_q, w13_s, w2_q, w2_s, k: int,
     g = r.gates[toks]
     y64 = np.einsum("nk,nkh->nh", g, o)
     return Forward(r, counts, offsets, perm, toks, aq, as_, hq, hs, h, o, y64, f64_to_bf16(y64))
+
+
+def tp_partials(f: Forward, w2_q, w2_s, G: int, weight_format: str = "mxfp4"):
+    """The layer output split over G tensor-parallel shards of the expert
+    middle dimension, as the pages deploy it (vLLM recipe
+    "XiaomiMiMo/MiMo-V2.6-Pro-RL", "Overview": TP8 on H200, TP4 on MI355X).
+
+    Shard r holds middle columns [r I/G, (r+1) I/G) of every expert: its
+    SwiGLU codes are those columns of the layer's Q2 codes (I/G is a multiple
+    of 128, so no 1 x 128 block straddles two shards), its down projection
+    the same columns of W2, and its partial output
+        y_r[t] = sum_j gate[t, j] * dequant(hq[t, j, cols_r]) . W2[e_j][:, cols_r]^T
+    in fp64.  The layer output is bf16( sum_r y_r ).  Returns the G partials
+    (float64 [n, H] each, for the tokens of ``f``).
+    """
+    decode = fp8_block_decode if weight_format == "fp8" else mxfp4_decode
+    n, k, I = f.hq.shape
+    H = f.o.shape[2]
+    assert I % (128 * G) == 0
+    Il = I // G
+    sel = f.route.ids[f.tokens]
+    a = act_dequant(f.hq.reshape(n * k, I), f.hs.reshape(n * k, I // 128), 128).reshape(n, k, I)
+    parts = []
+    for r in range(G):
+        cols = slice(r * Il, (r + 1) * Il)
+        o = np.zeros((n, k, H), dtype=np.float64)
+        for e in np.unique(sel):
+            rows, slots = np.nonzero(sel == e)
+            W2 = decode(w2_q[e], w2_s[e])
+            o[rows, slots] = a[rows, slots][:, cols] @ W2[:, cols].T
+        parts.append(np.einsum("nk,nkh->nh", f.route.gates[f.tokens], o))
+    return parts

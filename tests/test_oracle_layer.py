@@ -265,3 +265,78 @@ def test_forward_structural_invariants():
     for e in range(E):
         rows = f.perm[flat == e]
         assert np.array_equal(np.sort(rows), np.arange(f.offsets[e], f.offsets[e + 1]))
+
+
+# ----------------------------------------------------------- routing override
+def _small_layer(seed, T=6, H=128, E=8, I=128, k=2):
+    inp = synth.custom_inputs(T, H, E, I, k, seed=seed, bias="normal:0.3")
+    c = inp.cfg
+    args = (inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
+    kw = dict(score_func=c.score_func, logit_bias=inp.logit_bias, sel_bias=inp.sel_bias)
+    return inp, args, kw
+
+
+def test_forward_with_its_own_ids_is_the_plain_forward():
+    inp, args, kw = _small_layer(41)
+    f0 = oracle.forward(*args, 2, **kw)
+    f1 = oracle.forward(*args, 2, **kw, ids=f0.route.ids.copy())
+    for name in ["counts", "offsets", "perm", "aq", "as_", "hq", "hs", "h", "o", "y64", "y"]:
+        assert np.array_equal(getattr(f0, name), getattr(f1, name)), name
+    assert np.array_equal(f0.route.gates, f1.route.gates)
+
+
+def test_forward_with_other_ids_reuses_each_token_expert_output():
+    """An expert's output for a token depends only on that (token, expert)
+    pair: with the override (1st, 3rd choice) the 1st slot equals the plain
+    top-2 forward's slot 0 and the 2nd slot equals the plain top-3 forward's
+    slot 2; gates renormalise the chosen scores; dispatch follows the ids."""
+    inp, args, kw = _small_layer(42)
+    f2 = oracle.forward(*args, 2, **kw)
+    f3 = oracle.forward(*args, 3, **kw)
+    ids = np.stack([f3.route.ids[:, 0], f3.route.ids[:, 2]], axis=1).astype(np.int32)
+    fo = oracle.forward(*args, 2, **kw, ids=ids)
+    assert np.array_equal(fo.route.ids, ids)
+    assert np.array_equal(fo.o[:, 0], f2.o[:, 0]) and np.array_equal(fo.hq[:, 0], f2.hq[:, 0])
+    assert np.array_equal(fo.o[:, 1], f3.o[:, 2]) and np.array_equal(fo.hq[:, 1], f3.hq[:, 2])
+    s = np.take_along_axis(f3.route.scores, ids.astype(np.int64), axis=1)
+    np.testing.assert_allclose(fo.route.gates, s / s.sum(axis=1, keepdims=True), rtol=1e-15)
+    assert np.array_equal(fo.counts, np.bincount(ids.reshape(-1), minlength=inp.cfg.E))
+    flat = ids.reshape(-1)
+    for e in range(inp.cfg.E):   # rows of expert e: contiguous, token-ascending
+        rows = fo.perm[flat == e]
+        assert np.array_equal(rows, np.arange(fo.offsets[e], fo.offsets[e + 1]))
+    np.testing.assert_allclose(fo.y64, np.einsum("nk,nkh->nh", fo.route.gates, fo.o), rtol=1e-14)
+
+
+def test_forward_with_permuted_slots_keeps_the_output_when_all_experts_are_chosen():
+    """k = E: every selection order is the same set, so y cannot change
+    (fp64 sums in another order: equal to 1e-12) while gates and expert
+    outputs move with their slots."""
+    inp, args, kw = _small_layer(43, E=4, k=4)
+    f0 = oracle.forward(*args, 4, **kw)
+    ids = f0.route.ids[:, ::-1].copy()
+    f1 = oracle.forward(*args, 4, **kw, ids=ids)
+    np.testing.assert_allclose(f1.y64, f0.y64, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(f1.route.gates, f0.route.gates[:, ::-1], rtol=1e-15)
+    assert np.array_equal(f1.o, f0.o[:, ::-1])
+
+
+# ----------------------------------------------------------- tensor-parallel split
+@pytest.mark.parametrize("weights", ["mxfp4", "fp8"])
+def test_tp_partials_add_up_to_the_layer(weights):
+    """Splitting the expert middle dimension over G shards and adding the
+    partial outputs gives the whole layer's fp64 output (G = 1: the same
+    operations, so bit for bit)."""
+    inp = synth.custom_inputs(5, 256, 4, 512, 2, seed=44, weights=weights)
+    c = inp.cfg
+    f = oracle.forward(inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, c.k, c.score_func,
+                       inp.logit_bias, inp.sel_bias, weight_format=weights)
+    (p1,) = oracle.tp_partials(f, inp.w2_q, inp.w2_s, 1, weights)
+    assert np.array_equal(p1, f.y64)
+    for G in (2, 4):
+        parts = oracle.tp_partials(f, inp.w2_q, inp.w2_s, G, weights)
+        assert len(parts) == G
+        np.testing.assert_allclose(sum(parts), f.y64, rtol=1e-12, atol=1e-14)
+        assert not np.allclose(parts[0], f.y64)          # each shard holds only part of the sum
+    with pytest.raises(AssertionError):
+        oracle.tp_partials(f, inp.w2_q, inp.w2_s, 3, weights)   # 512 / 3 is not a multiple of 128
