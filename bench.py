@@ -1,20 +1,28 @@
 """Benchmark of the routed MXFP4 / e4m3 MoE layer on B300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--windows R] [--config all|NAME]
+                    [--impl reference] [--weights mxfp4|fp8] [--act-scale e8m0|f32] [--peak-only]
 
 One step = one forward of the whole layer (router, top-k, dispatch with
 activation quantisation, gate/up grouped GEMM with SwiGLU and
 re-quantisation, down grouped GEMM, combine) over one batch of T synthetic
-tokens already resident in HBM.  Prints one JSON line.  Default workload:
-the Flash-shaped decode layer (T=64, H=4096, E=256 top-8, I=2048).
+tokens already resident in HBM.  Each workload is timed in R windows of K
+steps (CUDA events on the forward's stream, barrier + synchronize around
+each window); the median window gives ``ms_per_step``.  Prints one JSON
+line.  Default (``--config all``): the line is the largest single-GPU
+workload, the Pro-shaped prefill with skewed routing (T=16384, H=6144,
+E=384 top-8, I=2048); the other four workloads ride in its ``per_config``
+key, each with its own timing, roofline, stage times, routing statistics,
+end-to-end rate, CPU baseline and clocks.  The block-scaled tensor-core
+rate the prefill rooflines divide by is measured in the same run
+(``block_scaled_peak``).
 
 Under torchrun (N > 1) every rank runs an independent replica of the layer on
-its own GPU (the layer does not shard on one box): a barrier and a max over
-ranks bracket the timed region, and ``value`` is the tokens of all ranks
-divided by that time.
+its own GPU: a barrier and a max over ranks bracket the timed region, and
+``value`` is the tokens of all ranks divided by that time.
 
 ``--impl reference`` times the CPU oracle (fp64 restatement of the layer) on
-the host cores on a bounded sample of the same workload.
+the host cores on a bounded sample of the same workload (rank 0 only).
 """
 from __future__ import annotations
 
@@ -35,7 +43,8 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s and % of roofline (HBM GB/s decode, tensor TFLOP/s prefill) on 1 B300"
-DEFAULT_CONFIG = "flash-decode"
+HEADLINE = "pro-prefill-skew"      # the largest single-GPU workload
+ORDER = ["toy", "flash-decode", "pro-decode", "flash-prefill", "pro-prefill-skew"]
 
 
 def peaks():
@@ -207,24 +216,34 @@ def whole_job_rate(tokens_per_rank: int, seconds_max: float, world: int) -> floa
     return world * tokens_per_rank / seconds_max
 
 
-def oracle_sample(inp, budget_s=12.0, max_tokens=None, act_scale_mode=0):
-    """Time the CPU oracle token by token on the workload (routing of the
-    whole batch included in every call) until the time budget is spent."""
+def oracle_sample(inp, budget_s=12.0, act_scale_mode=0):
+    """Time the CPU oracle, as it stands, on a bounded sample of the workload:
+    oracle.forward routes every token of the batch and runs the expert FFNs
+    of the sampled tokens.  A first call on one token sizes a second call
+    whose sample fills the rest of the budget.  Returns (tokens, seconds,
+    description)."""
     import oracle
     c = inp.cfg
-    rng = np.random.default_rng(12345)
-    order = rng.permutation(c.T)
-    t0 = time.perf_counter()
-    done = 0
-    for t in order:
+    order = np.random.default_rng(12345).permutation(c.T)
+
+    def call(toks):
+        t0 = time.perf_counter()
         oracle.forward(inp.x, inp.router_w, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s, c.k, c.score_func,
-                       inp.logit_bias, inp.sel_bias, tokens=[int(t)], act_scale_mode=act_scale_mode,
+                       inp.logit_bias, inp.sel_bias, tokens=np.sort(toks), act_scale_mode=act_scale_mode,
                        weight_format=inp.weight_format)
-        done += 1
-        if time.perf_counter() - t0 >= budget_s or (max_tokens and done >= max_tokens):
-            break
-    el = time.perf_counter() - t0
-    return done, el
+        return time.perf_counter() - t0
+
+    el = call(order[:1])
+    done, calls = 1, 1
+    n = int(max(0.0, budget_s - el) / max(el, 1e-3))
+    if n >= 1:
+        n = min(n, c.T - 1)
+        el += call(order[1:1 + n])
+        done += n
+        calls += 1
+    desc = (f"{done} tokens of the {c.name} batch in {calls} oracle calls (each routes all {c.T} tokens in fp64, "
+            f"then runs the sampled tokens' {c.k} expert FFNs in fp64)")
+    return done, el, desc
 
 
 def cpu_cores():
@@ -236,61 +255,110 @@ def cpu_cores():
     return max(n, os.cpu_count() or 1)
 
 
-def run_reference(args, cfg):
+def config_dict(cfg, args):
+    """The workload a line measures (identical in both arms)."""
+    return dict(workload_desc(cfg), act_scale=args.act_scale, weights=args.weights)
+
+
+def headline_config(args):
+    import dataclasses
+    name = HEADLINE if args.config == "all" else args.config
+    cfg = synth.CONFIGS[name]
+    if args.experts:
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}-e{args.experts}", E=args.experts,
+                                  desc=cfg.desc + f" (reduced to {args.experts} experts)")
+    if args.tokens:
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}-t{args.tokens}", T=args.tokens,
+                                  desc=cfg.desc + f" (T overridden to {args.tokens})")
+    return cfg
+
+
+def run_reference(args):
     ws, rank, local = dist_env()
     if rank != 0:
         return 0
+    cfg = headline_config(args)
     inp = synth.make_inputs(cfg, weights=args.weights)
-    tokens = 0
-    elapsed = 0.0
+    mode = ACT_SCALES[args.act_scale]
+    per_step = args.ref_budget / max(args.steps, 1)
     for _ in range(args.warmup):
-        oracle_sample(inp, budget_s=args.ref_budget / max(args.steps, 1), max_tokens=1,
-                      act_scale_mode=ACT_SCALES[args.act_scale])
-    per = []
+        oracle_sample(inp, budget_s=0.0, act_scale_mode=mode)
+    tokens, elapsed, desc = 0, 0.0, ""
     for _ in range(args.steps):
-        n, el = oracle_sample(inp, budget_s=args.ref_budget / max(args.steps, 1),
-                              act_scale_mode=ACT_SCALES[args.act_scale])
+        n, el, desc = oracle_sample(inp, budget_s=per_step, act_scale_mode=mode)
         tokens += n
         elapsed += el
-        per.append(el)
     value = tokens / elapsed
-    cores = cpu_cores()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * elapsed / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(workload_desc(cfg), act_scale=args.act_scale, weights=args.weights),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{tokens} tokens of the {cfg.name} batch, one oracle call per token "
-                                   f"(routing of all {cfg.T} tokens + that token's {cfg.k} expert FFNs, fp64)"},
+        "config": config_dict(cfg, args),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"per step: {desc}; {tokens} tokens over {args.steps} steps"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def run_gpu(args, cfg):
+PEAK_STEPS = 8192   # 4 x 8192 MMAs per SM per probe launch (~2 ms)
+
+
+def burst_block_scaled_peak(device):
+    """The tensor-core rate of the instruction the grouped GEMMs issue
+    (moe_selftest_mma_peak: block-scaled e4m3 x E2M1, 128 x 256 x 32) as a
+    burst: the best of five ~2 ms launches on a rested GPU."""
+    import fp8_mxfp4_expert_bf16_b300 as moe
+    moe.mma_peak(device, 1024, 3)
+    bursts = [moe.mma_peak(device, PEAK_STEPS, 1) for _ in range(5)]
+    b = max(bursts, key=lambda r: r["tflops"])
+    return {"burst_tflops": b["tflops"], "burst_sm_mhz": b["sm_mhz"], "cycles_per_mma": b["cycles_per_mma"],
+            "burst_ms": b["ms"]}
+
+
+def sustained_block_scaled_peak(device, burst, seconds=3.0):
+    """The same instruction issued back to back for about ``seconds``: the
+    rate the chip holds under its power cap (the denominator for a kernel
+    timed inside a long run of steps)."""
+    import fp8_mxfp4_expert_bf16_b300 as moe
+    n = max(1, int(seconds * 1000.0 / max(burst["burst_ms"], 0.1)))
+    sus = moe.mma_peak(device, PEAK_STEPS, n)
+    return dict(burst, sustained_tflops=sus["tflops"], sustained_sm_mhz=sus["sm_mhz"], sustained_ms=sus["ms"],
+                how="moe_selftest_mma_peak: one CTA per SM issuing tcgen05.mma kind::mxf8f6f4.block_scale "
+                    "128x256x32 (e4m3 x e2m1, E8M0 scales) from shared memory with the GEMMs' elected issue loop; "
+                    f"burst = best of 5 launches of {4 * PEAK_STEPS} MMAs per SM before the workloads, sustained = "
+                    f"{n} such launches back to back after them; SM clock from the SMs' cycle counters")
+
+
+def expert_bytes(c, weights):
+    """Algorithmic bytes of one expert's gate/up and down weights (with scales)."""
+    if weights == "fp8":   # e4m3 bytes + a 4-byte scale per 128 x 128 block
+        return (2 * c.I * c.H + 4 * (2 * c.I // 128) * (c.H // 128), c.H * c.I + 4 * (c.H // 128) * (c.I // 128))
+    return (2 * c.I * c.H // 2 + 2 * c.I * c.H // 32, c.H * c.I // 2 + c.H * c.I // 32)
+
+
+L2_BYTES = 126 * 1024 * 1024
+
+
+def run_config(args, cfg, device, stream, P, peak, ws, rank, dist, cpu_budget):
+    """Time one workload; returns its result entry (rank 0) or None."""
     import torch
     import fp8_mxfp4_expert_bf16_b300 as moe
-
-    ws, rank, local = dist_env()
-    dist = ws > 1
     if dist:
         import torch.distributed as tdist
-        torch.cuda.set_device(local)
-        tdist.init_process_group("nccl")
-    device = local
-    torch.cuda.set_device(device)
-    inp = synth.make_inputs(cfg, weights=args.weights)
     c = cfg
     act_mode = ACT_SCALES[args.act_scale]
+    inp = synth.make_inputs(cfg, weights=args.weights)
     layer = moe.MoELayer(c.H, c.I, c.E, c.k, c.T, c.score_func, device=device, act_scale_mode=act_mode)
     load = layer.load_weights_fp8 if args.weights == "fp8" else layer.load_weights
     load(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
     x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).to(f"cuda:{device}")
     y = torch.empty_like(x)
-    stream = torch.cuda.Stream(device)
-    P = peaks()
+    eb13, eb2 = expert_bytes(c, args.weights)
+    # weights that fit in L2 would be re-read from it: flush L2 between steps then
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=f"cuda:{device}") \
+        if c.E * (eb13 + eb2) < 2 * L2_BYTES else None
 
     def barrier():
         torch.cuda.synchronize(device)
@@ -301,60 +369,60 @@ def run_gpu(args, cfg):
         for _ in range(max(args.warmup, 3)):
             layer.forward(x, y, stream)
     layer.check_device_error()
-
-    # routing statistics of this batch (for the algorithmic byte / flop counts)
     counts, _ = layer.expert_counts()
     active = int((counts > 0).sum())
     rows = int(counts.sum())
-    if args.weights == "fp8":   # e4m3 bytes + a 4-byte scale per 128 x 128 block
-        ebytes13 = 2 * c.I * c.H + 4 * (2 * c.I // 128) * (c.H // 128)
-        ebytes2 = c.H * c.I + 4 * (c.H // 128) * (c.I // 128)
-    else:                       # E2M1 nibbles + one E8M0 byte per 32
-        ebytes13 = 2 * c.I * c.H // 2 + 2 * c.I * c.H // 32
-        ebytes2 = c.H * c.I // 2 + c.H * c.I // 32
-    g1_bytes = active * ebytes13
-    g2_bytes = active * ebytes2
+    g1_bytes, g2_bytes = active * eb13, active * eb2
     g1_flops = 2.0 * rows * (2 * c.I) * c.H
     g2_flops = 2.0 * rows * c.H * c.I
     decode = rows <= 64 * max(active, 1)   # a few rows per expert: streaming the weights binds
 
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(device) as clk:
-        barrier()
-        clk.mark(True)
+    def timed_window(k):
+        """k forwards; device milliseconds (per-step events around each
+        forward when L2 is flushed between steps, else one pair)."""
+        if flush is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(k):
+                    layer.forward(x, y, stream)
+                e1.record(stream)
+            barrier()
+            return e0.elapsed_time(e1)
+        evs = []
         with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(args.steps):
+            for _ in range(k):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
                 layer.forward(x, y, stream)
-            ev1.record(stream)
+                e1.record(stream)
+                evs.append((e0, e1))
         barrier()
-        clk.mark(False)
-    ms_total = ev0.elapsed_time(ev1)
-    launches = layer.launch_count() * args.steps
-    layer.check_device_error()
+        return sum(a.elapsed_time(b) for a, b in evs)
 
-    # Kernel durations: the same K forwards once more, with the library's CUDA
-    # events recorded between the kernels on the forward's stream.  The events
-    # stop consecutive kernels from overlapping (programmatic dependent
-    # launch), so this window is timed separately from the one above.
-    ev2 = torch.cuda.Event(enable_timing=True)
-    ev3 = torch.cuda.Event(enable_timing=True)
+    windows = []
+    with ClockSampler(device) as clk:
+        for _ in range(args.windows):
+            barrier()
+            clk.mark(True)
+            windows.append(timed_window(args.steps))
+            clk.mark(False)
+    layer.check_device_error()
+    ms_med = statistics.median(windows)
+    ms_max = max_over_ranks(ms_med, f"cuda:{device}")
+    value = whole_job_rate(c.T * args.steps, ms_max / 1000.0, ws)
+    launches = layer.launch_count() * args.steps
+
+    # Kernel durations: K more forwards with the library's CUDA events between
+    # the kernels on the forward's stream.  Those events stop consecutive
+    # kernels from overlapping (programmatic dependent launch), so this
+    # window is timed apart from the ones above.
     layer.set_profiling(True)
-    barrier()
-    with torch.cuda.stream(stream):
-        ev2.record(stream)
-        for _ in range(args.steps):
-            layer.forward(x, y, stream)
-        ev3.record(stream)
-    barrier()
-    ms_profiled = ev2.elapsed_time(ev3) / args.steps
+    ms_profiled = timed_window(args.steps) / args.steps
     stage = layer.stage_times()       # averages over the last <= 64 forwards of that window
     layer.set_profiling(False)
     layer.check_device_error()
-
-    ms_max = max_over_ranks(ms_total, f"cuda:{device}")
-    value = whole_job_rate(c.T * args.steps, ms_max / 1000.0, ws)
 
     # end to end through the host-buffer entry point (pinned host memory)
     xh = torch.from_numpy(inp.x.view(np.int16)).pin_memory()
@@ -368,69 +436,203 @@ def run_gpu(args, cfg):
     el = time.perf_counter() - t0
     e2e_value = whole_job_rate(c.T * args.steps, max_over_ranks(el, f"cuda:{device}"), ws)
 
-    g1_ms = stage["gemm1_gate_up"]
-    g2_ms = stage["gemm2_down"]
-    if decode:
+    g1_ms, g2_ms = stage["gemm1_gate_up"], stage["gemm2_down"]
+    step_s = ms_max / args.steps / 1e3
+    clocks = clk.summary()
+    if flush is not None:
+        roof = {"bound": "none", "note": f"the {c.E} experts' weights ({c.E * (eb13 + eb2) / 1e6:.1f} MB) fit in L2: "
+                                        "a parity workload; L2 flushed between timed steps"}
+    elif decode:
         ach = g1_bytes / (g1_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": "k_mx_gemm<0> (gate/up grouped GEMM)", "achieved": ach,
                 "peak": P["hbm_gbs"], "unit": "GB/s", "frac": ach / P["hbm_gbs"],
-                "peak_source": f"{P['source']} HBM copy bandwidth",
-                "algorithmic_bytes_per_launch": g1_bytes,
-                "traffic": ncu_traffic(cfg.name, "gemm1"),
-                "down_gemm": {"achieved": g2_bytes / (g2_ms / 1e3) / 1e9, "bytes_per_launch": g2_bytes},
-                "layer_weight_gbs": (g1_bytes + g2_bytes) / (ms_max / args.steps / 1e3) / 1e9}
+                "peak_source": f"{P['source']} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": g1_bytes, "traffic": ncu_traffic(cfg.name, "gemm1"),
+                "down_gemm": {"achieved": g2_bytes / (g2_ms / 1e3) / 1e9, "bytes_per_launch": g2_bytes,
+                              "frac": g2_bytes / (g2_ms / 1e3) / 1e9 / P["hbm_gbs"]},
+                "layer_weight_gbs": (g1_bytes + g2_bytes) / step_s / 1e9,
+                "layer_frac": (g1_bytes + g2_bytes) / step_s / 1e9 / P["hbm_gbs"]}
     else:
-        pk = 2.0 * P["bf16_tflops"]
-        ach = g1_flops / (g1_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": "k_mx_gemm<0> (gate/up grouped GEMM)", "achieved": ach, "peak": pk,
-                "unit": "TFLOP/s", "frac": ach / pk,
-                "peak_source": f"{P['source']} bf16 burst x 2 (nominal fp8/bf16 ratio; block-scaled fp8 peak not measured)",
+        # the tensor rate is filled in once the sustained peak is measured
+        roof = {"bound": "tensor", "kernel": "k_mx_gemm<0> (gate/up grouped GEMM)",
+                "achieved": g1_flops / (g1_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "algorithmic_flops_per_launch": g1_flops, "traffic": ncu_traffic(cfg.name, "gemm1"),
                 "down_gemm": {"achieved": g2_flops / (g2_ms / 1e3) / 1e12},
-                "layer_tflops": (g1_flops + g2_flops) / (ms_max / args.steps / 1e3) / 1e12}
+                "layer_tflops": (g1_flops + g2_flops) / step_s / 1e12, "kernel_sm_mhz": clocks.get("sm_mhz")}
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        n, el = oracle_sample(inp, budget_s=args.ref_budget, act_scale_mode=act_mode)
-        cpu = {"value": n / el, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{n} tokens of the {cfg.name} batch, one oracle call per token "
-                         f"(routing of all {cfg.T} tokens + that token's {cfg.k} expert FFNs, fp64)"}
+    if rank == 0 and cpu_budget > 0:
+        n, el, desc = oracle_sample(inp, budget_s=cpu_budget, act_scale_mode=act_mode)
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle", "sample": desc}
+    entry = {
+        "value": value, "unit": "tokens/s", "ms_per_step": ms_max / args.steps,
+        "windows_ms_per_step": [w / args.steps for w in windows],
+        "config": config_dict(cfg, args),
+        "l2": ("weights fit in L2: L2 flushed (256 MB write) between timed steps" if flush is not None else
+               "inputs larger than L2: every step streams the active experts' weights from HBM"),
+        "roofline": roof, "stage_ms": stage,
+        "stage_window": {"ms_per_step": ms_profiled,
+                         "how": "a further window of K forwards with CUDA events between the kernels on the "
+                                "forward's stream (stage_ms and the roofline's kernel time come from it)"},
+        "routing": {"active_experts": active, "rows": rows, "max_count": int(counts.max()),
+                    "min_count": int(counts.min()), "cv": float(counts.std() / max(counts.mean(), 1e-9))},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": c.T * c.H * 2,
+                "d2h_bytes_per_step": c.T * c.H * 2},
+        "gpu_launches": launches * args.windows,
+        "clocks": clocks,
+    }
+    layer.close()
+    del x, y, flush, inp
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+    return entry if rank == 0 else None
+
+
+def run_tp(args):
+    """Tensor-parallel layer: rank r of the torchrun group holds shard r of
+    the expert middle dimension; one step = its fp32 partial forward, a sum
+    all-reduce over NCCL and one bf16 rounding (strong scaling: every rank
+    works on the same batch).  With --tp 1 the same path runs on one GPU."""
+    import torch
+    from fp8_mxfp4_expert_bf16_b300.tp import TensorParallelMoE, make_shard
+    ws, rank, local = dist_env()
+    if ws != args.tp:
+        raise SystemExit(f"--tp {args.tp} needs {args.tp} ranks (torchrun --nproc-per-node {args.tp}), got {ws}")
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+    cfg = headline_config(args)
+    c = cfg
+    inp = synth.make_inputs(cfg, weights=args.weights)
+    layer = make_shard(c.H, c.I, c.E, c.k, c.T, args.tp, rank, c.score_func, local, ACT_SCALES[args.act_scale])
+    load = layer.load_weights_fp8 if args.weights == "fp8" else layer.load_weights
+    load(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
+    tp = TensorParallelMoE(layer)
+    x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).cuda()
+    y = torch.empty_like(x)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            tdist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        tp.forward(x, y)
+    layer.check_device_error()
+    windows = []
+    with ClockSampler(local) as clk:
+        for _ in range(args.windows):
+            barrier()
+            clk.mark(True)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                tp.forward(x, y)
+            e1.record()
+            barrier()
+            clk.mark(False)
+            windows.append(e0.elapsed_time(e1))
+    layer.check_device_error()
+    ms = max_over_ranks(statistics.median(windows), f"cuda:{local}")
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e2m1 (fp32 accumulate)",
-            "data": "synthetic", "config": dict(workload_desc(cfg), act_scale=args.act_scale, weights=args.weights,
-                                               parallelism=f"replicas{ws}",
-                                               l2="inputs larger than L2: every step streams the active experts' "
-                                                  "weights from HBM"),
-            "roofline": roof,
-            "stage_ms": stage,
-            "stage_window": {"ms_per_step": ms_profiled,
-                             "how": "a second window of the same K forwards with CUDA events between the kernels "
-                                    "on the forward's stream (stage_ms and the roofline's kernel time come from it)"},
-            "routing": {"active_experts": active, "rows": rows, "max_count": int(counts.max()),
-                        "min_count": int(counts.min())},
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": c.T * c.H * 2,
-                    "d2h_bytes_per_step": c.T * c.H * 2},
-            "gpu_launches": launches,
-            "clocks": clk.summary(),
-        }
+        line = {"metric": METRIC, "value": c.T * args.steps / (ms / 1000.0), "unit": "tokens/s", "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+                "dtype": "e4m3 x e2m1 (fp32 accumulate)", "data": "synthetic",
+                "config": dict(config_dict(cfg, args), tp=args.tp), "parallelism": f"tp{args.tp}",
+                "windows_ms_per_step": [w / args.steps for w in windows],
+                "gpu_launches": (layer.launch_count() + 1) * args.steps * args.windows,
+                "clocks": clk.summary(),
+                "note": "tensor-parallel split of the expert middle dimension, one NCCL sum all-reduce per step"}
         print(json.dumps(line), flush=True)
-    if dist:
+    if ws > 1:
         tdist.barrier()
         tdist.destroy_process_group()
     layer.close()
     return 0
 
 
+def tensor_roofline(roof, peak, P):
+    """Fractions of a tensor-bound entry: against the sustained block-scaled
+    rate (the kernel is timed inside long runs of back-to-back steps), the
+    burst rate, the instruction's rate at the SM clock sampled while the
+    kernel ran (cycles per MMA x that clock), and twice the bf16 burst."""
+    ach, pk = roof["achieved"], peak["sustained_tflops"]
+    kclk = roof.pop("kernel_sm_mhz", None) or peak["sustained_sm_mhz"]
+    pk_clk = peak["burst_tflops"] * kclk / peak["burst_sm_mhz"]
+    roof.update(peak=pk, frac=ach / pk,
+                peak_source=(f"block-scaled e4m3 x e2m1 MMA rate measured in this run, sustained "
+                             f"({peak['sustained_sm_mhz']:.0f} MHz under the power cap; "
+                             f"{peak['cycles_per_mma']:.1f} cycles per 128x256x32 MMA)"),
+                frac_vs_burst_peak=ach / peak["burst_tflops"], burst_peak=peak["burst_tflops"],
+                frac_at_kernel_clock=ach / pk_clk, peak_at_kernel_clock=pk_clk, kernel_sm_mhz=kclk,
+                frac_vs_2x_bf16_burst=ach / (2.0 * P["bf16_tflops"]))
+    roof["down_gemm"]["frac"] = roof["down_gemm"]["achieved"] / pk
+    roof["layer_frac"] = roof["layer_tflops"] / pk
+    return roof
+
+
+def run_gpu(args):
+    import torch
+    ws, rank, local = dist_env()
+    dist = ws > 1
+    if dist:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+    device = local
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    P = peaks()
+    burst = burst_block_scaled_peak(device)
+    if args.peak_only:
+        peak = sustained_block_scaled_peak(device, burst, args.peak_seconds)
+        if rank == 0:
+            print(json.dumps({"block_scaled_peak": peak, "measured_peaks": P}), flush=True)
+        return 0
+    head = headline_config(args)
+    others = [n for n in ORDER if n != head.name] if args.config == "all" and not (args.experts or args.tokens) else []
+    # the headline workload first (the GPU as the burst probe left it), then the others
+    e = run_config(args, head, device, stream, P, None, ws, rank, dist,
+                   0 if args.no_cpu_baseline else args.ref_budget)
+    entries = {}
+    for name in others:
+        entries[name] = run_config(args, synth.CONFIGS[name], device, stream, P, None, ws, rank, dist,
+                                   0 if args.no_cpu_baseline else args.ref_budget / 4)
+    peak = sustained_block_scaled_peak(device, burst, args.peak_seconds)
+    if rank == 0:
+        for ent in [e] + list(entries.values()):
+            if ent["roofline"].get("bound") == "tensor":
+                tensor_roofline(ent["roofline"], peak, P)
+        line = {
+            "metric": METRIC, "value": e["value"], "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": e["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e2m1 (fp32 accumulate)",
+            "data": "synthetic", "config": e["config"], "parallelism": f"replicas{ws}",
+            "windows": args.windows, "windows_ms_per_step": e["windows_ms_per_step"], "l2": e["l2"],
+            "roofline": e["roofline"], "stage_ms": e["stage_ms"], "stage_window": e["stage_window"],
+            "routing": e["routing"], "cpu_baseline": e["cpu_baseline"], "e2e": e["e2e"],
+            "gpu_launches": e["gpu_launches"], "clocks": e["clocks"], "block_scaled_peak": peak,
+            "per_config": entries,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        tdist.barrier()
+        tdist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20, help="forwards per timed window")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--windows", type=int, default=5, help="timed windows per workload (the median is reported)")
+    ap.add_argument("--config", default="all", choices=["all"] + sorted(synth.CONFIGS),
+                    help="all: the headline workload plus the other four in per_config")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -438,22 +640,20 @@ def main():
                     help="expert format: MXFP4 (default) or e4m3 with an fp32 scale per 128 x 128 block")
     ap.add_argument("--act-scale", default="e8m0", choices=sorted(ACT_SCALES),
                     help="activation block scales: power-of-two E8M0 (default) or fp32 amax/448")
+    ap.add_argument("--peak-only", action="store_true", help="only measure the block-scaled tensor-core rate")
+    ap.add_argument("--peak-seconds", type=float, default=3.0, help="length of the sustained peak measurement")
+    ap.add_argument("--tp", type=int, default=0,
+                    help="tensor-parallel layer over the torchrun group (N ranks = N shards, NCCL all-reduce)")
     ap.add_argument("--experts", type=int, default=None,
                     help="shrink the workload to this many experts (small profiling captures only)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the batch size T (small profiling captures only)")
     args = ap.parse_args()
-    cfg = synth.CONFIGS[args.config]
-    import dataclasses
-    if args.experts:
-        cfg = dataclasses.replace(cfg, name=f"{cfg.name}-e{args.experts}", E=args.experts,
-                                  desc=cfg.desc + f" (reduced to {args.experts} experts)")
-    if args.tokens:
-        cfg = dataclasses.replace(cfg, name=f"{cfg.name}-t{args.tokens}", T=args.tokens,
-                                  desc=cfg.desc + f" (T overridden to {args.tokens})")
     if args.impl == "reference":
-        return run_reference(args, cfg)
-    return run_gpu(args, cfg)
+        return run_reference(args)
+    if args.tp:
+        return run_tp(args)
+    return run_gpu(args)
 
 
 if __name__ == "__main__":

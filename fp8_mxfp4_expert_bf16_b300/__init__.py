@@ -16,7 +16,8 @@ import numpy as np
 
 from .build import LIB as _LIB_PATH, build as _build
 
-__all__ = ["MoELayer", "MoEError", "lib", "declared_symbols", "STAGES", "route_noalloc", "mxfp4_quantize"]
+__all__ = ["MoELayer", "MoEError", "lib", "declared_symbols", "STAGES", "route_noalloc", "route_noalloc_check_error",
+           "mxfp4_quantize", "mma_peak", "sum_partials_bf16"]
 
 _HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_mx.h")
 
@@ -33,7 +34,8 @@ class MoEError(RuntimeError):
 class _Config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("num_experts", ctypes.c_int),
                 ("top_k", ctypes.c_int), ("max_tokens", ctypes.c_int), ("score_func", ctypes.c_int),
-                ("device", ctypes.c_int), ("act_scale_mode", ctypes.c_int)]
+                ("device", ctypes.c_int), ("act_scale_mode", ctypes.c_int), ("tp_size", ctypes.c_int),
+                ("tp_rank", ctypes.c_int)]
 
 
 ACT_SCALE_E8M0 = 0
@@ -67,6 +69,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_load_weights_fp8": (S, [P, P, P, P, P, P, P, P]),
         "moe_forward": (S, [P, P, I, P, P]),
         "moe_forward_host": (S, [P, P, I, P, P]),
+        "moe_forward_partial": (S, [P, P, I, P, P]),
+        "moe_sum_partials_bf16": (S, [ctypes.POINTER(P), I, ctypes.c_size_t, P, P]),
         "moe_get_logits": (S, [P, P]),
         "moe_get_routing": (S, [P, P, P]),
         "moe_get_expert_counts": (S, [P, P, P]),
@@ -86,6 +90,9 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_last_error": (ctypes.c_char_p, [P]),
         "moe_status_string": (ctypes.c_char_p, [I]),
         "moe_route_noalloc": (S, [P, I, I, P, P, P, I, I, I, P, P, P]),
+        "moe_route_noalloc_check_error": (S, [P]),
+        "moe_selftest_mma_peak": (S, [I, I, I, P]),
+        "moe_debug_fill_workspace": (S, [P, I]),
         "moe_mxfp4_quantize": (S, [P, ctypes.c_size_t, I, P, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -123,13 +130,17 @@ class MoELayer:
     """
 
     def __init__(self, hidden: int, inter: int, num_experts: int, top_k: int, max_tokens: int,
-                 score_func: int = 0, device: int = 0, act_scale_mode: int = ACT_SCALE_E8M0):
+                 score_func: int = 0, device: int = 0, act_scale_mode: int = ACT_SCALE_E8M0,
+                 tp_size: int = 1, tp_rank: int = 0):
         import torch  # noqa: F401  (device memory and streams)
         self.L = lib()
         self.H, self.I, self.E, self.k, self.max_tokens = hidden, inter, num_experts, top_k, max_tokens
+        self.tp_size, self.tp_rank = tp_size, tp_rank
+        self.I_loc = inter // max(tp_size, 1)       # this shard's slice of the expert middle dimension
         self.device = device
         self.act_scale_mode = act_scale_mode
-        cfg = _Config(hidden, inter, num_experts, top_k, max_tokens, score_func, device, act_scale_mode)
+        cfg = _Config(hidden, inter, num_experts, top_k, max_tokens, score_func, device, act_scale_mode, tp_size,
+                      tp_rank)
         h = ctypes.c_void_p()
         st = self.L.moe_init(ctypes.byref(cfg), ctypes.byref(h))
         if st != 0:
@@ -195,6 +206,19 @@ class MoELayer:
         self.last_T = T
         return y
 
+    def forward_partial(self, x, y32=None, stream=None):
+        """x: cuda bf16 [T, H] -> y32: cuda fp32 [T, H], the gate-weighted sum
+        before the bf16 rounding (a tensor-parallel shard's partial output)."""
+        import torch
+        assert x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.shape[1] == self.H
+        T = x.shape[0]
+        if y32 is None:
+            y32 = torch.empty((T, self.H), dtype=torch.float32, device=x.device)
+        assert y32.dtype == torch.float32 and tuple(y32.shape) == (T, self.H) and y32.is_contiguous()
+        self._check(self.L.moe_forward_partial(self.h, _ptr(x), T, _ptr(y32), self._stream(stream)))
+        self.last_T = T
+        return y32
+
     def forward_host(self, x_host, y_host=None, stream=None):
         """Host bf16 bits (numpy uint16 or a CPU tensor) in and out; copies and
         synchronisation happen inside the library call."""
@@ -219,6 +243,12 @@ class MoELayer:
 
     def launch_count(self) -> int:
         return self.L.moe_last_launch_count(self.h)
+
+    def debug_fill_workspace(self, byte: int):
+        """Fill every workspace buffer with ``byte`` (a forward must not read
+        anything it did not write)."""
+        self._check(self.L.moe_debug_fill_workspace(self.h, int(byte)))
+        self.last_T = None
 
     # ------------------------------------------------------------ getters
     def logits(self):
@@ -259,20 +289,20 @@ class MoELayer:
     def inter_quant(self):
         """Q2 codes and block scales (perm order), as act_quant."""
         n = self.last_T * self.k
-        q = np.empty((n, self.I), dtype=np.uint8)
+        q = np.empty((n, self.I_loc), dtype=np.uint8)
         if self.act_scale_mode == ACT_SCALE_F32:
-            s = np.empty((n, self.I // 128), dtype=np.float32)
+            s = np.empty((n, self.I_loc // 128), dtype=np.float32)
             self._check(self.L.moe_get_inter_quant(self.h, _ptr(q), None))
             self._check(self.L.moe_get_inter_scales_f32(self.h, _ptr(s)))
         else:
-            s = np.empty((n, self.I // 128), dtype=np.uint8)
+            s = np.empty((n, self.I_loc // 128), dtype=np.uint8)
             self._check(self.L.moe_get_inter_quant(self.h, _ptr(q), _ptr(s)))
         return q, s
 
     def block_scales_f32(self, which: str = "act"):
         """Every block scale of Q1 ('act') or Q2 ('inter') as a float32 value."""
         rows = self.last_T if which == "act" else self.last_T * self.k
-        width = self.H if which == "act" else self.I
+        width = self.H if which == "act" else self.I_loc
         s = np.empty((rows, width // 128), dtype=np.float32)
         f = self.L.moe_get_act_scales_f32 if which == "act" else self.L.moe_get_inter_scales_f32
         self._check(f(self.h, _ptr(s)))
@@ -286,22 +316,85 @@ class MoELayer:
 
 def route_noalloc(x, router_w, logit_bias, sel_bias, k, score_func=0, ids=None, gates=None, stream=None):
     """Router + top-k for callers that cannot allocate device memory on their
-    call path: all buffers are the caller's (cuda tensors), the logits
-    scratch is a fixed array inside the library (T * E <= 2^20).  Calls that
-    overlap on the GPU share that array and must be serialised."""
+    call path: all buffers are the caller's (contiguous cuda tensors on one
+    device: x, router_w bf16; biases fp32 or None; ids int32 [T, k], gates
+    fp32 [T, k]), the logits scratch is a fixed array inside the library
+    (T * E <= 2^20).  Calls that overlap on the GPU share that array and must
+    be serialised.  A kernel timeout is reported by route_noalloc_check_error."""
     import torch
     L = lib()
     T, H = x.shape
     E = router_w.shape[0]
+    dev = x.device
     if ids is None:
-        ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
     if gates is None:
-        gates = torch.empty((T, k), dtype=torch.float32, device=x.device)
-    st = L.moe_route_noalloc(_ptr(x), T, H, _ptr(router_w), _ptr(logit_bias), _ptr(sel_bias), E, k, score_func,
-                             _ptr(ids), _ptr(gates), MoELayer._stream(stream))
+        gates = torch.empty((T, k), dtype=torch.float32, device=dev)
+    for name, t, dt in [("x", x, torch.bfloat16), ("router_w", router_w, torch.bfloat16),
+                        ("logit_bias", logit_bias, torch.float32), ("sel_bias", sel_bias, torch.float32),
+                        ("ids", ids, torch.int32), ("gates", gates, torch.float32)]:
+        if t is None:
+            continue
+        if not t.is_cuda or t.device != dev:
+            raise ValueError(f"{name} must be a cuda tensor on {dev}")
+        if t.dtype != dt:
+            raise ValueError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if router_w.shape[1] != H or tuple(ids.shape) != (T, k) or tuple(gates.shape) != (T, k):
+        raise ValueError("shapes: x [T, H], router_w [E, H], ids and gates [T, k]")
+    for b in (logit_bias, sel_bias):
+        if b is not None and tuple(b.shape) != (E,):
+            raise ValueError("biases must be [E]")
+    with torch.cuda.device(dev):
+        st = L.moe_route_noalloc(_ptr(x), T, H, _ptr(router_w), _ptr(logit_bias), _ptr(sel_bias), E, k,
+                                 score_func, _ptr(ids), _ptr(gates), MoELayer._stream(stream))
     if st != 0:
         raise MoEError(st, L.moe_last_error(None).decode())
     return ids, gates
+
+
+def route_noalloc_check_error(device=None, stream=None):
+    """Wait for the stream and raise MoEError if a kernel wait of an earlier
+    route_noalloc call on the device gave up (the record is then cleared)."""
+    import torch
+    L = lib()
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        st = L.moe_route_noalloc_check_error(MoELayer._stream(stream))
+    if st != 0:
+        raise MoEError(st, L.moe_last_error(None).decode())
+
+
+def mma_peak(device=0, steps_per_cta=8192, launches=1):
+    """Block-scaled tensor-core throughput probe (see moe_selftest_mma_peak):
+    returns dict(tflops, sm_mhz, cycles_per_mma, ms)."""
+    L = lib()
+    out = np.zeros(4, dtype=np.float32)
+    st = L.moe_selftest_mma_peak(int(device), int(steps_per_cta), int(launches), _ptr(out))
+    if st != 0:
+        raise MoEError(st, L.moe_last_error(None).decode())
+    return {"tflops": float(out[0]), "sm_mhz": float(out[1]), "cycles_per_mma": float(out[2]), "ms": float(out[3])}
+
+
+def sum_partials_bf16(parts, y=None, stream=None):
+    """bf16(parts[0] + parts[1] + ...): fp32 cuda tensors of one shape, added
+    in list order in fp32 and rounded once (the tensor-parallel shards'
+    partial outputs, or one all-reduced sum)."""
+    import torch
+    L = lib()
+    p0 = parts[0]
+    for p in parts:
+        if not (p.is_cuda and p.dtype == torch.float32 and p.is_contiguous() and p.shape == p0.shape
+                and p.device == p0.device):
+            raise ValueError("partials must be contiguous fp32 cuda tensors of one shape on one device")
+    if y is None:
+        y = torch.empty(p0.shape, dtype=torch.bfloat16, device=p0.device)
+    arr = (ctypes.c_void_p * len(parts))(*[p.data_ptr() for p in parts])
+    with torch.cuda.device(p0.device):
+        st = L.moe_sum_partials_bf16(arr, len(parts), p0.numel(), _ptr(y), MoELayer._stream(stream))
+    if st != 0:
+        raise MoEError(st, L.moe_last_error(None).decode())
+    return y
 
 
 def mxfp4_quantize(w, stream=None):

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmoe_mx.so")
-SOURCES = ["route.cu", "router_gemm.cu", "mx_gemm.cu", "api.cu", "noalloc.cu", "quantize.cu"]
+SOURCES = ["route.cu", "router_gemm.cu", "mx_gemm.cu", "api.cu", "noalloc.cu", "quantize.cu", "selftest.cu"]
 HEADERS = ["ptx.cuh", "moe_internal.cuh"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

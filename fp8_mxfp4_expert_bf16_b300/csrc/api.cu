@@ -35,7 +35,9 @@ struct moe_handle {
     uint16_t* xbuf = nullptr;   // staging for moe_forward_host
     uint16_t* ybuf = nullptr;
     // owned weight buffers
-    void* w_alloc[7] = {};
+    void* w_alloc[8] = {};      // [7]: staging of whole tensors while a shard loads its slice
+    // tensor-parallel shard of the expert middle dimension (1 / 0: the whole layer)
+    int tp_size = 1, tp_rank = 0, I_full = 0;
     std::string err;
 };
 
@@ -43,6 +45,9 @@ static thread_local std::string g_err;
 
 // Set the message moe_last_error(NULL) returns (for entry points without a handle).
 void moe_set_handle_free_error(const char* msg) { g_err = msg; }
+
+// noalloc.cu: the error record of the allocation-free routing on the current device
+moe_status noalloc_error_record(int32_t** out);
 
 static moe_status fail(moe_handle* h, moe_status st, const char* fmt, ...)
 {
@@ -126,6 +131,37 @@ static moe_status with_tmp(moe_handle* h, size_t bytes, void* host_out, Fn&& fil
     return MOE_OK;
 }
 
+// Tensor-parallel shards keep a slice of the expert middle dimension I: rank
+// r of G holds middle columns [r Il, (r + 1) Il), Il = I / G, of every
+// expert.  The canonical tensors are first copied whole into `full` (device)
+// and the slice is then gathered into `dst`:
+//  * W13-like tensors [E][2 If][row bytes] (gate rows, then up rows): rows
+//    [r Il, (r+1) Il) of each half -> [E][2 Il][row bytes];
+//  * W2-like tensors [rows][If-dependent bytes]: the byte range
+//    [r * loc_bytes, (r + 1) * loc_bytes) of every row -> [rows][loc_bytes].
+// With G = 1 the tensor is copied as it is.
+static cudaError_t stage_w13(void* dst, const void* src, void* full, size_t E, size_t If, size_t Il, size_t r,
+                             size_t row_bytes)
+{
+    if (If == Il) return cudaMemcpy(dst, src, E * 2 * If * row_bytes, cudaMemcpyDefault);
+    cudaError_t e = cudaMemcpy(full, src, E * 2 * If * row_bytes, cudaMemcpyDefault);
+    for (size_t half = 0; half < 2 && e == cudaSuccess; ++half)
+        e = cudaMemcpy2D(static_cast<uint8_t*>(dst) + half * Il * row_bytes, 2 * Il * row_bytes,
+                         static_cast<const uint8_t*>(full) + (half * If + r * Il) * row_bytes, 2 * If * row_bytes,
+                         Il * row_bytes, E, cudaMemcpyDeviceToDevice);
+    return e;
+}
+
+static cudaError_t stage_w2(void* dst, const void* src, void* full, size_t rows, size_t full_bytes, size_t loc_bytes,
+                            size_t r)
+{
+    if (full_bytes == loc_bytes) return cudaMemcpy(dst, src, rows * full_bytes, cudaMemcpyDefault);
+    cudaError_t e = cudaMemcpy(full, src, rows * full_bytes, cudaMemcpyDefault);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2D(dst, loc_bytes, static_cast<const uint8_t*>(full) + r * loc_bytes, full_bytes, loc_bytes, rows,
+                         cudaMemcpyDeviceToDevice);
+    return e;
+}
 
 extern "C" {
 
@@ -184,6 +220,12 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
         return fail(nullptr, MOE_ERR_INVALID_ARG, "score_func=%d", c.score_func);
     if (c.act_scale_mode != MOE_ACT_SCALE_E8M0 && c.act_scale_mode != MOE_ACT_SCALE_F32)
         return fail(nullptr, MOE_ERR_INVALID_ARG, "act_scale_mode=%d", c.act_scale_mode);
+    const int G = c.tp_size == 0 ? 1 : c.tp_size;
+    if (G < 1 || G > kMaxTp || c.tp_rank < 0 || c.tp_rank >= G)
+        return fail(nullptr, MOE_ERR_INVALID_ARG, "tp_size=%d tp_rank=%d: need 1 <= tp_size <= %d, 0 <= tp_rank < tp_size",
+                    c.tp_size, c.tp_rank, kMaxTp);
+    if (c.inter % (128 * G))
+        return fail(nullptr, MOE_ERR_SHAPE, "inter=%d is not a multiple of 128 * tp_size=%d", c.inter, 128 * G);
     if (cudaSetDevice(c.device) != cudaSuccess)
         return fail(nullptr, MOE_ERR_CUDA, "cudaSetDevice(%d) failed", c.device);
     cudaDeviceProp prop;
@@ -196,9 +238,12 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
 
     moe_handle* h = new moe_handle;
     h->cfg = c;
+    h->tp_size = G;
+    h->tp_rank = c.tp_rank;
+    h->I_full = c.inter;
     DevState& s = h->s;
     s.H = c.hidden;
-    s.I = c.inter;
+    s.I = c.inter / G;   // this shard's slice of the expert middle dimension
     s.E = c.num_experts;
     s.K = c.top_k;
     s.Tm = c.max_tokens;
@@ -291,15 +336,20 @@ moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float
             cudaFree(p);
             p = nullptr;
         }
-    const size_t E = s.E, H = s.H, I = s.I;
+    const size_t E = s.E, H = s.H, I = s.I;   // I: this shard's middle width
+    const size_t If = h->I_full, r = h->tp_rank;
     const size_t n_wr = E * H * 2, n_13q = E * 2 * I * H / 2, n_13s = E * 2 * I * H / 32, n_2q = E * H * I / 2,
                  n_2s = E * H * I / 32;
     const int halves2 = s.BN2 / 128;
     const uint64_t rows13 = (uint64_t)E * s.NT1 * s.KB1 * 2 * kWBlockRowsPerHalf;
     const uint64_t rows2 = (uint64_t)E * s.NT2 * s.KB2 * halves2 * kWBlockRowsPerHalf;
-    void *d_wr, *d_b, *d_13, *d_2, *d_tmp;
+    void *d_wr, *d_b, *d_13, *d_2, *d_tmp, *d_full = nullptr;
     size_t n_tmp = n_13q;
     if (n_2q > n_tmp) n_tmp = n_2q;
+    if (If != I) {   // a shard: the canonical tensors are staged whole, then sliced
+        CUDA_TRY(h, cudaMalloc(&d_full, E * 2 * If * H / 2 > E * H * If / 2 ? E * 2 * If * H / 2 : E * H * If / 2));
+        h->w_alloc[7] = d_full;
+    }
     CUDA_TRY(h, cudaMalloc(&d_wr, n_wr));
     h->w_alloc[0] = d_wr;
     CUDA_TRY(h, cudaMalloc(&d_b, 2 * E * sizeof(float)));
@@ -317,23 +367,24 @@ moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float
     CUDA_TRY(h, cudaMemset(d_b, 0, 2 * E * sizeof(float)));
     if (logit_bias) CUDA_TRY(h, cudaMemcpy(d_lb, logit_bias, E * sizeof(float), cudaMemcpyDefault));
     if (sel_bias) CUDA_TRY(h, cudaMemcpy(d_cb, sel_bias, E * sizeof(float), cudaMemcpyDefault));
-    // expert values: canonical [E][R][K/2] -> interleaved tile-major blocks (one contiguous run per GEMM stage)
-    CUDA_TRY(h, cudaMemcpy(tmp, w13_q, n_13q, cudaMemcpyDefault));
+    // expert values: canonical [E][R][K/2] (this shard's slice) -> interleaved
+    // tile-major blocks (one contiguous run per GEMM stage)
+    CUDA_TRY(h, stage_w13(tmp, w13_q, d_full, E, If, I, r, H / 2));
     CUDA_TRY(h, launch_repack_w(tmp, static_cast<uint8_t*>(d_13), s.E, s.KB1, s.NT1, 2, 2 * s.I, 0, s.I / 128, 0));
     CUDA_TRY(h, cudaDeviceSynchronize());
-    CUDA_TRY(h, cudaMemcpy(tmp, w2_q, n_2q, cudaMemcpyDefault));
+    CUDA_TRY(h, stage_w2(tmp, w2_q, d_full, E * H, If / 2, I / 2, r));
     CUDA_TRY(h, launch_repack_w(tmp, static_cast<uint8_t*>(d_2), s.E, s.KB2, s.NT2, halves2, s.H, 1, s.I / 128, 0));
     CUDA_TRY(h, cudaDeviceSynchronize());
 
     int32_t* flag = s.err + 3;
     CUDA_TRY(h, cudaMemset(flag, 0, sizeof(int32_t)));
     // scales: canonical [E][R][K/32] -> the scale rows of the same blocks
-    CUDA_TRY(h, cudaMemcpy(tmp, w13_s, n_13s, cudaMemcpyDefault));
+    CUDA_TRY(h, stage_w13(tmp, w13_s, d_full, E, If, I, r, H / 32));
     CUDA_TRY(h, launch_check_e8m0(tmp, n_13s, flag, 0));
     CUDA_TRY(h, launch_repack_sf(tmp, static_cast<uint8_t*>(d_13), s.E, s.KB1, s.NT1, 2, 2 * s.I, s.H / 32, 0,
                                  s.I / 128, 0));
     CUDA_TRY(h, cudaDeviceSynchronize());
-    CUDA_TRY(h, cudaMemcpy(tmp, w2_s, n_2s, cudaMemcpyDefault));
+    CUDA_TRY(h, stage_w2(tmp, w2_s, d_full, E * H, If / 32, I / 32, r));
     CUDA_TRY(h, launch_check_e8m0(tmp, n_2s, flag, 0));
     CUDA_TRY(h, launch_repack_sf(tmp, static_cast<uint8_t*>(d_2), s.E, s.KB2, s.NT2, halves2, s.H, s.I / 32, 1,
                                  s.I / 128, 0));
@@ -342,6 +393,10 @@ moe_status moe_load_weights(moe_handle* h, const uint16_t* router_w, const float
     CUDA_TRY(h, cudaMemcpy(&nan_found, flag, sizeof(int32_t), cudaMemcpyDeviceToHost));
     cudaFree(d_tmp);
     h->w_alloc[6] = nullptr;
+    if (d_full) {
+        cudaFree(d_full);
+        h->w_alloc[7] = nullptr;
+    }
     if (nan_found) {
         CUDA_TRY(h, cudaMemset(flag, 0, sizeof(int32_t)));
         return fail(h, MOE_ERR_INVALID_ARG, "moe_load_weights: an expert scale byte is 0xFF (E8M0 NaN)");
@@ -379,7 +434,8 @@ moe_status moe_load_weights_fp8(moe_handle* h, const uint16_t* router_w, const f
             cudaFree(p);
             p = nullptr;
         }
-    const size_t E = s.E, H = s.H, I = s.I;
+    const size_t E = s.E, H = s.H, I = s.I;   // I: this shard's middle width
+    const size_t If = h->I_full, r = h->tp_rank;
     const size_t n_wr = E * H * 2, n_13 = E * 2 * I * H, n_2 = E * H * I;
     const size_t n_13s = E * (2 * I / 128) * (H / 128), n_2s = E * (H / 128) * (I / 128);
     const int halves2 = s.BN2 / 128;
@@ -401,6 +457,11 @@ moe_status moe_load_weights_fp8(moe_handle* h, const uint16_t* router_w, const f
     h->w_alloc[5] = d_s2;
     CUDA_TRY(h, cudaMalloc(&d_tmp, (n_13 > n_2 ? n_13 : n_2) + 256));
     h->w_alloc[6] = d_tmp;
+    void* d_full = nullptr;
+    if (If != I) {   // a shard: the canonical tensors are staged whole, then sliced
+        CUDA_TRY(h, cudaMalloc(&d_full, E * 2 * If * H));
+        h->w_alloc[7] = d_full;
+    }
     float* d_lb = static_cast<float*>(d_b);
     float* d_cb = d_lb + E;
     uint8_t* tmp = static_cast<uint8_t*>(d_tmp);
@@ -410,22 +471,25 @@ moe_status moe_load_weights_fp8(moe_handle* h, const uint16_t* router_w, const f
     if (sel_bias) CUDA_TRY(h, cudaMemcpy(d_cb, sel_bias, E * sizeof(float), cudaMemcpyDefault));
     int32_t* flag = s.err + 3;
     CUDA_TRY(h, cudaMemset(flag, 0, sizeof(int32_t)));
-    CUDA_TRY(h, cudaMemcpy(tmp, w13, n_13, cudaMemcpyDefault));
+    CUDA_TRY(h, stage_w13(tmp, w13, d_full, E, If, I, r, H));
     CUDA_TRY(h, launch_check_fp8(tmp, n_13, nullptr, 0, flag, 0));
     CUDA_TRY(h, launch_repack_w8(tmp, static_cast<uint8_t*>(d_13), s.E, s.KB1, s.NT1, 2, 2 * s.I, 0, s.I / 128, 0));
     CUDA_TRY(h, cudaDeviceSynchronize());
-    CUDA_TRY(h, cudaMemcpy(tmp, w2, n_2, cudaMemcpyDefault));
+    CUDA_TRY(h, stage_w2(tmp, w2, d_full, E * H, If, I, r));
     CUDA_TRY(h, launch_check_fp8(tmp, n_2, nullptr, 0, flag, 0));
     CUDA_TRY(h, launch_repack_w8(tmp, static_cast<uint8_t*>(d_2), s.E, s.KB2, s.NT2, halves2, s.H, 1, s.I / 128, 0));
     CUDA_TRY(h, cudaDeviceSynchronize());
-    CUDA_TRY(h, cudaMemcpy(d_s13, w13_scale, n_13s * sizeof(float), cudaMemcpyDefault));
-    CUDA_TRY(h, cudaMemcpy(d_s2, w2_scale, n_2s * sizeof(float), cudaMemcpyDefault));
+    // block scales: [E][2I/128][H/128] (gate block rows, then up) and [E][H/128][I/128]
+    CUDA_TRY(h, stage_w13(d_s13, w13_scale, d_full, E, If / 128, I / 128, r, 4 * (H / 128)));
+    CUDA_TRY(h, stage_w2(d_s2, w2_scale, d_full, E * (H / 128), 4 * (If / 128), 4 * (I / 128), r));
     CUDA_TRY(h, launch_check_fp8(nullptr, 0, static_cast<const float*>(d_s13), n_13s, flag, 0));
     CUDA_TRY(h, launch_check_fp8(nullptr, 0, static_cast<const float*>(d_s2), n_2s, flag, 0));
     int32_t bad = 0;
     CUDA_TRY(h, cudaMemcpy(&bad, flag, sizeof(int32_t), cudaMemcpyDeviceToHost));
     cudaFree(d_tmp);
     h->w_alloc[6] = nullptr;
+    cudaFree(d_full);
+    h->w_alloc[7] = nullptr;
     if (bad) {
         CUDA_TRY(h, cudaMemset(flag, 0, sizeof(int32_t)));
         return fail(h, MOE_ERR_INVALID_ARG,
@@ -463,19 +527,20 @@ moe_status moe_set_profiling(moe_handle* h, int enable)
     return MOE_OK;
 }
 
-moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, void* stream)
+// The forward of moe_forward (y bf16) and moe_forward_partial (y fp32, not rounded).
+static moe_status forward_impl(moe_handle* h, const uint16_t* x, int T, void* y, bool f32_out, void* stream,
+                               const char* who)
 {
-    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_forward: handle is NULL");
-    if (!h->loaded) return fail(h, MOE_ERR_NOT_LOADED, "moe_forward: weights not loaded");
-    if (T < 0 || T > h->s.Tm)
-        return fail(h, MOE_ERR_SHAPE, "moe_forward: T=%d outside [0, max_tokens=%d]", T, h->s.Tm);
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "%s: handle is NULL", who);
+    if (!h->loaded) return fail(h, MOE_ERR_NOT_LOADED, "%s: weights not loaded", who);
+    if (T < 0 || T > h->s.Tm) return fail(h, MOE_ERR_SHAPE, "%s: T=%d outside [0, max_tokens=%d]", who, T, h->s.Tm);
     if (T == 0) return MOE_OK;
-    if (!x || !y) return fail(h, MOE_ERR_INVALID_ARG, "moe_forward: x or y is NULL");
+    if (!x || !y) return fail(h, MOE_ERR_INVALID_ARG, "%s: x or y is NULL", who);
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u)
-        return fail(h, MOE_ERR_INVALID_ARG, "moe_forward: x and y must be 16-byte aligned");
-    const size_t bytes = (size_t)T * h->s.H * 2;
+        return fail(h, MOE_ERR_INVALID_ARG, "%s: x and y must be 16-byte aligned", who);
+    const size_t xbytes = (size_t)T * h->s.H * 2, ybytes = (size_t)T * h->s.H * (f32_out ? 4 : 2);
     const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
-    if (xa < ya + bytes && ya < xa + bytes) return fail(h, MOE_ERR_INVALID_ARG, "moe_forward: x and y overlap");
+    if (xa < ya + ybytes && ya < xa + xbytes) return fail(h, MOE_ERR_INVALID_ARG, "%s: x and y overlap", who);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const DevState& s = h->s;
     CUDA_TRY(h, cudaSetDevice(h->cfg.device));
@@ -485,7 +550,7 @@ moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, voi
     CUtensorMap tmX;
     if (!make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t*>(x), s.H, (uint64_t)T, (uint64_t)s.H * 2,
                   64, 128))
-        return fail(h, MOE_ERR_CUDA, "moe_forward: cuTensorMapEncodeTiled failed for x");
+        return fail(h, MOE_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed for x", who);
     const int ksplit = router_split(T, s.H);
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[0], st));
     CUDA_TRY(h, launch_router_tc(s, tmX, T, st, ksplit));
@@ -509,12 +574,36 @@ moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, voi
     CUDA_TRY(h, launch_gemm2(s, st));
     ++n;
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[5], st));
-    CUDA_TRY(h, launch_combine(s, y, T, st));
+    CUDA_TRY(h, f32_out ? launch_combine_f32(s, static_cast<float*>(y), T, st)
+                        : launch_combine(s, static_cast<uint16_t*>(y), T, st));
     ++n;
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[6], st));
     h->last_T = T;
     h->last_launches = n;
     if (prof) ++h->prof_count;
+    return MOE_OK;
+}
+
+moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, void* stream)
+{
+    return forward_impl(h, x, T, y, false, stream, "moe_forward");
+}
+
+moe_status moe_forward_partial(moe_handle* h, const uint16_t* x, int T, float* y32, void* stream)
+{
+    return forward_impl(h, x, T, y32, true, stream, "moe_forward_partial");
+}
+
+moe_status moe_sum_partials_bf16(const float* const* parts, int n_parts, size_t n, uint16_t* y, void* stream)
+{
+    if (!parts || !y || n_parts < 1 || n_parts > kMaxTp)
+        return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_sum_partials_bf16: need 1..%d partials and an output", kMaxTp);
+    for (int i = 0; i < n_parts; ++i)
+        if (!parts[i]) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_sum_partials_bf16: partial %d is NULL", i);
+    if (n == 0) return MOE_OK;
+    cudaError_t e = launch_sum_partials(parts, n_parts, n, y, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return fail(nullptr, MOE_ERR_CUDA, "moe_sum_partials_bf16: %s", cudaGetErrorString(e));
     return MOE_OK;
 }
 
@@ -538,6 +627,31 @@ moe_status moe_forward_host(moe_handle* h, const uint16_t* x_host, int T, uint16
 }
 
 int moe_last_launch_count(moe_handle* h) { return h ? h->last_launches : 0; }
+
+moe_status moe_debug_fill_workspace(moe_handle* h, int byte)
+{
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_debug_fill_workspace: handle is NULL");
+    if (byte < 0 || byte > 255) return fail(h, MOE_ERR_INVALID_ARG, "moe_debug_fill_workspace: byte=%d", byte);
+    DevState& s = h->s;
+    CUDA_TRY(h, cudaSetDevice(h->cfg.device));
+    CUDA_TRY(h, cudaDeviceSynchronize());
+    const size_t Tm = s.Tm, E = s.E, K = s.K, R = s.Rmax, MT = s.MTmax;
+    const size_t Ts = Tm < (size_t)kRouterSplitMaxT ? Tm : (size_t)kRouterSplitMaxT;
+    struct Buf { void* p; size_t n; } bufs[] = {
+        {s.logits, 4 * Tm * E}, {s.logit_part, 4 * kRouterMaxSplit * Ts * E}, {s.ids, 4 * Tm * K},
+        {s.gates, 4 * Tm * K}, {s.chunk_hist, 4 * (size_t)s.nchunk_max * E},
+        {s.chunk_base, 4 * (size_t)s.nchunk_max * E}, {s.counts, 4 * E}, {s.offsets, 4 * (E + 1)},
+        {s.mtile_off, 4 * (E + 1)}, {s.mtile_expert, 4 * MT}, {s.mtile_rows, 4 * MT}, {s.n_mtiles, 4 * 4},
+        {s.light_list, 4 * MT}, {s.heavy_list, 4 * MT}, {s.prow, 4 * Tm * K}, {s.aq, R * s.H},
+        {s.asf, 4 * MT * s.KB1 * 128}, {s.hq, R * s.I}, {s.hsf, 4 * MT * s.KB2 * 128},
+        {s.asf32, s.act_f32 ? 4 * R * s.KB1 : 0}, {s.hsf32, s.act_f32 ? 4 * R * s.KB2 : 0},
+        {s.obuf, 4 * R * s.H}, {h->xbuf, 2 * Tm * s.H}, {h->ybuf, 2 * Tm * s.H}};
+    for (const Buf& b : bufs)
+        if (b.p && b.n) CUDA_TRY(h, cudaMemset(b.p, byte, b.n));
+    CUDA_TRY(h, cudaDeviceSynchronize());
+    h->last_T = -1;
+    return MOE_OK;
+}
 
 }   // extern "C"
 
@@ -568,11 +682,17 @@ extern "C" {
 
 moe_status moe_selftest_wait_timeout(moe_handle* h, unsigned int limit_us)
 {
-    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_selftest_wait_timeout: handle is NULL");
     if (limit_us < 1 || limit_us > 1000000)
         return fail(h, MOE_ERR_INVALID_ARG, "moe_selftest_wait_timeout: limit_us=%u outside [1, 10^6]", limit_us);
-    CUDA_TRY(h, cudaSetDevice(h->cfg.device));
-    moe::k_wait_probe<<<1, 32>>>(h->s.err, (uint64_t)limit_us * 1000ull);
+    int32_t* err = nullptr;
+    if (h) {
+        CUDA_TRY(h, cudaSetDevice(h->cfg.device));
+        err = h->s.err;
+    } else {
+        moe_status st = noalloc_error_record(&err);   // the allocation-free routing's error record
+        if (st != MOE_OK) return st;
+    }
+    moe::k_wait_probe<<<1, 32>>>(err, (uint64_t)limit_us * 1000ull);
     CUDA_TRY(h, cudaGetLastError());
     return MOE_OK;
 }

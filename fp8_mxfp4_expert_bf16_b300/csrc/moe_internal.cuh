@@ -16,6 +16,7 @@ constexpr int kWBlockRowsPerHalf = 136;   // interleaved weight block: 128 weigh
 constexpr int kRouterMaxSplit = 16;       // split-K factor of the router for small batches
 constexpr int kRouterSplitMaxT = 512;     // batches up to this size use the split-K router
 constexpr int kLightRows = 16;      // m-tiles with at most this many rows use the light GEMM shape
+constexpr int kMaxTp = 8;           // tensor-parallel shards of the expert middle dimension
 
 // Error word codes written by kernels (first writer wins).
 constexpr int kDevErrTimeout = 1;
@@ -111,6 +112,8 @@ cudaError_t launch_dispatch_small(const DevState& s, int T, cudaStream_t st);
 cudaError_t launch_quant_scatter(const DevState& s, const uint16_t* x, int T, cudaStream_t st);
 cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStream_t st, int* nlaunch);
 cudaError_t launch_combine(const DevState& s, uint16_t* y, int T, cudaStream_t st);
+cudaError_t launch_combine_f32(const DevState& s, float* y32, int T, cudaStream_t st);
+cudaError_t launch_sum_partials(const float* const* parts, int n_parts, size_t n, uint16_t* y, cudaStream_t st);
 // load-time helpers (route.cu)
 cudaError_t launch_repack_sf(const uint8_t* src, uint8_t* dst, int E, int KB, int NT, int halves, int rows_total,
                              int K32, int mode, int I128, cudaStream_t st);

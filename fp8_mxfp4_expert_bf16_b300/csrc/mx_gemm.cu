@@ -89,6 +89,12 @@ constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), 
 constexpr uint32_t kSFUnitCol = 352; // promotion modes: a constant unit scale chunk, twice (8 cols)
 constexpr uint32_t kStashHeavyCol = 320;  // down epilogue, heavy phase: 3 x 32 columns per warp parked here
 constexpr uint32_t kStashCol = 384;  // gate/up epilogue: the tile's up columns parked here (128 cols)
+// The two stashes are used only by the epilogues of the E8M0 (non-promotion)
+// instantiations; the unit chunk at kSFUnitCol, inside the heavy stash's
+// range, only by the promotion ones (the epilogue code paths that park
+// columns assert this where they are compiled).
+static_assert(kSFUnitCol + 8 <= kStashCol, "unit scale chunk overlaps the gate/up stash");
+static_assert(kSFUnitCol >= kSFCol + 16 * Shape<true>::kStages, "unit scale chunk overlaps the light ring's scales");
 static_assert(kSFCol + 16 * Shape<false>::kStages <= kStashHeavyCol && kStashHeavyCol + 2 * 96 <= kTmemCols,
               "heavy-phase down stash overlaps the heavy ring's scale chunks");
 static_assert(kSFCol + 16 * Shape<true>::kStages <= kStashCol && kStashCol + 128 <= kTmemCols,
@@ -700,6 +706,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
             const bool warp_live = q * 32 < rows;
             const bool row_live = row < rows;
             if (kMode == 0) {
+                static_assert(!(kF32S || kW8), "the gate/up stash is for the E8M0 epilogue only");
                 // this warp: middle columns [64 hw, 64 hw + 64) of the tile's 128
                 float h[64];
                 const uint32_t stash = tl + kStashCol + 64u * hw;
@@ -767,6 +774,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         args.hsf[sf_word_index(mt, nt, args.I / 128, row)] = (uint32_t)(ex + 127) * 0x01010101u;
                 }
             } else {
+                static_assert(!(kF32S || kW8), "the heavy down stash overlaps the promotion modes' unit scales");
                 // this warp: output columns [hw * ncols / 2, (hw + 1) * ncols / 2).  The
                 // whole slice is read into registers first and the accumulator released,
                 // so the next tile's MMAs run while the rows are stored.

@@ -149,9 +149,11 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int H, const u
     if (st != MOE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    // the zero bias vectors and the error record must start at zero; the
-    // logits are fully overwritten by the router before top-k reads them
-    cudaError_t e = cudaMemsetAsync(scratch + kNoAllocZeroOff, 0, (kNoAllocWords - kNoAllocZeroOff) * sizeof(float), s);
+    // the zero bias vectors must be zero (nothing writes them; cleared anyway);
+    // the logits are fully overwritten by the router before top-k reads them.
+    // The error record is left alone: a timeout of an earlier call stays
+    // recorded until moe_route_noalloc_check_error reads and clears it.
+    cudaError_t e = cudaMemsetAsync(scratch + kNoAllocZeroOff, 0, 2 * kMaxExperts * sizeof(float), s);
 
     DevState ds{};
     ds.pdl = false;   // plain stream order, as for any other library call on the caller's stream
@@ -180,4 +182,46 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int H, const u
         return MOE_ERR_CUDA;
     }
     return MOE_OK;
+}
+
+// The error record of the scratch on the current device (for the library's
+// wait-timeout self-test, which can target it instead of a handle's).
+moe_status noalloc_error_record(int32_t** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        set_error("no current CUDA device");
+        return MOE_ERR_CUDA;
+    }
+    float* scratch = nullptr;
+    moe_status st = setup_device(dev, &scratch);
+    if (st == MOE_OK) *out = reinterpret_cast<int32_t*>(scratch + kNoAllocErrOff);
+    return st;
+}
+
+extern "C" moe_status moe_route_noalloc_check_error(void* stream)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        set_error("moe_route_noalloc_check_error: no current CUDA device");
+        return MOE_ERR_CUDA;
+    }
+    char buf[256];
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    int32_t w[3] = {0, 0, 0};
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(w, g_noalloc_scratch, sizeof w, kNoAllocErrOff * sizeof(float));
+    if (e == cudaSuccess && w[0] != 0) {
+        const int32_t zero[3] = {0, 0, 0};
+        e = cudaMemcpyToSymbol(g_noalloc_scratch, zero, sizeof zero, kNoAllocErrOff * sizeof(float));
+    }
+    if (e != cudaSuccess) {
+        snprintf(buf, sizeof buf, "moe_route_noalloc_check_error: %s", cudaGetErrorString(e));
+        set_error(buf);
+        return MOE_ERR_CUDA;
+    }
+    if (w[0] == 0) return MOE_OK;
+    snprintf(buf, sizeof buf, "moe_route_noalloc: a kernel wait %s (site %d, block %d)",
+             w[0] == kDevErrTimeout ? "timed out" : "reported an error", w[1], w[2]);
+    set_error(buf);
+    return w[0] == kDevErrTimeout ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE;
 }

@@ -546,11 +546,13 @@ cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStr
 // y[t] = bf16_rne( sum_j gate[t][j] * o[row(t, j)] ), fp32 fused multiply-adds
 // in slot order.  Block (t, c): 1024 columns of token t, one float4 per
 // thread; the k expert-output loads are all issued before the additions.
+// With kF32Out the fp32 sum is stored unrounded (a tensor-parallel shard's
+// partial output, rounded once after the partials are added up).
 constexpr int kCombineCols = 1024;
 
+template <bool kF32Out>
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ obuf, const int32_t* __restrict__ prow,
-                                                 const float* __restrict__ gates, uint16_t* __restrict__ y, int H,
-                                                 int K)
+                                                 const float* __restrict__ gates, void* __restrict__ y, int H, int K)
 {
     griddep_wait();
     griddep_launch_dependents();
@@ -578,19 +580,55 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ obuf,
             acc.w = fmaf(g[j], o[j].w, acc.w);
         }
     }
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 out;
-    out.x = *reinterpret_cast<const uint32_t*>(&lo);
-    out.y = *reinterpret_cast<const uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(y + (size_t)t * H)[h4] = out;
+    if constexpr (kF32Out) {
+        reinterpret_cast<float4*>(static_cast<float*>(y) + (size_t)t * H)[h4] = acc;
+    } else {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 out;
+        out.x = *reinterpret_cast<const uint32_t*>(&lo);
+        out.y = *reinterpret_cast<const uint32_t*>(&hi);
+        reinterpret_cast<uint2*>(static_cast<uint16_t*>(y) + (size_t)t * H)[h4] = out;
+    }
 }
 
 cudaError_t launch_combine(const DevState& s, uint16_t* y, int T, cudaStream_t st)
 {
     const dim3 grid(T, (s.H + kCombineCols - 1) / kCombineCols);
-    return launch_kernel(k_combine, grid, dim3(256), 0, st, s.pdl, (const float*)s.obuf, (const int32_t*)s.prow,
-                         (const float*)s.gates, y, s.H, s.K);
+    return launch_kernel(k_combine<false>, grid, dim3(256), 0, st, s.pdl, (const float*)s.obuf, (const int32_t*)s.prow,
+                         (const float*)s.gates, (void*)y, s.H, s.K);
+}
+
+cudaError_t launch_combine_f32(const DevState& s, float* y32, int T, cudaStream_t st)
+{
+    const dim3 grid(T, (s.H + kCombineCols - 1) / kCombineCols);
+    return launch_kernel(k_combine<true>, grid, dim3(256), 0, st, s.pdl, (const float*)s.obuf, (const int32_t*)s.prow,
+                         (const float*)s.gates, (void*)y32, s.H, s.K);
+}
+
+// The tensor-parallel shards' partial outputs added up in shard order (fp32)
+// and rounded once to bf16: y[i] = bf16_rne(p0[i] + p1[i] + ...).
+struct Partials {
+    const float* p[kMaxTp];
+};
+
+__global__ void __launch_bounds__(256) k_sum_partials(Partials parts, int n_parts, size_t n, uint16_t* __restrict__ y)
+{
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        float v = parts.p[0][i];
+        for (int r = 1; r < n_parts; ++r) v += parts.p[r][i];
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        y[i] = *reinterpret_cast<const uint16_t*>(&b);
+    }
+}
+
+cudaError_t launch_sum_partials(const float* const* parts, int n_parts, size_t n, uint16_t* y, cudaStream_t st)
+{
+    Partials p{};
+    for (int r = 0; r < n_parts; ++r) p.p[r] = parts[r];
+    const size_t blocks = (n + 255) / 256;
+    k_sum_partials<<<(unsigned)(blocks < 4736 ? blocks : 4736), 256, 0, st>>>(p, n_parts, n, y);
+    return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ load time

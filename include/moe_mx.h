@@ -89,6 +89,19 @@ typedef struct {
     int score_func;   /* MOE_SCORE_SIGMOID (the pages' router) or MOE_SCORE_SOFTMAX */
     int device;       /* CUDA device ordinal; the device must be sm_103 */
     int act_scale_mode; /* MOE_ACT_SCALE_E8M0 (0, default) or MOE_ACT_SCALE_F32 */
+    /* Tensor-parallel shard of the expert middle dimension (the pages' TP8 /
+     * TP4 deployments: vLLM recipe "XiaomiMiMo/MiMo-V2.6-Pro-RL", "Overview"
+     * hardware line and the TP8 (H200) / TP4 (MI355X) launch recipes).
+     * tp_size G in 1..8 (0 means 1), 0 <= tp_rank < G, inter a multiple of
+     * 128 * G.  Shard r keeps, for every expert, gate and up rows
+     * [r I/G, (r+1) I/G) of W13 and the same columns of W2, so its SwiGLU
+     * blocks of 128 are exactly the whole layer's; routing, dispatch and the
+     * input quantisation are the same on every shard.  Its output is a
+     * partial sum (moe_forward_partial); the layer output is the sum of the
+     * G partials rounded once to bf16 (an all-reduce, then
+     * moe_sum_partials_bf16).  inter stays the whole layer's I. */
+    int tp_size;
+    int tp_rank;
 } moe_config;
 
 /* Create a handle: checks the configuration and the device, allocates the
@@ -101,6 +114,8 @@ moe_status moe_destroy(moe_handle* h);
 
 /* Copy the layer's weights into the handle (host or device pointers; the
  * copy is synchronous and the caller's buffers may be freed afterwards).
+ * The tensors are always the whole layer's; a tensor-parallel shard keeps
+ * its slice (and checks only the scales it keeps).
  *   router_w   bf16 [E][H]
  *   logit_bias fp32 [E], added to the router logits; NULL = zeros
  *   sel_bias   fp32 [E], the correction bias added to the scores for
@@ -140,6 +155,20 @@ moe_status moe_load_weights_fp8(moe_handle* h, const uint16_t* router_w, const f
  * the next call that synchronises (moe_check_device_error or a getter). */
 moe_status moe_forward(moe_handle* h, const uint16_t* x, int T, uint16_t* y, void* stream);
 
+/* The same forward with the gate-weighted sum left in fp32 and not rounded:
+ * y32 fp32 [T][H] device.  For a tensor-parallel shard this is its partial
+ * output (sum over the shard's slice of the expert middle dimension); for
+ * tp_size 1 it is the layer output before the bf16 rounding. */
+moe_status moe_forward_partial(moe_handle* h, const uint16_t* x, int T, float* y32, void* stream);
+
+/* y[i] = bf16( parts[0][i] + parts[1][i] + ... ), the n_parts (1..8) fp32
+ * device arrays of n elements added in index order in fp32, rounded once to
+ * nearest even: the layer output from the shards' partials (or from one
+ * all-reduced sum, n_parts = 1).  `parts` is a host array of device
+ * pointers; y bf16 device.  Enqueued on `stream` (current device); errors
+ * through moe_last_error(NULL). */
+moe_status moe_sum_partials_bf16(const float* const* parts, int n_parts, size_t n, uint16_t* y, void* stream);
+
 /* Same layer with host buffers: copies x (host, [T][H] bf16) to the device,
  * runs moe_forward on `stream`, copies y back to y_host and waits for the
  * stream.  Pinned host memory gives the fastest copies. */
@@ -155,12 +184,14 @@ moe_status moe_forward_host(moe_handle* h, const uint16_t* x_host, int T, uint16
  *            expert-contiguous order, token-ascending within an expert
  *   act q    u8 [T][H] e4m3 codes of x, scale u8 [T][H/128] E8M0 bytes
  *   inter q  u8 [T*k][I] e4m3 codes of silu(g)*u in perm order,
- *            scale u8 [T*k][I/128]
+ *            scale u8 [T*k][I/128] (a tensor-parallel shard: its I/G
+ *            columns, [T*k][I/G] and [T*k][I/(128 G)])
  *   (with MOE_ACT_SCALE_F32 the u8 scale outputs must be NULL: the scales
  *   are fp32 and come from the two *_scales_f32 getters, which in either
  *   mode return every block scale as its fp32 value, [T][H/128] and
  *   [T*k][I/128])
  *   expert_out fp32 [T*k][H]: o of every (token, slot) row in perm order
+ *            (a shard: the partial over its slice)
  * Any output pointer may be NULL to skip it. */
 moe_status moe_get_logits(moe_handle* h, float* logits);
 moe_status moe_get_routing(moe_handle* h, int32_t* ids, float* gates);
@@ -194,8 +225,35 @@ moe_status moe_check_device_error(moe_handle* h);
  * (1 .. 1,000,000) the wait gives up, records MOE_ERR_TIMEOUT in the
  * handle's device error word (site 99) as any kernel wait would, and the
  * kernel exits normally.  The next moe_check_device_error (or getter)
- * reports MOE_ERR_TIMEOUT and clears the word; the context stays usable. */
+ * reports MOE_ERR_TIMEOUT and clears the word; the context stays usable.
+ * With h = NULL the timeout is recorded in the error record of the
+ * allocation-free routing (moe_route_noalloc) on the current device, which
+ * moe_route_noalloc_check_error reports. */
 moe_status moe_selftest_wait_timeout(moe_handle* h, unsigned int limit_us);
+
+/* Throughput probe of the block-scaled tensor-core instruction the grouped
+ * GEMMs issue (the pages have no counterpart: it measures the denominator of
+ * the prefill roofline): tcgen05.mma kind::mxf8f6f4 .block_scale, M = 128,
+ * N = 256, K = 32, e4m3 x E2M1 with E8M0 scales, operands resident in shared
+ * memory, accumulation in TMEM.  One CTA per SM of `device` issues
+ * 4 * steps_per_cta MMAs (1 .. 2^22 steps) with the GEMMs' issue loop;
+ * `launches` (1 .. 10^5) launches run back to back on the legacy default
+ * stream and the call waits for them.  result (host, float[4]):
+ *   [0] dense TFLOP/s over all launches (2*128*256*32 per MMA, CUDA events),
+ *   [1] mean SM clock in MHz during the last launch (cycle counter against
+ *       the global timer), [2] SM cycles per MMA in the last launch,
+ *   [3] elapsed milliseconds of all launches.
+ * Allocates a small result buffer; errors through moe_last_error(NULL). */
+moe_status moe_selftest_mma_peak(int device, int steps_per_cta, int launches, float* result);
+
+/* Debug: fill every workspace buffer of the handle (routing and dispatch
+ * tables, the quantised activation and SwiGLU rows with their scales, the
+ * expert outputs, the host-entry staging buffers; not the device error word)
+ * with `byte` (0 .. 255), synchronously.  A forward writes everything it
+ * reads, so its output does not depend on what was there before; the tests
+ * check this with 0xFF (NaN as e4m3, E8M0, bf16 and fp32).  The getters
+ * report MOE_ERR_NOT_LOADED until the next forward. */
+moe_status moe_debug_fill_workspace(moe_handle* h, int byte);
 
 /* Number of kernels the last forward launched. */
 int moe_last_launch_count(moe_handle* h);
@@ -225,8 +283,12 @@ moe_status moe_mxfp4_quantize(const float* w, size_t rows, int K, uint8_t* packe
  * latency-critical loops in which cudaMalloc / cudaFree could synchronise
  * the device and stall work already in flight).
  *
- * Computes the router and top-k gate of the layer (the same kernels as
- * moe_forward) for T tokens, without a handle:
+ * Computes the router and top-k gate of the layer (the router and top-k
+ * kernels of moe_forward) for T tokens, without a handle.  The logits are
+ * accumulated over all of H in one pass, whereas moe_forward splits H into
+ * up to 16 partial sums for T <= 512: the fp32 rounding differs, so where a
+ * token's k-th and (k+1)-th keys lie within that rounding the two entry
+ * points may select differently (both selections are valid top-k sets).
  *   x          bf16 [T][H] device, 16-byte aligned
  *   router_w   bf16 [E][H] device, 16-byte aligned
  *   logit_bias fp32 [E] device or NULL (zeros); sel_bias fp32 [E] device or NULL
@@ -242,12 +304,23 @@ moe_status moe_mxfp4_quantize(const float* w, size_t rows, int K, uint8_t* packe
  * a kernel attribute on that device; make that first call before any stream
  * capture.  All calls share the one array and it keeps the last call's
  * contents, so calls that overlap on the GPU (different streams, or several
- * threads) race and must be serialised by the caller.  A kernel wait that
- * gives up is recorded in the array's error word but not reported here.
- * Errors are reported through moe_last_error(NULL). */
+ * threads) race and must be serialised by the caller.  The call does not
+ * wait for the GPU, so a kernel wait that gives up is recorded in the
+ * array's error record (kept until read) and reported by
+ * moe_route_noalloc_check_error.  Errors are reported through
+ * moe_last_error(NULL). */
 moe_status moe_route_noalloc(const uint16_t* x, int T, int H, const uint16_t* router_w, const float* logit_bias,
                              const float* sel_bias, int E, int k, int score_func, int32_t* ids, float* gates,
                              void* stream);
+
+/* Waits for `stream`, then reports and clears the error record of the
+ * allocation-free routing on the current device: MOE_ERR_TIMEOUT if a kernel
+ * wait of an earlier moe_route_noalloc call gave up since the last check
+ * (MOE_ERR_DEVICE for another kernel error), MOE_OK otherwise.  Reads and
+ * clears the record with cudaMemcpyFromSymbol / cudaMemcpyToSymbol, so it
+ * allocates nothing either; it synchronises, so keep it out of stream
+ * capture.  Errors through moe_last_error(NULL). */
+moe_status moe_route_noalloc_check_error(void* stream);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,8 @@ def test_library_is_sm103a_only_and_not_linked_to_libcuda():
 
 @pytest.mark.parametrize("field,value,status", [
     ("hidden", 100, 2), ("hidden", 0, 2), ("inter", 130, 2), ("num_experts", 0, 2), ("num_experts", 513, 2),
-    ("top_k", 9, 2), ("top_k", 0, 2), ("max_tokens", 0, 2), ("score_func", 5, 1)])
+    ("top_k", 9, 2), ("top_k", 0, 2), ("max_tokens", 0, 2), ("score_func", 5, 1),
+    ("tp_size", 9, 1), ("tp_size", -1, 1), ("tp_rank", 1, 1), ("tp_size", 3, 2)])
 def test_init_rejects_bad_config_on_host(field, value, status):
     L = moe.lib()
     c = dict(hidden=512, inter=256, num_experts=16, top_k=8, max_tokens=64, score_func=0, device=0)
