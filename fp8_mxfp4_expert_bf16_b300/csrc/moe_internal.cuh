@@ -74,6 +74,8 @@ struct DevState {
     CUtensorMap tm_aq[kNumABox], tm_hq[kNumABox], tm_w13, tm_w2;
     CUtensorMap tm_wr64, tm_wr128;   // router weights, 64 / 128-row boxes
     int num_sms;
+    int max_clusters2 = 0;   // resident clusters of two grouped-GEMM CTAs (the clustered grid / 2)
+    int gemm_cluster = 1;    // 1: heavy phase in clusters of two where it pays off; 0: never
     bool pdl = true;     // launch the forward's kernels with programmatic stream serialisation
 };
 
@@ -96,6 +98,12 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
+
+// Prefill-sized batches (on average at least 32 rows per expert): every
+// m-tile of the grouped GEMMs is loaded as a full 128-row activation box (its
+// padding rows are zero in HBM, so the MMAs on them spend little energy; the
+// GEMMs are bound by the power cap there) and there is no light phase.
+__host__ __forceinline__ bool prefill_mode(const DevState& s, int T) { return (long long)T * s.K >= 32LL * s.E; }
 
 // Word index of row r of m-tile mt, K-block kb, in a scale-factor buffer laid
 // out for tcgen05.cp .32x128b.warpx4: per (mt, kb) 128 words, row r at word
@@ -133,8 +141,9 @@ cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, c
 int router_split(int T, int H);
 cudaError_t router_set_attributes();
 // grouped GEMMs (mx_gemm.cu)
-cudaError_t launch_gemm1(const DevState& s, cudaStream_t st);
-cudaError_t launch_gemm2(const DevState& s, cudaStream_t st);
+cudaError_t launch_gemm1(const DevState& s, cudaStream_t st, int T);
+cudaError_t launch_gemm2(const DevState& s, cudaStream_t st, int T);
 cudaError_t gemm_set_attributes();
+int gemm_max_clusters2();
 
 }  // namespace moe

@@ -287,7 +287,8 @@ __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict_
                                                       int32_t* __restrict__ mtile_expert,
                                                       int32_t* __restrict__ mtile_rows, int32_t* __restrict__ n_mtiles,
                                                       int32_t* __restrict__ light_list,
-                                                      int32_t* __restrict__ heavy_list, int nchunk, int E)
+                                                      int32_t* __restrict__ heavy_list, int nchunk, int E,
+                                                      int light_rows)
 {
     griddep_wait();
     griddep_launch_dependents();
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(kMaxExperts) k_scan(const int32_t* __restrict_
     }
     const int mt = (run + kBM - 1) / kBM;
     const int rem = run - (mt - 1) * kBM;                 // rows of the last m-tile
-    const int light = (mt > 0 && rem <= kLightRows) ? 1 : 0;
+    const int light = (mt > 0 && rem <= light_rows) ? 1 : 0;
     const int heavy = mt - light;
     const int ex_cnt = block_exclusive_scan<kMaxExperts>(run, warp_tot);
     const int ex_mt = block_exclusive_scan<kMaxExperts>(mt, warp_tot);
@@ -444,7 +445,7 @@ __global__ void __launch_bounds__(kMaxExperts) k_dispatch_small(
     const int32_t* __restrict__ ids, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ mtile_off, int32_t* __restrict__ mtile_expert, int32_t* __restrict__ mtile_rows,
     int32_t* __restrict__ n_mtiles, int32_t* __restrict__ light_list, int32_t* __restrict__ heavy_list,
-    int32_t* __restrict__ prow, int T, int E, int K)
+    int32_t* __restrict__ prow, int T, int E, int K, int light_rows)
 {
     griddep_wait();
     griddep_launch_dependents();
@@ -471,7 +472,7 @@ __global__ void __launch_bounds__(kMaxExperts) k_dispatch_small(
     const int run = e < E ? hist[e] : 0;
     const int mt = (run + kBM - 1) / kBM;
     const int rem = run - (mt - 1) * kBM;
-    const int light = (mt > 0 && rem <= kLightRows) ? 1 : 0;
+    const int light = (mt > 0 && rem <= light_rows) ? 1 : 0;
     const int heavy = mt - light;
     const int ex_cnt = block_exclusive_scan<kMaxExperts>(run, warp_tot);
     const int ex_mt = block_exclusive_scan<kMaxExperts>(mt, warp_tot);
@@ -508,11 +509,16 @@ __global__ void __launch_bounds__(kMaxExperts) k_dispatch_small(
     }
 }
 
+// m-tiles with at most this many valid rows run in the GEMMs' light phase:
+// kLightRows for decode-sized batches, none for prefill-sized ones (there
+// every m-tile is loaded as a full 128-row box, see prefill_mode)
+static int light_rows(const DevState& s, int T) { return prefill_mode(s, T) ? 0 : kLightRows; }
+
 cudaError_t launch_dispatch_small(const DevState& s, int T, cudaStream_t st)
 {
     return launch_kernel(k_dispatch_small, dim3(1), dim3(kMaxExperts), 0, st, s.pdl, (const int32_t*)s.ids, s.counts,
                          s.offsets, s.mtile_off, s.mtile_expert, s.mtile_rows, s.n_mtiles, s.light_list, s.heavy_list,
-                         s.prow, T, s.E, s.K);
+                         s.prow, T, s.E, s.K, light_rows(s, T));
 }
 
 cudaError_t launch_quant_scatter(const DevState& s, const uint16_t* x, int T, cudaStream_t st)
@@ -533,7 +539,7 @@ cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStr
     if (e == cudaSuccess)
         e = launch_kernel(k_scan, dim3(1), dim3(kMaxExperts), 0, st, s.pdl, (const int32_t*)s.chunk_hist, s.chunk_base,
                           s.counts, s.offsets, s.mtile_off, s.mtile_expert, s.mtile_rows, s.n_mtiles, s.light_list,
-                          s.heavy_list, nchunk, s.E);
+                          s.heavy_list, nchunk, s.E, light_rows(s, T));
     if (e == cudaSuccess)
         e = launch_kernel(k_scatter_rows, dim3(nchunk), dim3(kChunk), 0, st, s.pdl, (const int32_t*)s.ids,
                           (const int32_t*)s.chunk_base, (const int32_t*)s.mtile_off, s.prow, T, s.E, s.K);

@@ -126,13 +126,11 @@ __global__ void __launch_bounds__(128, 1)
                 router_fail(ctl, err, 12);
     } else if (warp == 1 && lane == 0) {
         const uint32_t idesc = idesc_bf16(128, (uint32_t)N);
-        bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % kRStages;
             const uint32_t ph = (uint32_t)(kb / kRStages) & 1u;
             if (!mbar_wait(smem_u32(&ctl->full[s]), ph, abrt)) {
                 router_fail(ctl, err, 13);
-                ok = false;
                 break;
             }
             tc_fence_after();
@@ -143,8 +141,7 @@ __global__ void __launch_bounds__(128, 1)
                          (kb | k) != 0 ? 1u : 0u);
             tc_commit(smem_u32(&ctl->empty[s]));
         }
-        // acc_full also serves as the drain: it completes once every MMA above has
-        (void)ok;
+        // acc_full also serves as the drain: it completes once every MMA above has completed
         tc_commit(smem_u32(&ctl->acc_full));
     }
     __syncwarp();

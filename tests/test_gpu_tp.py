@@ -39,7 +39,7 @@ def _shard(inp, G, r, mode):
     (4, 0, "mxfp4", (300, 512, 16, 512, 8)),
     (4, 0, "mxfp4", (64, 1024, 32, 1024, 8)),   # decode-like: light m-tiles only
     (2, 1, "mxfp4", (300, 512, 16, 512, 8)),    # fp32 activation scales
-    (2, 0, "fp8", (200, 512, 16, 512, 4)),      # fp8 experts
+    (2, 0, "fp8", (200, 512, 16, 1024, 8)),     # fp8 experts
 ])
 def test_shards_add_up_to_the_layer(G, mode, weights, shape):
     import torch
