@@ -260,10 +260,6 @@ def config_dict(cfg, args):
     return dict(workload_desc(cfg), act_scale=args.act_scale, weights=args.weights)
 
 
-def launch_desc(args, layer=None):
-    return {"gemm_clusters": (layer.gemm_cluster_slots() if layer is not None else None) if not args.no_gemm_clusters
-            else 0}
-
 
 def headline_config(args):
     import dataclasses
@@ -358,8 +354,6 @@ def run_config(args, cfg, device, stream, P, peak, ws, rank, dist, cpu_budget):
     layer = moe.MoELayer(c.H, c.I, c.E, c.k, c.T, c.score_func, device=device, act_scale_mode=act_mode)
     load = layer.load_weights_fp8 if args.weights == "fp8" else layer.load_weights
     load(inp.router_w, inp.logit_bias, inp.sel_bias, inp.w13_q, inp.w13_s, inp.w2_q, inp.w2_s)
-    if args.no_gemm_clusters:
-        layer.set_gemm_clusters(False)
     x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).to(f"cuda:{device}")
     y = torch.empty_like(x)
     eb13, eb2 = expert_bytes(c, args.weights)
@@ -474,7 +468,7 @@ def run_config(args, cfg, device, stream, P, peak, ws, rank, dist, cpu_budget):
     entry = {
         "value": value, "unit": "tokens/s", "ms_per_step": ms_max / args.steps,
         "windows_ms_per_step": [w / args.steps for w in windows],
-        "config": config_dict(cfg, args), "launch": launch_desc(args, layer),
+        "config": config_dict(cfg, args),
         "l2": ("weights fit in L2: L2 flushed (256 MB write) between timed steps" if flush is not None else
                "inputs larger than L2: every step streams the active experts' weights from HBM"),
         "roofline": roof, "stage_ms": stage,
@@ -618,7 +612,7 @@ def run_gpu(args):
             "metric": METRIC, "value": e["value"], "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": e["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e2m1 (fp32 accumulate)",
-            "data": "synthetic", "config": e["config"], "launch": e["launch"], "parallelism": f"replicas{ws}",
+            "data": "synthetic", "config": e["config"], "parallelism": f"replicas{ws}",
             "windows": args.windows, "windows_ms_per_step": e["windows_ms_per_step"], "l2": e["l2"],
             "roofline": e["roofline"], "stage_ms": e["stage_ms"], "stage_window": e["stage_window"],
             "routing": e["routing"], "cpu_baseline": e["cpu_baseline"], "e2e": e["e2e"],
@@ -648,8 +642,6 @@ def main():
     ap.add_argument("--act-scale", default="e8m0", choices=sorted(ACT_SCALES),
                     help="activation block scales: power-of-two E8M0 (default) or fp32 amax/448")
     ap.add_argument("--peak-only", action="store_true", help="only measure the block-scaled tensor-core rate")
-    ap.add_argument("--no-gemm-clusters", action="store_true",
-                    help="single-CTA grouped-GEMM launches only (no clusters of two sharing activation tiles)")
     ap.add_argument("--peak-seconds", type=float, default=3.0, help="length of the sustained peak measurement")
     ap.add_argument("--tp", type=int, default=0,
                     help="tensor-parallel layer over the torchrun group (N ranks = N shards, NCCL all-reduce)")

@@ -87,8 +87,6 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_check_device_error": (S, [P]),
         "moe_selftest_wait_timeout": (S, [P, ctypes.c_uint]),
         "moe_last_launch_count": (I, [P]),
-        "moe_set_gemm_clusters": (S, [P, I]),
-        "moe_gemm_cluster_slots": (I, [P]),
         "moe_last_error": (ctypes.c_char_p, [P]),
         "moe_status_string": (ctypes.c_char_p, [I]),
         "moe_route_noalloc": (S, [P, I, I, P, P, P, I, I, I, P, P, P]),
@@ -245,14 +243,6 @@ class MoELayer:
 
     def launch_count(self) -> int:
         return self.L.moe_last_launch_count(self.h)
-
-    def set_gemm_clusters(self, enable: bool):
-        """Heavy grouped-GEMM tiles in clusters of two CTAs sharing each
-        activation tile by multicast (default on where it pays off)."""
-        self._check(self.L.moe_set_gemm_clusters(self.h, int(bool(enable))))
-
-    def gemm_cluster_slots(self) -> int:
-        return self.L.moe_gemm_cluster_slots(self.h)
 
     def debug_fill_workspace(self, byte: int):
         """Fill every workspace buffer with ``byte`` (a forward must not read

@@ -312,11 +312,7 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
     }
     if (ok)
         ok = gemm_set_attributes() == cudaSuccess && router_set_attributes() == cudaSuccess;
-    if (ok) {
-        s.max_clusters2 = gemm_max_clusters2();
-        // no multicast in a tensor-parallel shard (code that runs on several GPUs)
-        s.gemm_cluster = (G == 1) ? 1 : 0;
-    }
+
     if (ok) ok = cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         moe_destroy(h);
@@ -632,17 +628,6 @@ moe_status moe_forward_host(moe_handle* h, const uint16_t* x_host, int T, uint16
 }
 
 int moe_last_launch_count(moe_handle* h) { return h ? h->last_launches : 0; }
-
-moe_status moe_set_gemm_clusters(moe_handle* h, int enable)
-{
-    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_set_gemm_clusters: handle is NULL");
-    if (enable && h->tp_size > 1)
-        return fail(h, MOE_ERR_UNSUPPORTED, "moe_set_gemm_clusters: no multicast in a tensor-parallel shard");
-    h->s.gemm_cluster = enable ? 1 : 0;
-    return MOE_OK;
-}
-
-int moe_gemm_cluster_slots(moe_handle* h) { return (h && h->s.gemm_cluster) ? 2 * h->s.max_clusters2 : 0; }
 
 moe_status moe_debug_fill_workspace(moe_handle* h, int byte)
 {

@@ -74,8 +74,6 @@ struct DevState {
     CUtensorMap tm_aq[kNumABox], tm_hq[kNumABox], tm_w13, tm_w2;
     CUtensorMap tm_wr64, tm_wr128;   // router weights, 64 / 128-row boxes
     int num_sms;
-    int max_clusters2 = 0;   // resident clusters of two grouped-GEMM CTAs (the clustered grid / 2)
-    int gemm_cluster = 1;    // 1: heavy phase in clusters of two where it pays off; 0: never
     bool pdl = true;     // launch the forward's kernels with programmatic stream serialisation
 };
 
@@ -144,6 +142,5 @@ cudaError_t router_set_attributes();
 cudaError_t launch_gemm1(const DevState& s, cudaStream_t st, int T);
 cudaError_t launch_gemm2(const DevState& s, cudaStream_t st, int T);
 cudaError_t gemm_set_attributes();
-int gemm_max_clusters2();
 
 }  // namespace moe

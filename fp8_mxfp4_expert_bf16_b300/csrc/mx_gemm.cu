@@ -164,14 +164,12 @@ __device__ __forceinline__ void raise_error(GemmCtl* g, int32_t* err, int where)
     *(volatile int*)&g->abort = 1;
 }
 
-// empty_count: how many CTAs' MMA commits free a stage (2 when the two CTAs
-// of a cluster share each stage's activation tile)
 template <int kStages>
-__device__ __forceinline__ void init_phase(PhaseCtl<kStages>& pc, uint32_t empty_count)
+__device__ __forceinline__ void init_phase(PhaseCtl<kStages>& pc)
 {
     for (int s = 0; s < kStages; ++s) {
         mbar_init(smem_u32(&pc.full[s]), 1);
-        mbar_init(smem_u32(&pc.empty[s]), empty_count);
+        mbar_init(smem_u32(&pc.empty[s]), 1);
     }
     mbar_init(smem_u32(&pc.acc_full), 1);
     mbar_init(smem_u32(&pc.acc_empty), kEpiWarps);
@@ -304,56 +302,35 @@ __device__ __forceinline__ void store_rows_transposed(uint32_t taddr, uint32_t s
     }
 }
 
-// The tiles one CTA works on in a phase.  Alone (kCl = 1) it takes tiles
-// blockIdx.x, + gridDim.x, ... of the phase's count * NT (m-tile, n-tile)
-// tiles.  In a cluster of two (kCl = 2) the cluster takes pair tiles
-// cluster, + clusters, ... of count * NT / 2; both CTAs work on the same
-// m-tile at the same time, CTA rank r on n-tile 2 j + r, so that each loads
-// half of the shared activation tile and multicasts it to both.
-template <int kCl>
+// The tiles one CTA works on in a phase: tiles blockIdx.x, + gridDim.x, ...
+// of the phase's count * NT (m-tile, n-tile) tiles, m-tile-major.
 struct TileSeq {
-    int first, step, total, per_mt, rank;
+    int first, step, total, per_mt;
     __device__ __forceinline__ TileSeq(int count, int NT)
+        : first((int)blockIdx.x), step((int)gridDim.x), total(count * NT), per_mt(NT)
     {
-        if constexpr (kCl == 1) {
-            first = blockIdx.x;
-            step = gridDim.x;
-            total = count * NT;
-            per_mt = NT;
-            rank = 0;
-        } else {
-            rank = (int)cluster_ctarank();
-            first = blockIdx.x / kCl;
-            step = gridDim.x / kCl;
-            total = count * (NT / kCl);
-            per_mt = NT / kCl;
-        }
     }
     __device__ __forceinline__ int mt_index(int t) const { return t / per_mt; }
-    __device__ __forceinline__ int nt_of(int t) const { return (t - (t / per_mt) * per_mt) * kCl + rank; }
+    __device__ __forceinline__ int nt_of(int t) const { return t - (t / per_mt) * per_mt; }
 };
 
 // One phase (the light or the heavy m-tile list) of the grouped GEMM.  Every
 // role drains its own work before returning: the producer waits until its
 // copies have landed, the MMA issuer until its MMAs have completed, the
 // epilogue has read its last accumulator.
-// kCl = 2 (heavy phase only): the activation maps tmA0..2 have half the box
-// heights of the phase's shape; CTA rank r loads rows [r h, r h + h) of the
-// m-tile's box and multicasts them to both CTAs.
-template <int kMode, bool kLight, bool kF32S, bool kW8, int kCl>
+template <int kMode, bool kLight, bool kF32S, bool kW8>
 __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<Shape<kLight>::kStages>& pc,
                                            uint32_t tmem, const CUtensorMap* tmA0, const CUtensorMap* tmA1,
                                            const CUtensorMap* tmA2, const CUtensorMap* tmW, const GemmArgs& args,
                                            const int32_t* list, int count, bool& waited)
 {
     using S = Shape<kLight>;
-    static_assert(kCl == 1 || (!kLight && !kF32S && !kW8), "clusters of two: heavy phase, E8M0 path only");
     constexpr int kStages = S::kStages, kStageStride = S::kStageStride;
     constexpr int kSFAOff = S::kSFAOff, kSFBOff = S::kSFBOff;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const volatile int* abrt = &g->abort;
     const int NT = args.NT, KB = args.KB;
-    const TileSeq<kCl> ts(count, NT);
+    const TileSeq ts(count, NT);
 
     if (warp == 0) {
         if (lane == 0 && ts.first < ts.total) {
@@ -378,20 +355,12 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 cur_e = args.mtile_expert[cur_mt];
                 cur_rows = args.mtile_rows[cur_mt];
                 nxt_mt = load_mt(tile + 2 * stride);
-                // activation box: the smallest of the three heights that covers the valid rows
-                // (in a cluster each CTA loads one half of it: maps of half the height)
+                // activation box: the smallest of the three heights that covers the
+                // valid rows (prefill-sized batches: always the full 128-row box)
                 const int sel = (!kLight && args.full_box) ? 2 : (rows <= S::kBox0 ? 0 : (rows <= S::kBox1 ? 1 : 2));
                 const CUtensorMap* tA = sel == 0 ? tmA0 : (sel == 1 ? tmA1 : tmA2);
-                const int box_rows = sel == 0 ? S::kBox0 : (sel == 1 ? S::kBox1 : S::kBox2);
-                const uint32_t a_bytes = (uint32_t)box_rows * 128u;
-                const int a_row0 = mt * kBM + (kCl == 2 ? ts.rank * (box_rows / 2) : 0);
-                const uint32_t a_off = kCl == 2 ? (uint32_t)(ts.rank * (box_rows / 2) * 128) : 0u;
-                auto load_a = [&](uint8_t* st, uint32_t fb, int kb) {
-                    if constexpr (kCl == 2)
-                        tma_load_2d_mc(smem_u32(st) + a_off, tA, fb, kb * kBK, a_row0, (uint16_t)0x3);
-                    else
-                        tma_load_2d(smem_u32(st), tA, fb, kb * kBK, a_row0);
-                };
+                const uint32_t a_bytes = (uint32_t)(sel == 0 ? S::kBox0 : (sel == 1 ? S::kBox1 : S::kBox2)) * 128u;
+                auto load_a = [&](uint8_t* st, uint32_t fb, int kb) { tma_load_2d(smem_u32(st), tA, fb, kb * kBK, mt * kBM); };
                 // weight bytes of a stage: E2M1 rows (8 KB per 128 rows) + their scale chunks,
                 // or e4m3 rows (16 KB per 128 rows, block scales applied in the epilogue)
                 const uint32_t tx = a_bytes +
@@ -556,9 +525,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         mma_mxf8f6f4_elect(acc, ad + 2, bd + 2, id1, sfa_t, sfa_t + 8u, 1u);
                         mma_mxf8f6f4_elect(acc, ad + 4, bd + 4, id2, sfa_t, sfa_t + 8u, 1u);
                         mma_mxf8f6f4_elect(acc, ad + 6, bd + 6, id3, sfa_t, sfa_t + 8u, 1u);
-                        // the stage is free once both CTAs sharing its activation tile are done with it
-                        if constexpr (kCl == 2) tc_commit_mc_elect(empty0 + 8u * s, (uint16_t)0x3);
-                        else tc_commit_elect(empty0 + 8u * s);
+                        tc_commit_elect(empty0 + 8u * s);
                         advance();
                     }
                     if (ok) tc_commit_elect(smem_u32(&pc.acc_full));
@@ -846,10 +813,8 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
 
 // mode 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows; kF32S: the
 // activation blocks carry fp32 scales, kW8: the experts are e4m3 with fp32
-// 128 x 128 block scales (either one: promotion in the epilogue); kCl: CTAs
-// per cluster in the heavy phase (2: the activation tile of each stage is
-// loaded half by each CTA and multicast to both)
-template <int kMode, bool kF32S, bool kW8, int kCl>
+// 128 x 128 block scales (either one: promotion in the epilogue)
+template <int kMode, bool kF32S, bool kW8>
 __global__ void __launch_bounds__(kThreads, 1)
     k_mx_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
               const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
@@ -865,8 +830,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();   // generic-proxy writes above, read by tcgen05.cp
     }
     if (threadIdx.x == 0) {
-        init_phase(g->light, 1);
-        init_phase(g->heavy, (uint32_t)kCl);
+        init_phase(g->light);
+        init_phase(g->heavy);
         g->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA0);
@@ -886,24 +851,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = g->tmem_base;
     bool waited = false;   // the producer's wait for the previous kernel (producer thread only)
 
-    gemm_phase<kMode, true, kF32S, kW8, 1>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args,
-                                           args.light_list, *args.light_count, waited);
+    gemm_phase<kMode, true, kF32S, kW8>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args, args.light_list,
+                                        *args.light_count, waited);
     // the heavy phase reuses the ring and the accumulator: every role of the
-    // light phase has drained its own work.  In a cluster both CTAs must be
-    // past their light phase (and their barriers initialised) before either
-    // multicasts into the other's ring.
+    // light phase has drained its own work
     tc_fence_before();
-    if constexpr (kCl == 2) cluster_sync();
-    else __syncthreads();
+    __syncthreads();
     tc_fence_after();
-    if (!*(volatile int*)&g->abort) {
-        if constexpr (kCl == 2)   // half-height maps: 16 / 32 / 64 rows
-            gemm_phase<kMode, false, kF32S, kW8, 2>(smem, g, g->heavy, tmem, &tmA1, &tmA2, &tmA3, &tmW, args,
-                                                    args.heavy_list, *args.heavy_count, waited);
-        else
-            gemm_phase<kMode, false, kF32S, kW8, 1>(smem, g, g->heavy, tmem, &tmA2, &tmA3, &tmA4, &tmW, args,
-                                                    args.heavy_list, *args.heavy_count, waited);
-    }
+    if (!*(volatile int*)&g->abort)
+        gemm_phase<kMode, false, kF32S, kW8>(smem, g, g->heavy, tmem, &tmA2, &tmA3, &tmA4, &tmW, args,
+                                             args.heavy_list, *args.heavy_count, waited);
     // a CTA without tiles still waits before it lets the next kernel start
     if (warp == 0 && lane == 0) {
         producer_wait_once(waited, args.early_trigger);
@@ -911,10 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     tc_fence_before();
-    // neither CTA of a cluster leaves while the other may still signal its
-    // barriers or write its shared memory
-    if constexpr (kCl == 2) cluster_sync();
-    else __syncthreads();
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -923,38 +877,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t gemm_set_attributes()
 {
-    const void* ks[] = {(const void*)k_mx_gemm<0, false, false, 1>, (const void*)k_mx_gemm<1, false, false, 1>,
-                        (const void*)k_mx_gemm<0, true, false, 1>,  (const void*)k_mx_gemm<1, true, false, 1>,
-                        (const void*)k_mx_gemm<0, false, true, 1>,  (const void*)k_mx_gemm<1, false, true, 1>,
-                        (const void*)k_mx_gemm<0, true, true, 1>,   (const void*)k_mx_gemm<1, true, true, 1>,
-                        (const void*)k_mx_gemm<0, false, false, 2>, (const void*)k_mx_gemm<1, false, false, 2>};
+    const void* ks[] = {(const void*)k_mx_gemm<0, false, false>, (const void*)k_mx_gemm<1, false, false>,
+                        (const void*)k_mx_gemm<0, true, false>,  (const void*)k_mx_gemm<1, true, false>,
+                        (const void*)k_mx_gemm<0, false, true>,  (const void*)k_mx_gemm<1, false, true>,
+                        (const void*)k_mx_gemm<0, true, true>,   (const void*)k_mx_gemm<1, true, true>};
     cudaError_t e = cudaSuccess;
     for (const void* k : ks)
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     return e;
-}
-
-// How many clusters of two CTAs of the grouped GEMM can be resident at once
-// (0 if none): the grid of the clustered launch.
-int gemm_max_clusters2()
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_mx_gemm<0, false, false, 2>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    return n;
 }
 
 static GemmArgs common_args(const DevState& s)
@@ -1001,58 +931,24 @@ template <int kMode, bool kF32S, bool kW8>
 static cudaError_t launch_variant(const DevState& s, cudaStream_t st, const GemmArgs& a, const CUtensorMap* tA,
                                   const CUtensorMap& tW)
 {
-    return launch_kernel(k_mx_gemm<kMode, kF32S, kW8, 1>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl,
-                         tA[0], tA[1], tA[2], tA[3], tA[4], tW, a);
-}
-
-// The clustered variant (heavy phase in clusters of two with a multicast
-// activation tile): launched with the cluster dimension and, as every kernel
-// of the forward, programmatic stream serialisation.
-template <int kMode>
-static cudaError_t launch_clustered(const DevState& s, cudaStream_t st, const GemmArgs& a, const CUtensorMap* tA,
-                                   const CUtensorMap& tW)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * s.max_clusters2);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = s.pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, k_mx_gemm<kMode, false, false, 2>, tA[0], tA[1], tA[2], tA[3], tA[4], tW, a);
-}
-
-// Clusters pay off only when the heavy phase carries the work (prefill-sized
-// batches: on average at least 32 rows per expert); they need an even number
-// of n-tiles and the E8M0 (non-promotion) path.
-static bool use_clusters(const DevState& s, int T, int NT)
-{
-    return s.gemm_cluster && s.max_clusters2 > 0 && !s.act_f32 && !s.w_fp8 && NT % 2 == 0 && prefill_mode(s, T);
+    return launch_kernel(k_mx_gemm<kMode, kF32S, kW8>, dim3(s.num_sms), dim3(kThreads), kSmemBytes, st, s.pdl, tA[0],
+                         tA[1], tA[2], tA[3], tA[4], tW, a);
 }
 
 template <int kMode>
 static cudaError_t launch_mode(const DevState& s, cudaStream_t st, const GemmArgs& a, const CUtensorMap* tA,
-                               const CUtensorMap& tW, int T)
+                               const CUtensorMap& tW)
 {
     if (s.w_fp8) {
         return s.act_f32 ? launch_variant<kMode, true, true>(s, st, a, tA, tW)
                          : launch_variant<kMode, false, true>(s, st, a, tA, tW);
     }
-    if (s.act_f32) return launch_variant<kMode, true, false>(s, st, a, tA, tW);
-    if (use_clusters(s, T, a.NT)) return launch_clustered<kMode>(s, st, a, tA, tW);
-    return launch_variant<kMode, false, false>(s, st, a, tA, tW);
+    return s.act_f32 ? launch_variant<kMode, true, false>(s, st, a, tA, tW)
+                     : launch_variant<kMode, false, false>(s, st, a, tA, tW);
 }
 
 // Light m-tiles (activation boxes of 8 / 16 rows: maps 0, 1), then heavy
-// m-tiles (32 / 64 / 128 rows: maps 2..4; clustered: 16 / 32 / 64, maps
-// 1..3), in one launch.
+// m-tiles (32 / 64 / 128 rows: maps 2..4), in one launch.
 cudaError_t launch_gemm1(const DevState& s, cudaStream_t st, int T)
 {
     GemmArgs a = gemm1_args(s);
@@ -1061,7 +957,7 @@ cudaError_t launch_gemm1(const DevState& s, cudaStream_t st, int T)
     a.as32 = s.asf32;
     a.hs32 = s.hsf32;
     a.ws = s.ws13;
-    return launch_mode<0>(s, st, a, s.tm_aq, s.tm_w13, T);
+    return launch_mode<0>(s, st, a, s.tm_aq, s.tm_w13);
 }
 
 cudaError_t launch_gemm2(const DevState& s, cudaStream_t st, int T)
@@ -1071,7 +967,7 @@ cudaError_t launch_gemm2(const DevState& s, cudaStream_t st, int T)
     a.full_box = prefill_mode(s, T) ? 1 : 0;
     a.as32 = s.hsf32;
     a.ws = s.ws2;
-    return launch_mode<1>(s, st, a, s.tm_hq, s.tm_w2, T);
+    return launch_mode<1>(s, st, a, s.tm_hq, s.tm_w2);
 }
 
 }  // namespace moe

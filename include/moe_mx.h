@@ -258,19 +258,6 @@ moe_status moe_debug_fill_workspace(moe_handle* h, int byte);
 /* Number of kernels the last forward launched. */
 int moe_last_launch_count(moe_handle* h);
 
-/* Grouped-GEMM launch shape (a tuning knob; the pages have no counterpart).
- * With enable = 1 (the default of a whole-layer handle) a forward whose
- * batch gives the experts at least 32 rows on average runs the 128-row
- * m-tiles of both grouped GEMMs in clusters of two CTAs that work on the
- * same m-tile: each loads half of every activation tile from this GPU's
- * memory and multicasts it to both (needs an even number of n-tiles and the
- * E8M0 activation scales with MXFP4 experts; otherwise the single-CTA
- * launch runs).  enable = 0: single-CTA launches only.  The output is the
- * same bit for bit either way.  A tensor-parallel shard never multicasts
- * (MOE_ERR_UNSUPPORTED for enable = 1).  moe_gemm_cluster_slots returns the
- * CTAs of the clustered launch (0: not enabled or not available). */
-moe_status moe_set_gemm_clusters(moe_handle* h, int enable);
-int moe_gemm_cluster_slots(moe_handle* h);
 
 const char* moe_last_error(moe_handle* h);
 const char* moe_status_string(moe_status s);

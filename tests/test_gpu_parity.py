@@ -153,29 +153,3 @@ def test_forward_captures_in_a_cuda_graph():
     torch.cuda.synchronize()
     layer.check_device_error()
     assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), y_eager)
-
-
-@pytest.mark.parametrize("shape", [
-    # T, H, E, I, k, bias: heavy m-tiles (>= 32 rows per expert on average)
-    (300, 512, 16, 256, 8, "none"),
-    (1000, 1024, 24, 512, 8, "zipf:1.1"),     # skewed: full, partial and light m-tiles
-    (700, 768, 8, 512, 4, "normal:1.0"),      # 3 n-tiles per m-tile in the down GEMM: single-CTA there
-])
-def test_clustered_gemms_match_single_cta_bit_for_bit(shape):
-    """The clustered launch (two CTAs per m-tile sharing each activation
-    tile by multicast) computes every output element with the same MMAs in
-    the same order as the single-CTA launch: bit-identical outputs."""
-    T, H, E, I, k, bias = shape
-    inp = synth.custom_inputs(T, H, E, I, k, seed=1100 + T, bias=bias)
-    layer = make_layer(inp)
-    assert layer.gemm_cluster_slots() > 0
-    stats, y_cl, _ = full_check(layer, inp)
-    hq_cl, _ = layer.inter_quant()
-    o_cl = layer.expert_out()
-    layer.set_gemm_clusters(False)
-    assert layer.gemm_cluster_slots() == 0
-    y_1 = run_layer(layer, inp)
-    hq_1, _ = layer.inter_quant()
-    o_1 = layer.expert_out()
-    assert np.array_equal(y_cl, y_1) and np.array_equal(hq_cl, hq_1) and np.array_equal(o_cl, o_1)
-    print(shape, stats)
