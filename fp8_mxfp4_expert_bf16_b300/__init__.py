@@ -69,6 +69,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_load_weights_fp8": (S, [P, P, P, P, P, P, P, P]),
         "moe_forward": (S, [P, P, I, P, P]),
         "moe_forward_host": (S, [P, P, I, P, P]),
+        "moe_forward_host_async": (S, [P, P, I, P, P]),
+        "moe_host_sync": (S, [P]),
         "moe_forward_partial": (S, [P, P, I, P, P]),
         "moe_sum_partials_bf16": (S, [ctypes.POINTER(P), I, ctypes.c_size_t, P, P]),
         "moe_get_logits": (S, [P, P]),
@@ -228,6 +230,18 @@ class MoELayer:
         self._check(self.L.moe_forward_host(self.h, _ptr(x_host), T, _ptr(y_host), self._stream(stream)))
         self.last_T = T
         return y_host
+
+    def forward_host_async(self, x_host, y_host, stream=None):
+        """Enqueue a host-buffer forward (pinned numpy arrays or CPU tensors,
+        bf16 bits) and return; host_sync() waits for every call so far.
+        Consecutive calls overlap their copies with each other's forwards."""
+        T = x_host.shape[0]
+        self._check(self.L.moe_forward_host_async(self.h, _ptr(x_host), T, _ptr(y_host), self._stream(stream)))
+        self.last_T = T
+        return y_host
+
+    def host_sync(self):
+        self._check(self.L.moe_host_sync(self.h))
 
     def set_profiling(self, on: bool = True):
         self._check(self.L.moe_set_profiling(self.h, int(on)))

@@ -32,8 +32,15 @@ struct moe_handle {
     bool ev_valid = false;
     int prof_count = 0;      // forwards recorded since profiling was enabled / last read
     std::vector<void*> allocs;
-    uint16_t* xbuf = nullptr;   // staging for moe_forward_host
-    uint16_t* ybuf = nullptr;
+    // staging for the host-buffer entry points: two slots, so that one call's
+    // copies overlap the neighbouring calls' forwards
+    uint16_t* xbuf[2] = {nullptr, nullptr};
+    uint16_t* ybuf[2] = {nullptr, nullptr};
+    cudaStream_t s_in = nullptr, s_out = nullptr;   // copy streams (host -> device, device -> host)
+    cudaEvent_t ev_in[2] = {}, ev_fwd[2] = {}, ev_out[2] = {};
+    bool host_ready = false;      // streams and events created
+    bool slot_used[2] = {false, false};
+    int host_calls = 0;           // host-buffer calls so far (slot = calls % 2)
     // owned weight buffers
     void* w_alloc[8] = {};      // [7]: staging of whole tensors while a shard loads its slice
     // tensor-parallel shard of the expert middle dimension (1 / 0: the whole layer)
@@ -196,6 +203,16 @@ moe_status moe_destroy(moe_handle* h)
     if (h->ev_valid)
         for (auto& slot : h->ev)
             for (auto& e : slot) cudaEventDestroy(e);
+    if (h->host_ready) {
+        cudaStreamSynchronize(h->s_out);
+        for (int b = 0; b < 2; ++b) {
+            cudaEventDestroy(h->ev_in[b]);
+            cudaEventDestroy(h->ev_fwd[b]);
+            cudaEventDestroy(h->ev_out[b]);
+        }
+        cudaStreamDestroy(h->s_in);
+        cudaStreamDestroy(h->s_out);
+    }
     delete h;
     return MOE_OK;
 }
@@ -291,8 +308,10 @@ moe_status moe_init(const moe_config* cfg, moe_handle** out)
         ALLOC(s.hsf32, sizeof(float) * (size_t)s.Rmax * s.KB2);
     }
     ALLOC(s.err, sizeof(int32_t) * 4);
-    ALLOC(h->xbuf, sizeof(uint16_t) * (size_t)s.Tm * s.H);
-    ALLOC(h->ybuf, sizeof(uint16_t) * (size_t)s.Tm * s.H);
+    for (int b = 0; b < 2; ++b) {
+        ALLOC(h->xbuf[b], sizeof(uint16_t) * (size_t)s.Tm * s.H);
+        ALLOC(h->ybuf[b], sizeof(uint16_t) * (size_t)s.Tm * s.H);
+    }
 #undef ALLOC
     // padding rows of the activation / SwiGLU buffers are never written by a
     // forward; zero them once so every tile reads finite values
@@ -608,22 +627,68 @@ moe_status moe_sum_partials_bf16(const float* const* parts, int n_parts, size_t 
     return MOE_OK;
 }
 
-moe_status moe_forward_host(moe_handle* h, const uint16_t* x_host, int T, uint16_t* y_host, void* stream)
+// One host-buffer forward in staging slot b = calls % 2, on three streams:
+// the input copy on s_in (after the forward that last read slot b's input
+// buffer), the forward on `stream` (after the input copy, and after the
+// output copy that last read slot b's output buffer), the output copy on
+// s_out (after the forward).  So call i's input copy overlaps call i-1's
+// forward and call i-1's output copy overlaps call i's forward.
+static moe_status forward_host_enqueue(moe_handle* h, const uint16_t* x_host, int T, uint16_t* y_host, void* stream,
+                                       const char* who)
 {
-    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_forward_host: handle is NULL");
-    if (!h->loaded) return fail(h, MOE_ERR_NOT_LOADED, "moe_forward_host: weights not loaded");
-    if (T < 0 || T > h->s.Tm)
-        return fail(h, MOE_ERR_SHAPE, "moe_forward_host: T=%d outside [0, max_tokens=%d]", T, h->s.Tm);
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "%s: handle is NULL", who);
+    if (!h->loaded) return fail(h, MOE_ERR_NOT_LOADED, "%s: weights not loaded", who);
+    if (T < 0 || T > h->s.Tm) return fail(h, MOE_ERR_SHAPE, "%s: T=%d outside [0, max_tokens=%d]", who, T, h->s.Tm);
     if (T == 0) return MOE_OK;
-    if (!x_host || !y_host) return fail(h, MOE_ERR_INVALID_ARG, "moe_forward_host: x or y is NULL");
+    if (!x_host || !y_host) return fail(h, MOE_ERR_INVALID_ARG, "%s: x or y is NULL", who);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t bytes = (size_t)T * h->s.H * 2;
     CUDA_TRY(h, cudaSetDevice(h->cfg.device));
-    CUDA_TRY(h, cudaMemcpyAsync(h->xbuf, x_host, bytes, cudaMemcpyHostToDevice, st));
-    moe_status r = moe_forward(h, h->xbuf, T, h->ybuf, stream);
+    if (!h->host_ready) {
+        CUDA_TRY(h, cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking));
+        CUDA_TRY(h, cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking));
+        for (int b = 0; b < 2; ++b) {
+            CUDA_TRY(h, cudaEventCreateWithFlags(&h->ev_in[b], cudaEventDisableTiming));
+            CUDA_TRY(h, cudaEventCreateWithFlags(&h->ev_fwd[b], cudaEventDisableTiming));
+            CUDA_TRY(h, cudaEventCreateWithFlags(&h->ev_out[b], cudaEventDisableTiming));
+        }
+        h->host_ready = true;
+    }
+    const int b = h->host_calls & 1;
+    if (h->slot_used[b]) CUDA_TRY(h, cudaStreamWaitEvent(h->s_in, h->ev_fwd[b], 0));
+    CUDA_TRY(h, cudaMemcpyAsync(h->xbuf[b], x_host, bytes, cudaMemcpyHostToDevice, h->s_in));
+    CUDA_TRY(h, cudaEventRecord(h->ev_in[b], h->s_in));
+    CUDA_TRY(h, cudaStreamWaitEvent(st, h->ev_in[b], 0));
+    if (h->slot_used[b]) CUDA_TRY(h, cudaStreamWaitEvent(st, h->ev_out[b], 0));
+    moe_status r = moe_forward(h, h->xbuf[b], T, h->ybuf[b], stream);
     if (r != MOE_OK) return r;
-    CUDA_TRY(h, cudaMemcpyAsync(y_host, h->ybuf, bytes, cudaMemcpyDeviceToHost, st));
-    CUDA_TRY(h, cudaStreamSynchronize(st));
+    CUDA_TRY(h, cudaEventRecord(h->ev_fwd[b], st));
+    CUDA_TRY(h, cudaStreamWaitEvent(h->s_out, h->ev_fwd[b], 0));
+    CUDA_TRY(h, cudaMemcpyAsync(y_host, h->ybuf[b], bytes, cudaMemcpyDeviceToHost, h->s_out));
+    CUDA_TRY(h, cudaEventRecord(h->ev_out[b], h->s_out));
+    h->slot_used[b] = true;
+    ++h->host_calls;
+    return MOE_OK;
+}
+
+moe_status moe_forward_host(moe_handle* h, const uint16_t* x_host, int T, uint16_t* y_host, void* stream)
+{
+    moe_status r = forward_host_enqueue(h, x_host, T, y_host, stream, "moe_forward_host");
+    if (r != MOE_OK || T == 0) return r;
+    return moe_host_sync(h);
+}
+
+moe_status moe_forward_host_async(moe_handle* h, const uint16_t* x_host, int T, uint16_t* y_host, void* stream)
+{
+    return forward_host_enqueue(h, x_host, T, y_host, stream, "moe_forward_host_async");
+}
+
+moe_status moe_host_sync(moe_handle* h)
+{
+    if (!h) return fail(nullptr, MOE_ERR_INVALID_ARG, "moe_host_sync: handle is NULL");
+    if (!h->host_ready) return MOE_OK;
+    CUDA_TRY(h, cudaSetDevice(h->cfg.device));
+    CUDA_TRY(h, cudaStreamSynchronize(h->s_out));
     return MOE_OK;
 }
 
@@ -646,7 +711,8 @@ moe_status moe_debug_fill_workspace(moe_handle* h, int byte)
         {s.light_list, 4 * MT}, {s.heavy_list, 4 * MT}, {s.prow, 4 * Tm * K}, {s.aq, R * s.H},
         {s.asf, 4 * MT * s.KB1 * 128}, {s.hq, R * s.I}, {s.hsf, 4 * MT * s.KB2 * 128},
         {s.asf32, s.act_f32 ? 4 * R * s.KB1 : 0}, {s.hsf32, s.act_f32 ? 4 * R * s.KB2 : 0},
-        {s.obuf, 4 * R * s.H}, {h->xbuf, 2 * Tm * s.H}, {h->ybuf, 2 * Tm * s.H}};
+        {s.obuf, 4 * R * s.H}, {h->xbuf[0], 2 * Tm * s.H}, {h->ybuf[0], 2 * Tm * s.H},
+        {h->xbuf[1], 2 * Tm * s.H}, {h->ybuf[1], 2 * Tm * s.H}};
     for (const Buf& b : bufs)
         if (b.p && b.n) CUDA_TRY(h, cudaMemset(b.p, byte, b.n));
     CUDA_TRY(h, cudaDeviceSynchronize());

@@ -170,9 +170,23 @@ moe_status moe_forward_partial(moe_handle* h, const uint16_t* x, int T, float* y
 moe_status moe_sum_partials_bf16(const float* const* parts, int n_parts, size_t n, uint16_t* y, void* stream);
 
 /* Same layer with host buffers: copies x (host, [T][H] bf16) to the device,
- * runs moe_forward on `stream`, copies y back to y_host and waits for the
- * stream.  Pinned host memory gives the fastest copies. */
+ * runs moe_forward on `stream`, copies y back to y_host and waits until y_host
+ * holds the output.  Pinned host memory gives the fastest copies. */
 moe_status moe_forward_host(moe_handle* h, const uint16_t* x_host, int T, uint16_t* y_host, void* stream);
+
+/* The same without waiting: enqueues the input copy, the forward (on
+ * `stream`) and the output copy, and returns.  The handle keeps two device
+ * staging slots and two copy streams of its own, so the copies of one call
+ * overlap the forwards of the previous and next calls (a stream of batches
+ * runs at about the rate of its slowest engine: copy in, compute, copy out).
+ * x_host must stay unchanged and y_host untouched until the call's output has
+ * arrived: moe_host_sync waits for every call issued so far.  x_host and
+ * y_host must be pinned (page-locked) for the copies to run asynchronously.
+ * Issue the forwards of one handle on one stream (they share its
+ * workspace).  Errors of the enqueue are returned; device-side errors as for
+ * moe_forward. */
+moe_status moe_forward_host_async(moe_handle* h, const uint16_t* x_host, int T, uint16_t* y_host, void* stream);
+moe_status moe_host_sync(moe_handle* h);
 
 /* Debug getters for the last forward (they synchronise the device and copy
  * to HOST memory; T and k are those of that forward):

@@ -153,3 +153,24 @@ def test_forward_captures_in_a_cuda_graph():
     torch.cuda.synchronize()
     layer.check_device_error()
     assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), y_eager)
+
+
+def test_pipelined_host_calls_match_device_forwards():
+    """moe_forward_host_async: several batches of different sizes issued
+    back to back (copies overlapping the neighbouring forwards through two
+    staging slots), each into its own pinned output; after moe_host_sync
+    every output equals the device-buffer forward of the same batch."""
+    import torch
+    inp = synth.custom_inputs(300, 512, 16, 256, 8, seed=1301, bias="normal:0.5")
+    layer = make_layer(inp)
+    xs = [np.ascontiguousarray(inp.x[a:b]) for a, b in [(0, 300), (0, 1), (17, 117), (0, 300), (5, 264)]]
+    pinned_x = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs]
+    pinned_y = [torch.full_like(px, -1).pin_memory() for px in pinned_x]
+    for px, py in zip(pinned_x, pinned_y):
+        layer.forward_host_async(px, py)
+    layer.host_sync()
+    for x, py in zip(xs, pinned_y):
+        ref = layer.forward(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda())
+        torch.cuda.synchronize()
+        assert np.array_equal(py.numpy().view(np.uint16), ref.view(torch.int16).cpu().numpy().view(np.uint16))
+    layer.check_device_error()
