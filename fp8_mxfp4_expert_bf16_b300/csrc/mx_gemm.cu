@@ -249,16 +249,15 @@ __device__ __forceinline__ void store_rows_direct(uint32_t taddr, int ncols, int
 // accumulator columns of its 32 TMEM lanes (rows), in blocks of 32 columns.
 // Blocks 1.. are first copied to `stash` (TMEM columns outside the
 // accumulator, through registers), block 0 is read, and the accumulator is
-// released (arrive on `acc_empty`).  Then each block, from registers or
-// read back from the stash, is transposed across the warp with a five-step
-// butterfly of shuffles so that lane l holds column l of all 32 rows, and
-// stored one row per instruction (32 lanes x 4 B = one full 128-byte line,
-// instead of 32 rows' 16-byte pieces).  dst0 is row 0 of the warp's 32
-// rows, `live_rows` how many of them are valid, rows `row_stride` floats
-// apart.
+// released (arrive on `acc_empty`).  Each block is read with the 16-lane x
+// 256-bit shape, which gives four neighbouring threads 8 consecutive columns
+// of one row: every thread then stores 8-byte pieces, and each store
+// instruction of the warp fills whole 32-byte sectors of 8 rows (no
+// transposes across the warp).  dst0 is row 0 of the warp's 32 rows,
+// `live_rows` how many of them are valid, rows `row_stride` floats apart.
 template <int kCols>
-__device__ __forceinline__ void store_rows_transposed(uint32_t taddr, uint32_t stash, int live_rows, float* dst0,
-                                                      size_t row_stride, uint32_t acc_empty, int lane)
+__device__ __forceinline__ void store_rows_sectors(uint32_t taddr, uint32_t stash, int live_rows, float* dst0,
+                                                   size_t row_stride, uint32_t acc_empty, int lane)
 {
     if (live_rows > 0) {
 #pragma unroll 1
@@ -270,11 +269,14 @@ __device__ __forceinline__ void store_rows_transposed(uint32_t taddr, uint32_t s
             tmem_st_wait();
         }
     }
+    const int r0 = lane >> 2, c0 = 2 * (lane & 3);
 #pragma unroll 1
     for (int b = 0; b < kCols / 32; ++b) {
-        uint32_t a[32];
+        uint32_t lo[16], hi[16];   // rows 0..15, rows 16..31 of the block
+        const uint32_t src = b == 0 ? taddr : stash + 32u * (b - 1);
         if (live_rows > 0) {
-            tmem_ld32(b == 0 ? taddr : stash + 32u * (b - 1), a);
+            tmem_ld_16x256b_x4(src, lo);
+            tmem_ld_16x256b_x4(src + (16u << 16), hi);
             tmem_ld_wait();
         }
         if (b == 0) {
@@ -284,21 +286,18 @@ __device__ __forceinline__ void store_rows_transposed(uint32_t taddr, uint32_t s
         }
         if (live_rows <= 0) continue;
 #pragma unroll
-        for (int sft = 16; sft >= 1; sft >>= 1) {
-            const bool upper = (lane & sft) != 0;
+        for (int j = 0; j < 4; ++j) {
+            const int col = 32 * b + 8 * j + c0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                if ((i & sft) == 0) {
-                    const uint32_t send = upper ? a[i] : a[i + sft];
-                    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, sft);
-                    if (upper) a[i] = recv;
-                    else a[i + sft] = recv;
-                }
+            for (int q = 0; q < 4; ++q) {   // rows r0, r0 + 8, r0 + 16, r0 + 24
+                const int r = r0 + 8 * q;
+                const uint32_t* v = q < 2 ? lo : hi;
+                const int k = 4 * j + 2 * (q & 1);
+                if (r < live_rows)
+                    *reinterpret_cast<float2*>(dst0 + (size_t)r * row_stride + col) =
+                        make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1]));
             }
         }
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < live_rows) dst0[(size_t)j * row_stride + 32 * b + lane] = __uint_as_float(a[j]);
     }
 }
 
@@ -801,11 +800,11 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 if (kLight)
                     store_rows_direct(taddr, half_cols, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
                 else if (half_cols == 128)
-                    store_rows_transposed<128>(taddr, tl + kStashHeavyCol + 96u * hw, live, dst0, (size_t)args.H,
-                                               smem_u32(&pc.acc_empty), lane);
+                    store_rows_sectors<128>(taddr, tl + kStashHeavyCol + 96u * hw, live, dst0, (size_t)args.H,
+                                            smem_u32(&pc.acc_empty), lane);
                 else
-                    store_rows_transposed<64>(taddr, tl + kStashHeavyCol + 96u * hw, live, dst0, (size_t)args.H,
-                                              smem_u32(&pc.acc_empty), lane);
+                    store_rows_sectors<64>(taddr, tl + kStashHeavyCol + 96u * hw, live, dst0, (size_t)args.H,
+                                           smem_u32(&pc.acc_empty), lane);
             }
         }
     }

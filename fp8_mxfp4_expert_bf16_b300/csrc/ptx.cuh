@@ -261,6 +261,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "r"(taddr));
 }
 
+// 16 TMEM lanes x 256 bits, 4 times (32 columns): thread t of the warp gets,
+// for repetition j, r[4j], r[4j+1] = lane L + t/4, columns 8j + 2(t%4) + {0, 1}
+// and r[4j+2], r[4j+3] = lane L + 8 + t/4, the same columns (L = the lane of
+// taddr): four neighbouring threads hold 8 consecutive columns of one lane.
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Each thread of the warp writes 16 consecutive 32-bit columns of its TMEM lane.
