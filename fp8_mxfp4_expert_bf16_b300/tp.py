@@ -31,11 +31,16 @@ class TensorParallelMoE:
         self.layer = layer
         self.group = group
         self._round = round_bf16 or (lambda y32, y: sum_partials_bf16([y32], y))
+        self._y32 = None   # the partial-output buffer, reused while T stays the same
 
     def forward(self, x, y=None):
         """x: bf16 [T, H] (the same on every rank) -> y: bf16 [T, H] (the same on every rank)."""
+        import torch
         import torch.distributed as dist
-        y32 = self.layer.forward_partial(x)
+        T, H = x.shape
+        if self._y32 is None or tuple(self._y32.shape) != (T, H) or self._y32.device != x.device:
+            self._y32 = torch.empty((T, H), dtype=torch.float32, device=x.device)
+        y32 = self.layer.forward_partial(x, self._y32)
         if dist.is_available() and dist.is_initialized() and dist.get_world_size(self.group) > 1:
             dist.all_reduce(y32, op=dist.ReduceOp.SUM, group=self.group)
         return self._round(y32, y)
