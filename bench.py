@@ -13,7 +13,8 @@ line.  Default (``--config all``): the line is the largest single-GPU
 workload, the Pro-shaped prefill with skewed routing (T=16384, H=6144,
 E=384 top-8, I=2048); the other four workloads ride in its ``per_config``
 key, each with its own timing, roofline, stage times, routing statistics,
-end-to-end rate, CPU baseline and clocks.  The block-scaled tensor-core
+end-to-end rate, CPU baseline and clocks, and so do the Flash decode batch in
+the fp32-scale activation mode and with the fp8 expert format.  The block-scaled tensor-core
 rate the prefill rooflines divide by is measured in the same run
 (``block_scaled_peak``).
 
@@ -616,6 +617,15 @@ def run_gpu(args):
     for name in others:
         entries[name] = run_config(args, synth.CONFIGS[name], device, stream, P, None, ws, rank, dist,
                                    0 if args.no_cpu_baseline else args.ref_budget / 4)
+    # the layer's two other formats on the Flash decode batch: fp32 activation
+    # block scales, and the fp8 (V2.5) expert format
+    if others and args.act_scale == "e8m0" and args.weights == "mxfp4":
+        import copy
+        for key, val in [("act_scale", "f32"), ("weights", "fp8")]:
+            a2 = copy.copy(args)
+            setattr(a2, key, val)
+            entries[f"flash-decode/{key}={val}"] = run_config(a2, synth.CONFIGS["flash-decode"], device, stream, P,
+                                                               None, ws, rank, dist, 0)
     peak = sustained_block_scaled_peak(device, burst, args.peak_seconds)
     if rank == 0:
         for ent in [e] + list(entries.values()):

@@ -6,7 +6,7 @@
 // section "Why Are the V2.6 Files Half the Size of V2.5?" (router weights in
 // BF16).
 //
-// One CTA per (128-token tile, N-expert tile), N = 64 or 128.  Warp 0 lane 0
+// One CTA per (N-expert tile, 128-token tile), N = 64 or 128.  Warp 0 lane 0
 // streams 64-wide K slices of x and Wr with TMA (128-byte swizzle) through a
 // 4-stage ring; warp 1 lane 0 issues tcgen05.mma kind::f16 (128 x N x 16)
 // into TMEM; then all four warps read their 32 TMEM lanes (tokens) and write
@@ -74,7 +74,9 @@ __global__ void __launch_bounds__(128, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     RouterCtl* ctl = reinterpret_cast<RouterCtl*>(smem + kRBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x, nt = blockIdx.y;
+    // the expert tile is the fastest grid dimension: the CTAs that share a
+    // 128-token tile of x run side by side, so x comes from HBM about once
+    const int nt = blockIdx.x, mt = blockIdx.y;
     const int kb0 = blockIdx.z * KB;
 
     if (threadIdx.x == 0) {
@@ -200,7 +202,7 @@ int router_split(int T, int H)
 cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, cudaStream_t st, int ksplit)
 {
     const int N = router_tile_n(T);
-    dim3 grid((T + 127) / 128, (s.E + N - 1) / N, ksplit);
+    dim3 grid((s.E + N - 1) / N, (T + 127) / 128, ksplit);
     return launch_kernel(k_router_tc, grid, dim3(128), kRSmemBytes, st, s.pdl, tmX, N == 64 ? s.tm_wr64 : s.tm_wr128,
                          s.lb, s.logits, ksplit > 1 ? s.logit_part : nullptr, T, s.E, s.H / 64 / ksplit, N, s.err);
 }
