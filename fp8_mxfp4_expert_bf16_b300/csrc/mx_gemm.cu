@@ -34,6 +34,14 @@
 //               be double-buffered) is released early by parking columns in
 //               the TMEM columns the phase leaves free: the up half (gate/up)
 //               or three of each warp's four column blocks (down, heavy).
+// The promotion modes (fp32 activation scales, or fp8 experts with fp32
+// block scales) cannot fold their scales into the MMA: each K-step's product
+// lands in TMEM as a separate partial that the epilogue scales and adds in
+// registers.  Heavy m-tiles use a ring of three 128-column partials (one per
+// K-step and weight half); light m-tiles swap the operands, weights as the
+// 128-row A operand and the 16 token rows as B, so that a partial is only 16
+// columns wide and a ring unit carries four K-steps of both halves (see
+// kSwN).
 // Programmatic dependent launch: the kernel may start while the previous
 // kernel of the forward (which writes the activations) is still running.
 // Before waiting for it, the producer streams what does not depend on it:
@@ -86,19 +94,48 @@ constexpr uint32_t kBHalfTxBytes = 128 * 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;      // accumulator: 256 fp32 columns
 constexpr uint32_t kSFCol = 256;     // stage s: SFA at kSFCol + 16 s (4 cols), SFB at +8 (8 cols)
-constexpr uint32_t kSFUnitCol = 352; // promotion modes: a constant unit scale chunk, twice (8 cols)
 constexpr uint32_t kStashHeavyCol = 320;  // down epilogue, heavy phase: 3 x 32 columns per warp parked here
 constexpr uint32_t kStashCol = 384;  // gate/up epilogue: the tile's up columns parked here (128 cols)
-// The two stashes are used only by the epilogues of the E8M0 (non-promotion)
-// instantiations; the unit chunk at kSFUnitCol, inside the heavy stash's
-// range, only by the promotion ones (the epilogue code paths that park
-// columns assert this where they are compiled).
-static_assert(kSFUnitCol + 8 <= kStashCol, "unit scale chunk overlaps the gate/up stash");
-static_assert(kSFUnitCol >= kSFCol + 16 * Shape<true>::kStages, "unit scale chunk overlaps the light ring's scales");
 static_assert(kSFCol + 16 * Shape<false>::kStages <= kStashHeavyCol && kStashHeavyCol + 2 * 96 <= kTmemCols,
               "heavy-phase down stash overlaps the heavy ring's scale chunks");
 static_assert(kSFCol + 16 * Shape<true>::kStages <= kStashCol && kStashCol + 128 <= kTmemCols,
               "gate/up stash overlaps the light ring's scale chunks");
+// The promotion modes (fp32 activation scales, or fp8 experts with fp32
+// block scales) lay TMEM out differently: a ring of kPBufs partial products
+// of one 128-row half of a tile's weight rows and one K-step (128 fp32
+// columns each), so that the MMAs of the next half-steps run while the
+// epilogue folds the previous ones into its registers; then the stages'
+// scale chunks and a constant unit chunk.
+constexpr int kPBufs = 3;
+constexpr uint32_t kPBufCol = 0;
+constexpr uint32_t kPSFCol = kPBufCol + 128 * kPBufs;   // stage s: SFA at + 16 s (4 cols), SFB at + 8 (8 cols)
+constexpr uint32_t kPUnitCol = kPSFCol + 16 * 6;        // E8M0 1.0 chunk, twice (8 cols)
+static_assert(Shape<true>::kStages <= 6 && Shape<false>::kStages <= 6, "promotion-mode scale chunks");
+static_assert(kPUnitCol + 8 <= kTmemCols, "promotion-mode TMEM layout");
+// Light m-tiles (at most 16 valid rows) put the tokens on the MMA's N side:
+// the weights are the 128-row A operand (one MMA group per 128-row half of
+// the tile) and the 16 activation rows the B operand, so an MMA computes the
+// 128 x 16 outputs that are used instead of 128 x 256.  An accumulator is
+// then 16 TMEM columns (tokens) by 128 lanes (weight rows):
+//   E8M0 activations: one 32-column pair (both halves) per tile, a ring of
+//     kSwTBufs tiles, read once at the tile's end;
+//   promotion modes: one 16-column partial per (K-step, half), kSwG K-steps
+//     of both halves per unit of a ring of kSwPBufs units, each partial
+//     folded into registers with its fp32 scale(s).
+constexpr int kSwN = 16;                 // MMA N: the light m-tile's rows
+constexpr int kSwRingCols = 384;         // TMEM columns of the accumulator ring
+constexpr int kSwTBufs = 8;
+constexpr int kSwG = 4;                  // promotion: K-steps per ring unit (both halves, 32 columns each)
+constexpr int kSwPBufs = kSwRingCols / (32 * kSwG);
+constexpr uint32_t kSwBufCol = 0;
+constexpr uint32_t kSwSFCol = kSwRingCols;   // stage s: weight scales (half 0, half 1) at + 16 s, + 4; activation scales at + 8
+constexpr uint32_t kSwUnitCol = kSwSFCol + 16 * 6;   // E8M0 1.0 chunk (4 cols)
+constexpr int kMaxPBufs = 8;            // barriers of the accumulator rings (all three kinds)
+static_assert(kLightRows == kSwN, "light m-tile rows");
+static_assert(kSwTBufs * 2 * kSwN <= (int)kSwSFCol && kSwPBufs * kSwG * 2 * kSwN <= (int)kSwSFCol,
+              "light accumulator ring");
+static_assert(kSwSFCol + 16 * Shape<true>::kStages <= kSwUnitCol && kSwUnitCol + 4 <= kTmemCols, "light TMEM layout");
+static_assert(kPBufs <= kMaxPBufs && kSwPBufs <= kMaxPBufs && kSwTBufs <= kMaxPBufs, "accumulator ring barriers");
 constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
 constexpr int kThreads = 32 * (2 + kEpiWarps);     // TMA warp, MMA warp, epilogue warps
 
@@ -140,13 +177,13 @@ struct PhaseCtl {
     uint64_t acc_empty;
     uint64_t drain;
     uint64_t red_full[2];
-    uint64_t pfull;               // fp32-scale mode: a K-step's partial product is in TMEM
-    uint64_t pempty;              // fp32-scale mode: every epilogue warp has read it
+    uint64_t pfull[kMaxPBufs];    // accumulator ring (promotion partials, light tiles): buffer b is in TMEM
+    uint64_t pempty[kMaxPBufs];   // every epilogue warp has read buffer b
     float red[2][8][32];          // per-warp row amax halves, double-buffered by tile parity
 };
 
 struct GemmCtl {
-    uint32_t unit_sf[128];        // fp32-scale mode: E8M0 1.0 in every byte (a tcgen05.cp chunk)
+    uint32_t unit_sf[128];        // promotion modes: E8M0 1.0 in every byte (a tcgen05.cp chunk)
     PhaseCtl<Shape<true>::kStages> light;
     PhaseCtl<Shape<false>::kStages> heavy;
     uint32_t tmem_base;
@@ -176,8 +213,10 @@ __device__ __forceinline__ void init_phase(PhaseCtl<kStages>& pc)
     mbar_init(smem_u32(&pc.red_full[0]), kEpiWarps);
     mbar_init(smem_u32(&pc.red_full[1]), kEpiWarps);
     mbar_init(smem_u32(&pc.drain), 1);
-    mbar_init(smem_u32(&pc.pfull), 1);
-    mbar_init(smem_u32(&pc.pempty), kEpiWarps);
+    for (int b = 0; b < kMaxPBufs; ++b) {
+        mbar_init(smem_u32(&pc.pfull[b]), 1);
+        mbar_init(smem_u32(&pc.pempty[b]), kEpiWarps);
+    }
 }
 
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
@@ -313,11 +352,311 @@ struct TileSeq {
     __device__ __forceinline__ int nt_of(int t) const { return t - (t / per_mt) * per_mt; }
 };
 
+// 8-bit e4m3 code of one value (round to nearest even, saturating)
+__device__ __forceinline__ uint32_t e4m3x1(float v)
+{
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(v, 0.0f), __NV_SATFINITE, __NV_E4M3) & 0xFFu;
+}
+
+// v[sel] for a warp-uniform or per-lane index, without local memory
+__device__ __forceinline__ float pick8(const float (&v)[8], int sel)
+{
+    float r = v[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) r = sel == j ? v[j] : r;
+    return r;
+}
+
+// MMA issuer of a light phase with the tokens on the N side (see kSwN).
+template <int kMode, bool kF32S, bool kW8>
+__device__ __forceinline__ void light_mma(uint8_t* smem, GemmCtl* g, PhaseCtl<Shape<true>::kStages>& pc,
+                                          uint32_t tmem, const GemmArgs& args, const TileSeq& ts, int lane)
+{
+    using S = Shape<true>;
+    constexpr int kStages = S::kStages, kStageStride = S::kStageStride;
+    constexpr bool kPromo = kF32S || kW8;
+    const volatile int* abrt = &g->abort;
+    const int KB = args.KB, halves = args.halves;
+    const uint32_t idesc = idesc_mxf8f6f4(128, kSwN, kW8 ? kTypeE4M3 : kTypeE2M1, kTypeE4M3);
+    const uint32_t id1 = idesc_with_sf_id(idesc, 1, 1), id2 = idesc_with_sf_id(idesc, 2, 2),
+                   id3 = idesc_with_sf_id(idesc, 3, 3);
+    const uint32_t s0 = smem_u32(smem);
+    const uint64_t wd0 = desc_kmajor_sw128(s0 + S::kBOff);   // weight rows: the A operand
+    const uint64_t xd0 = desc_kmajor_sw128(s0);              // activation rows: the B operand
+    const uint64_t sfw0 = desc_sf_chunk(s0 + S::kSFBOff), sfx0 = desc_sf_chunk(s0 + S::kSFAOff);
+    const uint32_t full0 = smem_u32(&pc.full[0]), empty0 = smem_u32(&pc.empty[0]);
+    if constexpr (kPromo) tmem_cp_32x128b_warpx4_elect(tmem + kSwUnitCol, desc_sf_chunk(smem_u32(g->unit_sf)));
+    int s = 0;
+    uint32_t ph = 0, doff = 0;
+    int b = 0;             // accumulator ring position: partial (promotion) or tile (E8M0)
+    uint32_t pph = 0;      // its fill count's parity
+    bool wrapped = false;  // every buffer of the ring has been filled once
+    bool ok = true;
+    // take the ring's next buffer once the epilogue has read its previous contents
+    auto acquire = [&](int nbufs, int where, int& idx) {
+        if (wrapped && !__all_sync(~0u, mbar_wait(smem_u32(&pc.pempty[b]), pph ^ 1u, abrt))) {
+            if (lane == 0) raise_error(g, args.err, where);
+            return false;
+        }
+        idx = b;
+        if (++b == nbufs) {
+            b = 0;
+            pph ^= 1u;
+            wrapped = true;
+        }
+        return true;
+    };
+    for (int tile = ts.first; tile < ts.total && ok; tile += ts.step) {
+        int ub = 0;   // this tile's (E8M0) or this unit's (promotion) accumulator buffer
+        if constexpr (!kPromo) {
+            if (!acquire(kSwTBufs, 13, ub)) break;
+            tc_fence_after();
+        }
+        for (int kb = 0; kb < KB && ok; ++kb) {
+            const int g_in = kPromo ? kb % kSwG : 0;   // K-step within the unit
+            if (kPromo && g_in == 0) {
+                if (!acquire(kSwPBufs, 15, ub)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!__all_sync(~0u, mbar_wait(full0 + 8u * s, ph, abrt))) {
+                if (lane == 0) raise_error(g, args.err, 14);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sfw_t = tmem + kSwSFCol + 16u * s, sfx_t = sfw_t + 8u;
+            if constexpr (!kW8) {
+                tmem_cp_32x128b_warpx4_elect(sfw_t, sfw0 + doff);
+                if (halves == 2) tmem_cp_32x128b_warpx4_elect(sfw_t + 4u, sfw0 + doff + (512 >> 4));
+            }
+            if constexpr (!kF32S) tmem_cp_32x128b_warpx4_elect(sfx_t, sfx0 + doff);
+            const uint32_t sfb = kF32S ? tmem + kSwUnitCol : sfx_t;
+            // promotion: the K-step's partials (one per half) in slot g_in of the
+            // unit; E8M0: the tile's accumulator pair
+            const uint32_t d0 = kPromo ? tmem + kSwBufCol + 2u * kSwN * (uint32_t)(kSwG * ub + g_in)
+                                       : tmem + kSwBufCol + 2u * kSwN * (uint32_t)ub;
+            for (int h = 0; h < halves; ++h) {
+                // the half's 128 weight rows start 16 KB into the stage's weight tile
+                const uint32_t d = d0 + (uint32_t)kSwN * (uint32_t)h;
+                const uint32_t sfa = kW8 ? tmem + kSwUnitCol : sfw_t + 4u * (uint32_t)h;
+                const uint64_t ad = wd0 + doff + (uint64_t)h * (16384 >> 4), bd = xd0 + doff;
+                mma_mxf8f6f4_elect(d, ad, bd, idesc, sfa, sfb, (!kPromo && kb != 0) ? 1u : 0u);
+                mma_mxf8f6f4_elect(d, ad + 2, bd + 2, id1, sfa, sfb, 1u);
+                mma_mxf8f6f4_elect(d, ad + 4, bd + 4, id2, sfa, sfb, 1u);
+                mma_mxf8f6f4_elect(d, ad + 6, bd + 6, id3, sfa, sfb, 1u);
+            }
+            if (kPromo && (g_in == kSwG - 1 || kb == KB - 1)) tc_commit_elect(smem_u32(&pc.pfull[ub]));
+            tc_commit_elect(empty0 + 8u * s);
+            if (++s == kStages) {
+                s = 0;
+                ph ^= 1u;
+                doff = 0;
+            } else {
+                doff += kStageStride >> 4;
+            }
+        }
+        if constexpr (!kPromo) {
+            if (ok) tc_commit_elect(smem_u32(&pc.pfull[ub]));
+        }
+    }
+    // all MMAs of this warp complete before the ring or TMEM is reused
+    int zero = 0;
+    tc_commit_elect(smem_u32(&pc.drain));
+    if (!mbar_wait(smem_u32(&pc.drain), 0u, &zero) && lane == 0) raise_error(g, args.err, 5);
+}
+
+// Epilogue of a light phase with the tokens on the N side.  Warp (q, hw):
+// weight rows 32q .. 32q+31 of each half (its TMEM lane quarter), tokens
+// 8hw .. 8hw+7 (TMEM columns); acc[h][j] = output of weight row 32q + lane of
+// half h for token 8hw + j.  Tokens at or past the m-tile's valid rows hold
+// padding or stale shared memory (any bit pattern) and are never used.
+template <int kMode, bool kF32S, bool kW8>
+__device__ __forceinline__ void light_epilogue(GemmCtl* g, PhaseCtl<Shape<true>::kStages>& pc, uint32_t tmem,
+                                               const GemmArgs& args, const int32_t* list, const TileSeq& ts,
+                                               int warp, int lane)
+{
+    constexpr bool kPromo = kF32S || kW8;
+    const volatile int* abrt = &g->abort;
+    const int ew = warp - 2, q = warp & 3, hw = ew >> 2;
+    const int KB = args.KB, halves = args.halves;
+    const int tok0 = 8 * hw;
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + kSwBufCol + (uint32_t)tok0;
+    int b = 0;
+    uint32_t pph = 0;
+    auto ring_take = [&](int where) {
+        if (!mbar_wait(smem_u32(&pc.pfull[b]), pph, abrt)) {
+            raise_error(g, args.err, where);
+            return false;
+        }
+        tc_fence_after();
+        return true;
+    };
+    auto ring_release = [&](int nbufs) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&pc.pempty[b]));
+        if (++b == nbufs) {
+            b = 0;
+            pph ^= 1u;
+        }
+    };
+    // activation scales come from the previous kernel (quantisation, or the
+    // gate/up GEMM): wait for it before the first read
+    if (kF32S) griddep_wait();
+    int tcount = 0;
+    for (int tile = ts.first; tile < ts.total; tile += ts.step, ++tcount) {
+        const int mt = list[ts.mt_index(tile)], nt = ts.nt_of(tile);
+        const int rows = args.mtile_rows[mt];
+        const bool warp_live = tok0 < rows;
+        float acc[2][8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[0][j] = acc[1][j] = 0.0f;
+        bool ok = true;
+        if constexpr (kPromo) {
+            // acc += s_token * s_weight_block * partial, in K order
+            const float* wsa = nullptr;
+            const float* wsb = nullptr;
+            if constexpr (kW8) {
+                const int e = args.mtile_expert[mt];
+                const int RB = kMode == 0 ? 2 * (args.I / 128) : args.H / 128;
+                const int rba = kMode == 0 ? nt : nt * halves;
+                const int rbb = kMode == 0 ? args.I / 128 + nt : rba + (halves == 2 ? 1 : 0);
+                wsa = args.ws + ((size_t)e * RB + rba) * KB;
+                wsb = args.ws + ((size_t)e * RB + rbb) * KB;
+            }
+            const float* xs = kF32S ? args.as32 + (size_t)(mt * kBM + tok0) * KB : nullptr;
+            for (int kb0 = 0; kb0 < KB && ok; kb0 += kSwG) {
+                const int n_in = min(kSwG, KB - kb0);   // K-steps in this unit
+                // the unit's scales: the tokens' fp32 activation scales and the
+                // weight blocks' scales of its K-steps (loading them a unit ahead
+                // measured no faster)
+                float sx[kSwG][8], wa[kSwG], wb[kSwG];
+#pragma unroll
+                for (int gg = 0; gg < kSwG; ++gg) {
+                    const int kb = kb0 + gg;
+                    const bool in = gg < n_in;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        sx[gg][j] = (kF32S && in && tok0 + j < rows) ? xs[(size_t)j * KB + kb] : 1.0f;
+                    wa[gg] = (kW8 && in) ? wsa[kb] : 1.0f;
+                    wb[gg] = (kW8 && in) ? wsb[kb] : 1.0f;
+                }
+                if (!ring_take(16)) {
+                    ok = false;
+                    break;
+                }
+                if (warp_live) {
+                    uint32_t pv[kSwG][2][8];
+                    const uint32_t src = tl + 2u * kSwN * (uint32_t)(kSwG * b);
+#pragma unroll
+                    for (int gg = 0; gg < kSwG; ++gg) {
+                        if (gg < n_in) {
+                            tmem_ld8(src + 2u * kSwN * gg, pv[gg][0]);
+                            if (halves == 2) tmem_ld8(src + 2u * kSwN * gg + kSwN, pv[gg][1]);
+                        }
+                    }
+                    tmem_ld_wait();
+                    // K order: K-step kb0 + gg, then the next
+#pragma unroll
+                    for (int gg = 0; gg < kSwG; ++gg) {
+                        if (gg < n_in) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                acc[0][j] = fmaf(sx[gg][j] * wa[gg], __uint_as_float(pv[gg][0][j]), acc[0][j]);
+                                if (halves == 2)
+                                    acc[1][j] = fmaf(sx[gg][j] * wb[gg], __uint_as_float(pv[gg][1][j]), acc[1][j]);
+                            }
+                        }
+                    }
+                }
+                ring_release(kSwPBufs);
+            }
+        } else {
+            if (!ring_take(16)) break;
+            if (warp_live) {
+                uint32_t p0[8], p1[8];
+                tmem_ld8(tl + 2u * kSwN * (uint32_t)b, p0);
+                if (halves == 2) tmem_ld8(tl + 2u * kSwN * (uint32_t)b + kSwN, p1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    acc[0][j] = __uint_as_float(p0[j]);
+                    acc[1][j] = halves == 2 ? __uint_as_float(p1[j]) : 0.0f;
+                }
+            }
+            ring_release(kSwTBufs);
+        }
+        if (!ok) break;
+        const int i = 32 * q + lane;   // weight row within each half
+        if constexpr (kMode == 0) {
+            // h = silu(g) * u per token, then the token's 1 x 128 block of h
+            // (this n-tile's 128 middle columns: 4 lane quarters x 32 lanes)
+            // re-quantised to e4m3
+            float hv[8], am[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const bool live = tok0 + j < rows;
+                const float gf = live ? acc[0][j] : 0.0f;
+                const float uf = live ? acc[1][j] : 0.0f;
+                hv[j] = __fdividef(gf, 1.0f + __expf(-gf)) * uf;
+                float m = fabsf(hv[j]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(~0u, m, o));
+                am[j] = m;
+            }
+            const int p = tcount & 1;
+            if (lane < 8) pc.red[p][ew][lane] = pick8(am, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&pc.red_full[p]));
+            if (!mbar_wait(smem_u32(&pc.red_full[p]), (uint32_t)(tcount >> 1) & 1u, abrt)) {
+                raise_error(g, args.err, 17);
+                break;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                am[j] = fmaxf(fmaxf(pc.red[p][4 * hw][j], pc.red[p][4 * hw + 1][j]),
+                              fmaxf(pc.red[p][4 * hw + 2][j], pc.red[p][4 * hw + 3][j]));
+            uint8_t* hcol = args.hq + (size_t)(mt * kBM + tok0) * args.I + nt * 128 + i;
+            if constexpr (!kF32S) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int ex = act_block_exponent(am[j]);
+                    if (tok0 + j < rows) hcol[(size_t)j * args.I] = (uint8_t)e4m3x1(hv[j] * __int_as_float((127 - ex) << 23));
+                }
+                if (q == 0 && lane < 8 && tok0 + lane < rows)
+                    args.hsf[sf_word_index(mt, nt, args.I / 128, tok0 + lane)] =
+                        (uint32_t)(act_block_exponent(pick8(am, lane)) + 127) * 0x01010101u;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float s2 = __fdiv_rn(am[j], 448.0f);
+                    if (tok0 + j < rows) hcol[(size_t)j * args.I] = (uint8_t)(am[j] > 0.0f ? e4m3x1(__fdiv_rn(hv[j], s2)) : 0u);
+                }
+                if (q == 0 && lane < 8 && tok0 + lane < rows)
+                    args.hs32[(size_t)(mt * kBM + tok0 + lane) * (args.I / 128) + nt] = __fdiv_rn(pick8(am, lane), 448.0f);
+            }
+        } else {
+            // fp32 expert-output rows: for each token, the warp's 32 lanes
+            // store 32 consecutive features
+            float* ocol = args.obuf + (size_t)(mt * kBM + tok0) * args.H + (size_t)nt * (128 * halves) + i;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (h < halves) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (tok0 + j < rows) ocol[(size_t)j * args.H + 128 * h] = acc[h][j];
+                }
+        }
+    }
+}
+
 // One phase (the light or the heavy m-tile list) of the grouped GEMM.  Every
 // role drains its own work before returning: the producer waits until its
 // copies have landed, the MMA issuer until its MMAs have completed, the
 // epilogue has read its last accumulator.
-template <int kMode, bool kLight, bool kF32S, bool kW8>
+template <int kMode, bool kLight, bool kF32S, bool kW8, bool kSwap = false>
 __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<Shape<kLight>::kStages>& pc,
                                            uint32_t tmem, const CUtensorMap* tmA0, const CUtensorMap* tmA1,
                                            const CUtensorMap* tmA2, const CUtensorMap* tmW, const GemmArgs& args,
@@ -424,6 +763,9 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 if (issued[s] && !mbar_wait(smem_u32(&pc.full[s]), last_phase[s], &zero))
                     raise_error(g, args.err, 2);
         }
+    } else if (warp == 1 && kSwap) {
+        static_assert(!kSwap || kLight, "tokens on the N side: light m-tiles only");
+        if constexpr (kSwap) light_mma<kMode, kF32S, kW8>(smem, g, pc, tmem, args, ts, lane);
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         // The loops run on the whole warp (one elected lane issues each
@@ -458,45 +800,65 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 }
             };
             if constexpr (kF32S || kW8) {
-                // One partial product per K-step, handed to the epilogue, which
-                // folds the fp32 scales in (the rows' activation scales and / or
-                // the weights' block scales; in the MMA those are unit E8M0
-                // chunks); the next K-step's MMAs wait until every epilogue
-                // warp has read it.
+                // One partial product per K-step and 128-row half of the
+                // weight tile, into the next buffer of the partial ring, handed
+                // to the epilogue, which folds the fp32 scales in (the rows'
+                // activation scales and / or the weights' block scales; in the
+                // MMA those are unit E8M0 chunks).  A buffer is refilled once
+                // every epilogue warp has read its previous partial.
+                const uint32_t idh = idesc_mxf8f6f4(128, 128, kTypeE4M3, kW8 ? kTypeE4M3 : kTypeE2M1);
+                const uint32_t idh1 = idesc_with_sf_id(idh, 1, 1), idh2 = idesc_with_sf_id(idh, 2, 2),
+                               idh3 = idesc_with_sf_id(idh, 3, 3);
                 const uint64_t unit = desc_sf_chunk(smem_u32(g->unit_sf));
-                tmem_cp_32x128b_warpx4_elect(tmem + kSFUnitCol, unit);
-                tmem_cp_32x128b_warpx4_elect(tmem + kSFUnitCol + 4u, unit);
-                int ks = 0;
+                tmem_cp_32x128b_warpx4_elect(tmem + kPUnitCol, unit);
+                tmem_cp_32x128b_warpx4_elect(tmem + kPUnitCol + 4u, unit);
+                int b = 0;            // partial buffer of the next half-step
+                uint32_t pph = 0;     // its fill count's parity
+                bool wrapped = false; // every buffer has been filled once
                 for (int tile = ts.first; tile < ts.total && ok; tile += ts.step) {
-                    for (int kb = 0; kb < KB; ++kb, ++ks) {
+                    for (int kb = 0; kb < KB && ok; ++kb) {
                         if (!__all_sync(~0u, mbar_wait(full0 + 8u * s, ph, abrt))) {
                             if (lane == 0) raise_error(g, args.err, 8);
                             ok = false;
                             break;
                         }
-                        if (ks > 0 && !__all_sync(~0u, mbar_wait(smem_u32(&pc.pempty), (uint32_t)(ks - 1) & 1u, abrt))) {
-                            if (lane == 0) raise_error(g, args.err, 9);
-                            ok = false;
-                            break;
-                        }
                         tc_fence_after();
-                        uint32_t sfa_t = tmem + kSFUnitCol, sfb_t = tmem + kSFUnitCol;
+                        uint32_t sfa_t = tmem + kPUnitCol, sfb_t = tmem + kPUnitCol;
                         if constexpr (!kF32S) {
-                            sfa_t = tmem + kSFCol + 16u * s;
+                            sfa_t = tmem + kPSFCol + 16u * s;
                             tmem_cp_32x128b_warpx4_elect(sfa_t, sfad0 + doff);
                         }
                         if constexpr (!kW8) {
-                            sfb_t = tmem + kSFCol + 16u * s + 8u;
+                            sfb_t = tmem + kPSFCol + 16u * s + 8u;
                             tmem_cp_32x128b_warpx4_elect(sfb_t, sfbd0 + doff);
                             if (two) tmem_cp_32x128b_warpx4_elect(sfb_t + 4u, sfbd0 + doff + (512 >> 4));
                         }
-                        const uint64_t ad = ad0 + doff, bd = bd0 + doff;
-                        mma_mxf8f6f4_elect(acc, ad, bd, idesc, sfa_t, sfb_t, 0u);
-                        mma_mxf8f6f4_elect(acc, ad + 2, bd + 2, id1, sfa_t, sfb_t, 1u);
-                        mma_mxf8f6f4_elect(acc, ad + 4, bd + 4, id2, sfa_t, sfb_t, 1u);
-                        mma_mxf8f6f4_elect(acc, ad + 6, bd + 6, id3, sfa_t, sfb_t, 1u);
+                        for (int h = 0; h < args.halves; ++h) {
+                            if (wrapped &&
+                                !__all_sync(~0u, mbar_wait(smem_u32(&pc.pempty[b]), pph ^ 1u, abrt))) {
+                                if (lane == 0) raise_error(g, args.err, 9);
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t pacc = tmem + kPBufCol + 128u * (uint32_t)b;
+                            // the half's 128 weight rows start 16 KB into the stage's weight tile;
+                            // its scale chunk is the half's 4 columns of the stage's SFB
+                            const uint64_t ad = ad0 + doff, bd = bd0 + doff + (uint64_t)h * (16384 >> 4);
+                            const uint32_t sfb_h = kW8 ? sfb_t : sfb_t + 4u * (uint32_t)h;
+                            mma_mxf8f6f4_elect(pacc, ad, bd, idh, sfa_t, sfb_h, 0u);
+                            mma_mxf8f6f4_elect(pacc, ad + 2, bd + 2, idh1, sfa_t, sfb_h, 1u);
+                            mma_mxf8f6f4_elect(pacc, ad + 4, bd + 4, idh2, sfa_t, sfb_h, 1u);
+                            mma_mxf8f6f4_elect(pacc, ad + 6, bd + 6, idh3, sfa_t, sfb_h, 1u);
+                            tc_commit_elect(smem_u32(&pc.pfull[b]));
+                            if (++b == kPBufs) {
+                                b = 0;
+                                pph ^= 1u;
+                                wrapped = true;
+                            }
+                        }
+                        if (!ok) break;
                         tc_commit_elect(empty0 + 8u * s);
-                        tc_commit_elect(smem_u32(&pc.pfull));
                         advance();
                     }
                 }
@@ -535,6 +897,8 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
             tc_commit_elect(smem_u32(&pc.drain));
             if (!mbar_wait(smem_u32(&pc.drain), 0u, &zero) && lane == 0) raise_error(g, args.err, 5);
         }
+    } else if (kSwap) {
+        if constexpr (kSwap) light_epilogue<kMode, kF32S, kW8>(g, pc, tmem, args, list, ts, warp, lane);
     } else {
         // ---------------------------------------------------- epilogue
         // Eight warps, two per TMEM lane quarter: warp pair (q, q + 4) shares
@@ -547,13 +911,18 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         int tcount = 0;
         if constexpr (kF32S || kW8) {
-            // promotion modes: per K-step, this warp's 128 partial columns are
-            // read from TMEM and folded into fp32 registers, acc += s * partial
-            // in K order, s = the row's fp32 activation scale and / or the
-            // fp32 scale of the weight block the columns belong to; warps
-            // without live rows still take part in each K-step's hand-off.
+            // promotion modes: per K-step and weight half, this warp's 64
+            // partial columns of that half are read from TMEM and folded into
+            // fp32 registers, acc += s * partial in K order, s = the row's
+            // fp32 activation scale and / or the fp32 scale of the weight
+            // block the half belongs to; warps without live rows still take
+            // part in each hand-off.  Gate/up: acc[0, 64) = gate columns
+            // [64 hw, +64) of the n-tile, acc[64, 128) the same up columns;
+            // down: acc[64 h + j] = output feature 128 h + 64 hw + j of the
+            // tile.
             constexpr int kW = 128;
-            int ks = 0;
+            int b = 0;            // partial buffer of the next half-step
+            uint32_t pph = 0;     // its fill count's parity
             // activation scales come from the previous kernel (quantisation,
             // or the gate/up GEMM): wait for it before the first read
             if (kF32S) griddep_wait();
@@ -562,21 +931,18 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 const int rows = args.mtile_rows[mt];
                 const bool warp_live = q * 32 < rows;
                 const bool row_live = row < rows;
-                const int ncw = kMode == 0 ? 128 : 64 * args.halves;     // this warp's columns
-                // gate/up: gate columns [64 hw, +64) then up columns [128 + 64 hw, +64);
-                // down: columns [hw * ncw, +ncw)
-                const uint32_t c0 = kMode == 0 ? 64u * hw : (uint32_t)(hw * ncw);
-                const uint32_t c1 = kMode == 0 ? 128u + 64u * hw : c0 + 64u;
+                const int halves = args.halves;
+                const uint32_t c0 = 64u * (uint32_t)hw;   // this warp's columns within each half
                 const float* srow = kF32S ? args.as32 + (size_t)(mt * kBM + row) * KB : nullptr;
-                // weight blocks of this warp's two column groups: gate / up rows of
-                // the n-tile (gate/up), or the tile's 128-feature block (down)
+                // weight blocks of the two halves: gate / up rows of the n-tile
+                // (gate/up), or the tile's 128-feature blocks (down)
                 const float* wsa = nullptr;
                 const float* wsb = nullptr;
                 if constexpr (kW8) {
                     const int e = args.mtile_expert[mt];
                     const int RB = kMode == 0 ? 2 * (args.I / 128) : args.H / 128;
-                    const int rba = kMode == 0 ? nt : nt * args.halves + (args.halves == 2 ? hw : 0);
-                    const int rbb = kMode == 0 ? args.I / 128 + nt : rba;
+                    const int rba = kMode == 0 ? nt : nt * halves;
+                    const int rbb = kMode == 0 ? args.I / 128 + nt : rba + (halves == 2 ? 1 : 0);
                     wsa = args.ws + ((size_t)e * RB + rba) * KB;
                     wsb = args.ws + ((size_t)e * RB + rbb) * KB;
                 }
@@ -586,7 +952,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 float s_next = kF32S ? (row_live ? srow[0] : 0.0f) : 1.0f;
                 float wa_next = kW8 ? wsa[0] : 1.0f, wb_next = kW8 ? wsb[0] : 1.0f;
                 bool ok = true;
-                for (int kb = 0; kb < KB; ++kb, ++ks) {
+                for (int kb = 0; kb < KB && ok; ++kb) {
                     const float sc_a = s_next * wa_next, sc_b = s_next * wb_next;
                     if (kb + 1 < KB) {
                         if constexpr (kF32S) s_next = row_live ? srow[kb + 1] : 0.0f;
@@ -595,28 +961,37 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                             wb_next = wsb[kb + 1];
                         }
                     }
-                    if (!mbar_wait(smem_u32(&pc.pfull), (uint32_t)ks & 1u, abrt)) {
-                        raise_error(g, args.err, 10);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (warp_live) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            if (32 * c < ncw) {
-                                uint32_t pv[32];
-                                tmem_ld32(tl + kAccCol + (c < 2 ? c0 + 32u * c : c1 + 32u * (c - 2)), pv);
-                                tmem_ld_wait();
-                                const float sc = c < 2 ? sc_a : sc_b;
+                    for (int h = 0; h < 2; ++h) {
+                        if (h < halves) {
+                            if (!mbar_wait(smem_u32(&pc.pfull[b]), pph, abrt)) {
+                                raise_error(g, args.err, 10);
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            if (warp_live) {
+                                const float sc = h == 0 ? sc_a : sc_b;
+                                const uint32_t src = tl + kPBufCol + 128u * (uint32_t)b + c0;
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(sc, __uint_as_float(pv[j]), acc[32 * c + j]);
+                                for (int c = 0; c < 2; ++c) {
+                                    uint32_t pv[32];
+                                    tmem_ld32(src + 32u * c, pv);
+                                    tmem_ld_wait();
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j)
+                                        acc[64 * h + 32 * c + j] = fmaf(sc, __uint_as_float(pv[j]), acc[64 * h + 32 * c + j]);
+                                }
+                            }
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(&pc.pempty[b]));
+                            if (++b == kPBufs) {
+                                b = 0;
+                                pph ^= 1u;
                             }
                         }
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&pc.pempty));
                 }
                 if (!ok) break;
                 if (kMode == 0 && !kF32S) {
@@ -698,11 +1073,17 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         if (hw == 0) args.hs32[(size_t)(mt * kBM + row) * (args.I / 128) + nt] = s2;
                     }
                 } else if (row_live) {
-                    float4* d4 = reinterpret_cast<float4*>(args.obuf + (size_t)(mt * kBM + row) * args.H +
-                                                           (size_t)nt * (128 * args.halves) + c0);
+                    float* orow = args.obuf + (size_t)(mt * kBM + row) * args.H + (size_t)nt * (128 * halves) + c0;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (4 * j < ncw) d4[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+                    for (int h = 0; h < 2; ++h) {
+                        if (h < halves) {
+                            float4* d4 = reinterpret_cast<float4*>(orow + 128 * h);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                d4[j] = make_float4(acc[64 * h + 4 * j], acc[64 * h + 4 * j + 1],
+                                                    acc[64 * h + 4 * j + 2], acc[64 * h + 4 * j + 3]);
+                        }
+                    }
                 }
             }
         } else
@@ -788,7 +1169,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                         args.hsf[sf_word_index(mt, nt, args.I / 128, row)] = (uint32_t)(ex + 127) * 0x01010101u;
                 }
             } else {
-                static_assert(!(kF32S || kW8), "the heavy down stash overlaps the promotion modes' unit scales");
+                static_assert(!(kF32S || kW8), "the heavy down stash is for the E8M0 epilogue only");
                 // this warp: output columns [hw * ncols / 2, (hw + 1) * ncols / 2).  The
                 // whole slice is read into registers first and the accumulator released,
                 // so the next tile's MMAs run while the rows are stored.
@@ -809,6 +1190,11 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
         }
     }
 }
+
+// light m-tiles with the tokens on the MMA's N side (see kSwN): the
+// promotion modes (in the E8M0 mode the 128 x 256 form measured faster)
+template <bool kF32S, bool kW8>
+constexpr bool kLightTokensN = kF32S || kW8;
 
 // mode 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows; kF32S: the
 // activation blocks carry fp32 scales, kW8: the experts are e4m3 with fp32
@@ -850,8 +1236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = g->tmem_base;
     bool waited = false;   // the producer's wait for the previous kernel (producer thread only)
 
-    gemm_phase<kMode, true, kF32S, kW8>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args, args.light_list,
-                                        *args.light_count, waited);
+    gemm_phase<kMode, true, kF32S, kW8, kLightTokensN<kF32S, kW8>>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args,
+                                                       args.light_list, *args.light_count, waited);
     // the heavy phase reuses the ring and the accumulator: every role of the
     // light phase has drained its own work
     tc_fence_before();
