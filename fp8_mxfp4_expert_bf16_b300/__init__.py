@@ -94,6 +94,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         "moe_route_noalloc": (S, [P, I, I, P, P, P, I, I, I, P, P, P]),
         "moe_route_noalloc_check_error": (S, [P]),
         "moe_selftest_mma_peak": (S, [I, I, I, P]),
+        "moe_selftest_mma_shape": (S, [I, I, I, I, P]),
         "moe_debug_fill_workspace": (S, [P, I]),
         "moe_mxfp4_quantize": (S, [P, ctypes.c_size_t, I, P, P, P]),
     }
@@ -388,6 +389,17 @@ def mma_peak(device=0, steps_per_cta=8192, launches=1):
     if st != 0:
         raise MoEError(st, L.moe_last_error(None).decode())
     return {"tflops": float(out[0]), "sm_mhz": float(out[1]), "cycles_per_mma": float(out[2]), "ms": float(out[3])}
+
+
+def mma_shape(n, tokens_on_n=False, device=0, steps_per_cta=4096):
+    """Cost of one block-scaled 128 x n x 32 MMA (see moe_selftest_mma_shape):
+    returns dict(cycles_per_mma, sm_mhz, tflops)."""
+    L = lib()
+    out = np.zeros(3, dtype=np.float32)
+    st = L.moe_selftest_mma_shape(int(device), int(n), 1 if tokens_on_n else 0, int(steps_per_cta), _ptr(out))
+    if st != 0:
+        raise MoEError(st, L.moe_last_error(None).decode())
+    return {"cycles_per_mma": float(out[0]), "sm_mhz": float(out[1]), "tflops": float(out[2])}
 
 
 def sum_partials_bf16(parts, y=None, stream=None):

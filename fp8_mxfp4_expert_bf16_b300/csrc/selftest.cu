@@ -2,6 +2,9 @@
 // on: tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale, M = 128, N = 256,
 // K = 32, e4m3 activations (A) against E2M1 weights (B) with one E8M0 scale
 // per 32 values.  It measures the dense rate the prefill roofline divides by.
+// The same kernel times other N and the operand order of the light m-tiles
+// in the promotion modes (E2M1 weights as the 128-row A operand, N e4m3
+// token rows as B): the instruction's cost in cycles for each shape.
 //
 // One CTA per SM (the shared-memory request leaves room for one), four
 // warps: warp 1 allocates TMEM, copies the two scale chunks into it and then
@@ -46,7 +49,7 @@ __device__ __forceinline__ uint32_t hash32(uint32_t x)
     return x;
 }
 
-__global__ void __launch_bounds__(128, 1) k_mma_peak(int n_steps, PeakOut* out)
+__global__ void __launch_bounds__(128, 1) k_mma_peak(int n_steps, int N, int tokens_on_n, PeakOut* out)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -81,12 +84,15 @@ __global__ void __launch_bounds__(128, 1) k_mma_peak(int n_steps, PeakOut* out)
 
     if (warp == 1) {
         const uint32_t s0 = smem_u32(smem);
-        const uint64_t ad = desc_kmajor_sw128(s0), bd = desc_kmajor_sw128(s0 + kPeakABytes);
+        // activation rows (e4m3) at s0, weight rows (E2M1 in 16-byte slots) after them
+        const uint64_t xd = desc_kmajor_sw128(s0), wd = desc_kmajor_sw128(s0 + kPeakABytes);
+        const uint64_t ad = tokens_on_n ? wd : xd, bd = tokens_on_n ? xd : wd;
         const uint32_t sfa = tmem + 256, sfb = tmem + 264;
         tmem_cp_32x128b_warpx4_elect(sfa, desc_sf_chunk(s0 + kPeakSFOff));
         tmem_cp_32x128b_warpx4_elect(sfb, desc_sf_chunk(s0 + kPeakSFOff + 512));
         tmem_cp_32x128b_warpx4_elect(sfb + 4u, desc_sf_chunk(s0 + kPeakSFOff + 1024));
-        const uint32_t id0 = idesc_mxf8f6f4(128, 256, kTypeE4M3, kTypeE2M1);
+        const uint32_t id0 = tokens_on_n ? idesc_mxf8f6f4(128, (uint32_t)N, kTypeE2M1, kTypeE4M3)
+                                         : idesc_mxf8f6f4(128, (uint32_t)N, kTypeE4M3, kTypeE2M1);
         const uint32_t id1 = idesc_with_sf_id(id0, 1, 1), id2 = idesc_with_sf_id(id0, 2, 2),
                        id3 = idesc_with_sf_id(id0, 3, 3);
         __syncwarp();
@@ -122,18 +128,17 @@ __global__ void __launch_bounds__(128, 1) k_mma_peak(int n_steps, PeakOut* out)
 
 void moe_set_handle_free_error(const char* msg);
 
-extern "C" moe_status moe_selftest_mma_peak(int device, int steps_per_cta, int launches, float* result)
+// Runs `launches` probe launches; cycles / ns / CUDA-event ms of the last launch's CTAs.
+static moe_status run_probe(const char* who, int device, int steps_per_cta, int launches, int N, int tokens_on_n,
+                            double* cyc_per_sm, double* ns_per_sm, float* ms_all, int* nsm_out)
 {
     char buf[256];
     auto fail = [&](moe_status st, const char* what, cudaError_t e) {
-        snprintf(buf, sizeof buf, "moe_selftest_mma_peak: %s%s%s", what, e != cudaSuccess ? ": " : "",
+        snprintf(buf, sizeof buf, "%s: %s%s%s", who, what, e != cudaSuccess ? ": " : "",
                  e != cudaSuccess ? cudaGetErrorString(e) : "");
         moe_set_handle_free_error(buf);
         return st;
     };
-    if (!result) return fail(MOE_ERR_INVALID_ARG, "result is NULL", cudaSuccess);
-    if (steps_per_cta < 1 || steps_per_cta > (1 << 22) || launches < 1 || launches > 100000)
-        return fail(MOE_ERR_INVALID_ARG, "steps_per_cta must be in [1, 2^22] and launches in [1, 10^5]", cudaSuccess);
     cudaError_t e = cudaSetDevice(device);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaSetDevice", e);
     cudaDeviceProp prop;
@@ -154,7 +159,7 @@ extern "C" moe_status moe_selftest_mma_peak(int device, int steps_per_cta, int l
     float ms = 0.f;
     e = cudaEventRecord(ev0, 0);
     for (int i = 0; i < launches && e == cudaSuccess; ++i) {
-        moe::k_mma_peak<<<nsm, 128, moe::kPeakSmem + 1024>>>(steps_per_cta, d_out);
+        moe::k_mma_peak<<<nsm, 128, moe::kPeakSmem + 1024>>>(steps_per_cta, N, tokens_on_n, d_out);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = cudaEventRecord(ev1, 0);
@@ -174,10 +179,52 @@ extern "C" moe_status moe_selftest_mma_peak(int device, int steps_per_cta, int l
     cudaEventDestroy(ev1);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "launch or readback", e);
     if (errs) return fail(MOE_ERR_TIMEOUT, "a CTA's closing wait timed out", cudaSuccess);
+    *cyc_per_sm = cyc / nsm;
+    *ns_per_sm = ns / nsm;
+    *ms_all = ms;
+    *nsm_out = nsm;
+    return MOE_OK;
+}
+
+static moe_status probe_arg_error(const char* msg)
+{
+    moe_set_handle_free_error(msg);
+    return MOE_ERR_INVALID_ARG;
+}
+
+extern "C" moe_status moe_selftest_mma_peak(int device, int steps_per_cta, int launches, float* result)
+{
+    if (!result) return probe_arg_error("moe_selftest_mma_peak: result is NULL");
+    if (steps_per_cta < 1 || steps_per_cta > (1 << 22) || launches < 1 || launches > 100000)
+        return probe_arg_error("moe_selftest_mma_peak: steps_per_cta must be in [1, 2^22] and launches in [1, 10^5]");
+    double cyc = 0, ns = 0;
+    float ms = 0.f;
+    int nsm = 0;
+    const moe_status st = run_probe("moe_selftest_mma_peak", device, steps_per_cta, launches, 256, 0, &cyc, &ns, &ms, &nsm);
+    if (st != MOE_OK) return st;
     const double flop = 2.0 * 128 * 256 * 32 * 4.0 * steps_per_cta * nsm * launches;
     result[0] = (float)(flop / (ms * 1e-3) / 1e12);             // TFLOP/s over all launches (CUDA events)
     result[1] = (float)(cyc / ns * 1e3);                         // mean SM clock (MHz) of the last launch
-    result[2] = (float)(cyc / nsm / (4.0 * steps_per_cta));      // SM cycles per MMA (last launch)
+    result[2] = (float)(cyc / (4.0 * steps_per_cta));            // SM cycles per MMA (last launch)
     result[3] = ms;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_selftest_mma_shape(int device, int n, int tokens_on_n, int steps_per_cta, float* result)
+{
+    if (!result) return probe_arg_error("moe_selftest_mma_shape: result is NULL");
+    if (steps_per_cta < 1 || steps_per_cta > (1 << 22))
+        return probe_arg_error("moe_selftest_mma_shape: steps_per_cta must be in [1, 2^22]");
+    if (n < 16 || n % 16 != 0 || n > (tokens_on_n ? 128 : 256) || (tokens_on_n != 0 && tokens_on_n != 1))
+        return probe_arg_error("moe_selftest_mma_shape: n must be a multiple of 16 in [16, 256] (tokens_on_n = 0) "
+                               "or [16, 128] (tokens_on_n = 1)");
+    double cyc = 0, ns = 0;
+    float ms = 0.f;
+    int nsm = 0;
+    const moe_status st = run_probe("moe_selftest_mma_shape", device, steps_per_cta, 1, n, tokens_on_n, &cyc, &ns, &ms, &nsm);
+    if (st != MOE_OK) return st;
+    result[0] = (float)(cyc / (4.0 * steps_per_cta));            // SM cycles per MMA
+    result[1] = (float)(cyc / ns * 1e3);                         // mean SM clock (MHz)
+    result[2] = (float)(2.0 * 128 * n * 32 * 4.0 * steps_per_cta * nsm / (ms * 1e-3) / 1e12);   // TFLOP/s
     return MOE_OK;
 }

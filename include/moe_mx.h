@@ -260,6 +260,17 @@ moe_status moe_selftest_wait_timeout(moe_handle* h, unsigned int limit_us);
  * Allocates a small result buffer; errors through moe_last_error(NULL). */
 moe_status moe_selftest_mma_peak(int device, int steps_per_cta, int launches, float* result);
 
+/* The same probe for other shapes of the instruction (no counterpart in the
+ * pages either): M = 128, K = 32, N = n columns, in the order the heavy
+ * m-tiles use (tokens_on_n = 0: 128 e4m3 token rows as A, n E2M1 weight rows
+ * as B; n a multiple of 16 in [16, 256]) or the order of the light m-tiles
+ * in the promotion modes (tokens_on_n = 1: 128 E2M1 weight rows as A, n
+ * e4m3 token rows as B; n a multiple of 16 in [16, 128]).  One launch of
+ * 4 * steps_per_cta MMAs per SM (1 .. 2^22 steps), waited for.  result
+ * (host, float[3]): [0] SM cycles per MMA, [1] mean SM clock in MHz, [2]
+ * dense TFLOP/s (2*128*n*32 per MMA).  Errors through moe_last_error(NULL). */
+moe_status moe_selftest_mma_shape(int device, int n, int tokens_on_n, int steps_per_cta, float* result);
+
 /* Debug: fill every workspace buffer of the handle (routing and dispatch
  * tables, the quantised activation and SwiGLU rows with their scales, the
  * expert outputs, the host-entry staging buffers; not the device error word)

@@ -27,3 +27,23 @@ def test_mma_peak_probe():
     assert abs(r["tflops"] - implied) <= 0.15 * implied, (r, implied)
     with pytest.raises(moe.MoEError):
         moe.mma_peak(0, 0, 1)
+
+
+def test_mma_shape_probe():
+    """The instruction's cost per shape: 128 x 256 at about the peak probe's
+    cycle count, and the tokens-on-N form (weights as A) no dearer than the
+    128 x 256 form for N <= 128, at most N / 256 of its work per instruction."""
+    import fp8_mxfp4_expert_bf16_b300 as moe
+    moe.mma_shape(256, False, 0, 512)              # warm-up
+    full = moe.mma_shape(256, False, 0, 4096)
+    print("128x256", full)
+    assert 100.0 <= full["cycles_per_mma"] <= 400.0
+    for n in (16, 64, 128):
+        r = moe.mma_shape(n, True, 0, 4096)
+        print(f"128x{n} weights as A", r)
+        assert 0.0 < r["cycles_per_mma"] <= full["cycles_per_mma"] * 1.05
+    r = moe.mma_shape(128, False, 0, 4096)
+    assert 0.0 < r["cycles_per_mma"] <= full["cycles_per_mma"] * 1.05
+    for bad in [(8, False), (144, True), (272, False), (24, False)]:
+        with pytest.raises(moe.MoEError):
+            moe.mma_shape(bad[0], bad[1], 0, 16)
