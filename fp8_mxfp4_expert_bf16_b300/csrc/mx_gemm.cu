@@ -64,10 +64,8 @@ namespace moe {
 //  heavy (m-tiles with more than kLightRows = 16 valid rows): 128-row
 //    activation slot, 4-stage ring;
 //  light (at most 16 valid rows: decode, and an expert's last m-tile): the
-//    activation slot holds only the 16-row box (2 KB), which buys 6 stages.
-//    The MMA still reads 128 rows; rows 16..127 then come from the first
-//    14 KB of the same stage's weight tile - finite or not, they only reach
-//    accumulator rows that the epilogue never uses.
+//    activation slot holds only the 16-row box (2 KB), which buys 6 stages;
+//    these m-tiles put the token rows on the MMA's N side (see kSwN).
 // With six stages in flight per SM (about 100 KB of weights) the weight
 // stream needs no separate L2 prefetch; one measured on top of the ring
 // slowed both GEMMs.
@@ -115,7 +113,10 @@ static_assert(kPUnitCol + 8 <= kTmemCols, "promotion-mode TMEM layout");
 // Light m-tiles (at most 16 valid rows) put the tokens on the MMA's N side:
 // the weights are the 128-row A operand (one MMA group per 128-row half of
 // the tile) and the 16 activation rows the B operand, so an MMA computes the
-// 128 x 16 outputs that are used instead of 128 x 256.  An accumulator is
+// 128 x 16 outputs that are used instead of 128 x 256 (a 128 x 16 x 32 MMA
+// costs 39 cycles against 128 for 128 x 256 x 32, and 1/16 of the
+// multiply-adds: in decode the 128 x 256 form kept the tensor pipe busy on
+// rows it discarded and drove the chip to its power cap).  An accumulator is
 // then 16 TMEM columns (tokens) by 128 lanes (weight rows):
 //   E8M0 activations: one 32-column pair (both halves) per tile, a ring of
 //     kSwTBufs tiles, read once at the tile's end;
@@ -253,34 +254,6 @@ __device__ __forceinline__ void producer_wait_once(bool& waited, int early_trigg
         griddep_wait();
         if (early_trigger) griddep_launch_dependents();
         waited = true;
-    }
-}
-
-// Down-GEMM epilogue of one warp, light m-tiles (at most kLightRows valid
-// rows): `ncols` (64 or 128) fp32 accumulator columns of its 32 TMEM lanes
-// go to registers, the accumulator is released (arrive on `acc_empty`), then
-// each live lane stores its own row.  With so few rows the stores are short
-// and the accumulator is held only for the TMEM reads.
-__device__ __forceinline__ void store_rows_direct(uint32_t taddr, int ncols, int live_rows, float* dst0,
-                                                  size_t row_stride, uint32_t acc_empty, int lane)
-{
-    uint32_t v[128];
-    if (live_rows > 0) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if (32 * c < ncols) tmem_ld32(taddr + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
-        tmem_ld_wait();
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(acc_empty);
-    if (lane < live_rows) {
-        float4* d4 = reinterpret_cast<float4*>(dst0 + (size_t)lane * row_stride);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (4 * j < ncols)
-                d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
     }
 }
 
@@ -656,7 +629,7 @@ __device__ __forceinline__ void light_epilogue(GemmCtl* g, PhaseCtl<Shape<true>:
 // role drains its own work before returning: the producer waits until its
 // copies have landed, the MMA issuer until its MMAs have completed, the
 // epilogue has read its last accumulator.
-template <int kMode, bool kLight, bool kF32S, bool kW8, bool kSwap = false>
+template <int kMode, bool kLight, bool kF32S, bool kW8>
 __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<Shape<kLight>::kStages>& pc,
                                            uint32_t tmem, const CUtensorMap* tmA0, const CUtensorMap* tmA1,
                                            const CUtensorMap* tmA2, const CUtensorMap* tmW, const GemmArgs& args,
@@ -763,9 +736,9 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                 if (issued[s] && !mbar_wait(smem_u32(&pc.full[s]), last_phase[s], &zero))
                     raise_error(g, args.err, 2);
         }
-    } else if (warp == 1 && kSwap) {
-        static_assert(!kSwap || kLight, "tokens on the N side: light m-tiles only");
-        if constexpr (kSwap) light_mma<kMode, kF32S, kW8>(smem, g, pc, tmem, args, ts, lane);
+    } else if (warp == 1 && kLight) {
+        // light m-tiles: tokens on the MMA's N side
+        if constexpr (kLight) light_mma<kMode, kF32S, kW8>(smem, g, pc, tmem, args, ts, lane);
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         // The loops run on the whole warp (one elected lane issues each
@@ -897,8 +870,8 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
             tc_commit_elect(smem_u32(&pc.drain));
             if (!mbar_wait(smem_u32(&pc.drain), 0u, &zero) && lane == 0) raise_error(g, args.err, 5);
         }
-    } else if (kSwap) {
-        if constexpr (kSwap) light_epilogue<kMode, kF32S, kW8>(g, pc, tmem, args, list, ts, warp, lane);
+    } else if (kLight) {
+        if constexpr (kLight) light_epilogue<kMode, kF32S, kW8>(g, pc, tmem, args, list, ts, warp, lane);
     } else {
         // ---------------------------------------------------- epilogue
         // Eight warps, two per TMEM lane quarter: warp pair (q, q + 4) shares
@@ -1178,9 +1151,7 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
                     args.obuf + (size_t)(mt * kBM + q * 32) * args.H + (size_t)nt * ncols + hw * half_cols;
                 const int live = warp_live ? min(32, rows - q * 32) : 0;
                 const uint32_t taddr = tl + kAccCol + (uint32_t)(hw * half_cols);
-                if (kLight)
-                    store_rows_direct(taddr, half_cols, live, dst0, (size_t)args.H, smem_u32(&pc.acc_empty), lane);
-                else if (half_cols == 128)
+                if (half_cols == 128)
                     store_rows_sectors<128>(taddr, tl + kStashHeavyCol + 96u * hw, live, dst0, (size_t)args.H,
                                             smem_u32(&pc.acc_empty), lane);
                 else
@@ -1190,11 +1161,6 @@ __device__ __forceinline__ void gemm_phase(uint8_t* smem, GemmCtl* g, PhaseCtl<S
         }
     }
 }
-
-// light m-tiles with the tokens on the MMA's N side (see kSwN): the
-// promotion modes (in the E8M0 mode the 128 x 256 form measured faster)
-template <bool kF32S, bool kW8>
-constexpr bool kLightTokensN = kF32S || kW8;
 
 // mode 0: gate/up + SwiGLU + e4m3 requant, 1: down -> fp32 rows; kF32S: the
 // activation blocks carry fp32 scales, kW8: the experts are e4m3 with fp32
@@ -1236,8 +1202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = g->tmem_base;
     bool waited = false;   // the producer's wait for the previous kernel (producer thread only)
 
-    gemm_phase<kMode, true, kF32S, kW8, kLightTokensN<kF32S, kW8>>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args,
-                                                       args.light_list, *args.light_count, waited);
+    gemm_phase<kMode, true, kF32S, kW8>(smem, g, g->light, tmem, &tmA0, &tmA1, &tmA1, &tmW, args, args.light_list,
+                                        *args.light_count, waited);
     // the heavy phase reuses the ring and the accumulator: every role of the
     // light phase has drained its own work
     tc_fence_before();
