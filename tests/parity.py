@@ -20,8 +20,15 @@ inputs.  Bars (written here, used by the GPU tests):
     gate/up sums and the oracle's fp64 sums round differently only near an
     e4m3 rounding boundary).  With fp32 block scales (amax / 448) the scales
     themselves come from those sums: they must agree to Q2_F32_SCALE_REL.
-  * y: relative L2 error <= 1e-3 and max |error| <= 2e-2 * RMS(y_oracle)
-    against the oracle's bf16-rounded output.
+  * y: relative L2 error <= 1e-3 against the oracle's bf16-rounded output,
+    and max |error| <= 2e-2 * RMS(y_oracle).  Where a Q2 code sits at an e4m3
+    rounding boundary to within the fp32/fp64 difference, both neighbouring
+    codes are correct (the reading that decides near-tie routing), and one
+    such code moves its token's output by up to a whole e4m3 step of h times
+    the down weights.  So, when the intermediates are read back, the max-abs
+    bar is measured against the oracle fed the GPU's own Q2 codes and scales
+    (identical to the oracle's output wherever the codes agree); the relative
+    L2 bar stays against the oracle's own output.
 """
 from __future__ import annotations
 
@@ -125,13 +132,16 @@ def check_act_quant_all(layer, inp):
     assert bad.size == 0, f"Q1 differs on {bad.size} tokens, first {bad[:8]}"
 
 
-def check_y(y_g, y_o):
+def check_y(y_g, y_o, y_q2=None):
+    """y_g against the oracle's output y_o (relative L2) and against y_q2, the
+    oracle's output from the GPU's own Q2 codes, when given (max abs)."""
     a = bf16_f64(y_g)
     b = bf16_f64(y_o)
+    c = b if y_q2 is None else bf16_f64(y_q2)
     assert np.isfinite(a).all()
     rms = np.sqrt(np.mean(b * b))
     rel = np.linalg.norm(a - b) / np.linalg.norm(b)
-    mx = np.abs(a - b).max() / rms
+    mx = np.abs(a - c).max() / rms
     assert rel <= Y_REL_L2, f"rel L2 {rel:.3e}"
     assert mx <= Y_MAX_ABS_RMS, f"max abs / rms {mx:.3e}"
     return rel, mx
@@ -183,14 +193,17 @@ DOWN_TF_REL = 1e-5
 def check_down_teacher_forced(layer, inp, perm, toks, sel, o_g):
     """The down GEMM alone: the oracle recomputes each row's expert output in
     fp64 from the GPU's own Q2 codes and scales (so Q2 rounding differences
-    drop out); the GPU's fp32 accumulation must agree to DOWN_TF_REL."""
+    drop out); the GPU's fp32 accumulation must agree to DOWN_TF_REL.
+    Returns the relative error and those fp64 outputs, [len(sel), k, H] in
+    the GPU's slot order."""
     hq_g, hs_g = layer.inter_quant()
     ids_g, _ = layer.routing()
     c = inp.cfg
     fp8 = getattr(inp, "weight_format", "mxfp4") == "fp8"
     num = den = 0.0
     W2 = {}
-    for i in sel:
+    o_tf = np.zeros((len(sel), c.k, c.H))
+    for n_i, i in enumerate(sel):
         t = toks[i]
         for j in range(c.k):
             e = int(ids_g[t, j])
@@ -200,11 +213,12 @@ def check_down_teacher_forced(layer, inp, perm, toks, sel, o_g):
             row = perm[t * c.k + j]
             h = oracle.act_dequant(hq_g[row:row + 1], hs_g[row:row + 1])
             o = (h @ W2[e].T)[0]
+            o_tf[n_i, j] = o
             num += float(np.sum((o_g[row].astype(np.float64) - o) ** 2))
             den += float(np.sum(o * o))
     rel = np.sqrt(num / max(den, 1e-300))
     assert rel <= DOWN_TF_REL, f"down GEMM vs fp64 on its own inputs: rel L2 {rel:.3e}"
-    return float(rel)
+    return float(rel), o_tf
 
 
 def full_check(layer, inp, tokens=None, check_intermediates=True, poison=False):
@@ -228,6 +242,7 @@ def full_check(layer, inp, tokens=None, check_intermediates=True, poison=False):
     perm = check_dispatch(layer, f)
     check_act_quant_all(layer, inp)
     stats = {"near_tie_set_tokens": int((~same).sum()), "near_tie_order_tokens": int((same & ~same_order).sum())}
+    y_q2 = None
     if check_intermediates:
         stats["q2_mismatch"] = check_q2(layer, f, perm, toks, ids_g)
         o_g = layer.expert_out()
@@ -237,8 +252,11 @@ def full_check(layer, inp, tokens=None, check_intermediates=True, poison=False):
         o_rel = np.linalg.norm(og - oo) / np.linalg.norm(oo)
         assert o_rel <= Y_REL_L2, f"expert output rel L2 {o_rel:.3e}"
         stats["expert_out_rel_l2"] = float(o_rel)
-        stats["down_teacher_forced_rel_l2"] = check_down_teacher_forced(layer, inp, perm, toks,
-                                                                         np.arange(toks.size), o_g)
-    rel, mx = check_y(y_g[toks], f.y)
+        stats["down_teacher_forced_rel_l2"], o_tf = check_down_teacher_forced(layer, inp, perm, toks,
+                                                                               np.arange(toks.size), o_g)
+        # the oracle's combine of the outputs from the GPU's own Q2 codes (the
+        # oracle's gates; its slots are the GPU's, asserted above)
+        y_q2 = oracle.f64_to_bf16(np.einsum("nk,nkh->nh", f.route.gates[toks], o_tf))
+    rel, mx = check_y(y_g[toks], f.y, y_q2)
     stats.update(rel_l2=rel, max_abs_over_rms=mx)
     return stats, y_g, f
