@@ -573,11 +573,19 @@ static moe_status forward_impl(moe_handle* h, const uint16_t* x, int T, void* y,
         return fail(h, MOE_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed for x", who);
     const int ksplit = router_split(T, s.H);
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[0], st));
-    CUDA_TRY(h, launch_router_tc(s, tmX, T, st, ksplit));
-    ++n;
-    if (prof) CUDA_TRY(h, cudaEventRecord(ev[1], st));
-    CUDA_TRY(h, launch_topk(s, T, st, ksplit));
-    ++n;
+    if (router_fused(T, s.E)) {
+        // prefill-sized batch: the top-k runs in the router's epilogue (the
+        // "topk" stage then times nothing)
+        CUDA_TRY(h, launch_router_topk(s, tmX, T, st));
+        ++n;
+        if (prof) CUDA_TRY(h, cudaEventRecord(ev[1], st));
+    } else {
+        CUDA_TRY(h, launch_router_tc(s, tmX, T, st, ksplit));
+        ++n;
+        if (prof) CUDA_TRY(h, cudaEventRecord(ev[1], st));
+        CUDA_TRY(h, launch_topk(s, T, st, ksplit));
+        ++n;
+    }
     if (prof) CUDA_TRY(h, cudaEventRecord(ev[2], st));
     if (T <= kChunk) {
         // small batch: histogram, scan and ranks in one single-block kernel

@@ -15,6 +15,7 @@ constexpr int kNumABox = 5;         // activation tile maps with 8 / 16 / 32 / 6
 constexpr int kWBlockRowsPerHalf = 136;   // interleaved weight block: 128 weight rows + 8 scale rows of 64 B
 constexpr int kRouterMaxSplit = 16;       // split-K factor of the router for small batches
 constexpr int kRouterSplitMaxT = 512;     // batches up to this size use the split-K router
+constexpr int kRouterFusedMinT = 4096;    // batches from this size use the router with the top-k in its epilogue
 constexpr int kLightRows = 16;      // m-tiles with at most this many rows use the light GEMM shape
 constexpr int kMaxTp = 8;           // tensor-parallel shards of the expert middle dimension
 
@@ -138,6 +139,8 @@ cudaError_t launch_gather_scales_f32(const DevState& s, int T, int which, float*
 cudaError_t launch_router_tc(const DevState& s, const CUtensorMap& tmX, int T, cudaStream_t st, int ksplit = 1);
 int router_split(int T, int H);
 cudaError_t router_set_attributes();
+bool router_fused(int T, int E);
+cudaError_t launch_router_topk(const DevState& s, const CUtensorMap& tmX, int T, cudaStream_t st);
 // grouped GEMMs (mx_gemm.cu)
 cudaError_t launch_gemm1(const DevState& s, cudaStream_t st, int T);
 cudaError_t launch_gemm2(const DevState& s, cudaStream_t st, int T);

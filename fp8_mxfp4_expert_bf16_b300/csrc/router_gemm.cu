@@ -13,6 +13,7 @@
 // the logits.  Waits are bounded in time as in the grouped GEMMs.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "moe_internal.cuh"
@@ -181,9 +182,338 @@ __global__ void __launch_bounds__(128, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Prefill-sized batches: the router and the top-k gate in one kernel.  One
+// CTA per 128 tokens computes the logits of all E experts (E <= 512 fp32
+// TMEM columns, MMAs of at most 256 columns per expert chunk) from 64-wide K
+// slices of x and of every router row, so x is read once and the logits do
+// not make a round trip through memory before the selection.  Then 16
+// warps read the logits out of TMEM, warp (q, g) the rows of lane quarter q
+// (32 tokens, one per thread) in column group g (every fourth 16-column
+// chunk): logits (+ logit bias, also stored for the getters), scores
+// (sigmoid, or softmax over the experts, its row maximum and sum combined
+// across the groups through shared memory), keys = scores + correction
+// bias, and each thread's partial top 8 by insertion under the order key
+// descending, ties to the lower expert index, a NaN key ranking last.  One
+// thread per token then merges its four partial lists (the ring's shared
+// memory is free once the MMAs are done) under the same order -- the
+// selection of the separate top-k kernel; gates = the selected scores /
+// their sum, summed in selection order.
+constexpr int kRTMaxStages = 4;
+constexpr int kRTGroups = 4;                             // epilogue warps per TMEM lane quarter (column groups)
+constexpr int kRTThreads = 32 * 4 * kRTGroups;
+constexpr int kRTXBytes = 128 * 128;                     // 128 tokens x 64 bf16
+// the epilogue's scratch (row maxima / sums, partial lists) reuses the ring,
+// whose smallest form (E <= 128: four 32 KB stages) it must fit
+static_assert(4 * (kRTGroups * 128 + 3 * 128 * kRTGroups * kMaxTopK) <= 4 * (kRTXBytes + 128 * 128),
+              "router epilogue scratch");
+constexpr int kRTSmemBytes = 232448;                      // the opt-in maximum; the ring takes what fits
+
+struct RouterTopkCtl {
+    uint64_t full[kRTMaxStages];
+    uint64_t empty[kRTMaxStages];
+    uint64_t acc_full;
+    uint32_t tmem_base;
+    int abort;
+    float lb[kMaxExperts];
+    float cb[kMaxExperts];
+};
+
+__device__ __forceinline__ void router_fail(RouterTopkCtl* ctl, int32_t* err, int where)
+{
+    if (atomicCAS(err, 0, kDevErrTimeout) == 0) {
+        err[1] = where;
+        err[2] = blockIdx.x;
+    }
+    *(volatile int*)&ctl->abort = 1;
+}
+
+// stage layout: the x tile, then Epad = E rounded up to 128 router rows (128-row TMA boxes)
+__host__ __device__ __forceinline__ int rt_epad(int E) { return (E + 127) / 128 * 128; }
+__host__ __device__ __forceinline__ int rt_stage_bytes(int E) { return kRTXBytes + rt_epad(E) * 128; }
+__host__ __device__ __forceinline__ int rt_stages(int E)
+{
+    const int n = (kRTSmemBytes - 1024 - (int)sizeof(RouterTopkCtl)) / rt_stage_bytes(E);
+    return n < kRTMaxStages ? n : kRTMaxStages;
+}
+__host__ __device__ __forceinline__ uint32_t rt_tmem_cols(int E16)
+{
+    uint32_t c = 32;
+    while ((int)c < E16) c <<= 1;
+    return c;
+}
+
+__device__ __forceinline__ void mma_bf16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kRTThreads, 1)
+    k_router_topk(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                  const float* __restrict__ lb, const float* __restrict__ cb, float* __restrict__ logits,
+                  int32_t* __restrict__ ids, float* __restrict__ gates, int T, int E, int K, int KB, int score_func,
+                  int32_t* err)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int nst = rt_stages(E), stride = rt_stage_bytes(E), epad = rt_epad(E);
+    RouterTopkCtl* ctl = reinterpret_cast<RouterTopkCtl*>(smem + nst * stride);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = blockIdx.x;
+    const int E16 = (E + 15) / 16 * 16;
+    const uint32_t ncols = rt_tmem_cols(E16);
+    const int n0 = E16 < 256 ? E16 : 256, n1 = E16 - n0;   // the two expert chunks' MMA widths
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        mbar_init(smem_u32(&ctl->acc_full), 1);
+        ctl->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW);
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        ctl->lb[e] = lb[e];
+        ctl->cb[e] = cb[e];
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), ncols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // x and the routing outputs belong to the previous kernel on the stream until it has completed
+    griddep_wait();
+    griddep_launch_dependents();
+    const uint32_t tmem = ctl->tmem_base;
+    const volatile int* abrt = &ctl->abort;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint32_t tx = (uint32_t)stride;
+            int last = -1;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int s = kb % nst;
+                const uint32_t ph = (uint32_t)(kb / nst) & 1u;
+                if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abrt)) {
+                    router_fail(ctl, err, 21);
+                    break;
+                }
+                uint8_t* st = smem + s * stride;
+                const uint32_t fb = smem_u32(&ctl->full[s]);
+                mbar_arrive_expect_tx(fb, tx);
+                tma_load_2d(smem_u32(st), &tmX, fb, kb * 64, mt * 128);
+                for (int r = 0; r < epad; r += 128) tma_load_2d(smem_u32(st + kRTXBytes + r * 128), &tmW, fb, kb * 64, r);
+                last = kb;
+            }
+            // every copy started here has landed before the ring is read again or the CTA exits
+            int zero = 0;
+            for (int kb = last - nst + 1; kb <= last; ++kb)
+                if (kb >= 0 && !mbar_wait(smem_u32(&ctl->full[kb % nst]), (uint32_t)(kb / nst) & 1u, &zero))
+                    router_fail(ctl, err, 22);
+        }
+    } else if (warp == 1) {
+        // the whole warp runs the loop, one elected lane issues
+        const uint32_t id0 = idesc_bf16(128, (uint32_t)n0), id1 = idesc_bf16(128, (uint32_t)(n1 > 0 ? n1 : 16));
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % nst;
+            const uint32_t ph = (uint32_t)(kb / nst) & 1u;
+            if (!__all_sync(~0u, mbar_wait(smem_u32(&ctl->full[s]), ph, abrt))) {
+                if (lane == 0) router_fail(ctl, err, 23);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t st = smem_u32(smem + s * stride);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = desc_kmajor_sw128(st + 32u * k);
+                const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+                mma_bf16_elect(tmem, ad, desc_kmajor_sw128(st + kRTXBytes + 32u * k), id0, acc);
+                if (n1 > 0)
+                    mma_bf16_elect(tmem + 256u, ad, desc_kmajor_sw128(st + kRTXBytes + 256u * 128u + 32u * k), id1,
+                                   acc);
+            }
+            tc_commit_elect(smem_u32(&ctl->empty[s]));
+        }
+        // acc_full also serves as the drain: it completes once every MMA above has completed
+        tc_commit_elect(smem_u32(&ctl->acc_full));
+    }
+    __syncwarp();
+
+    // epilogue: warp (q, g) = lane quarter q, column group g; thread = token row
+    int zero = 0;
+    const bool acc_ok = mbar_wait(smem_u32(&ctl->acc_full), 0u, &zero);
+    if (!acc_ok && lane == 0) router_fail(ctl, err, 24);
+    const int q = warp & 3, g = warp >> 2;
+    const int row = q * 32 + lane;
+    const int t = mt * 128 + row;
+    const bool live = acc_ok && t < T && !ctl->abort;
+    const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
+    const int nc = (E + 15) / 16;
+    // the ring's shared memory, free once every MMA has completed: the groups'
+    // row maxima / sums, then their partial lists
+    float* red = reinterpret_cast<float*>(smem);                               // [kRTGroups][128]
+    float* pk = red + kRTGroups * 128;                                          // [128][kRTGroups][kMaxTopK]
+    float* ps = pk + 128 * kRTGroups * kMaxTopK;
+    int* pi = reinterpret_cast<int*>(ps + 128 * kRTGroups * kMaxTopK);
+    if (acc_ok) tc_fence_after();
+    // softmax: the row's maximum and the sum of exp(l - max) (each group in
+    // expert order, the groups added in group order)
+    float m = 0.f, sum = 1.f;
+    if (score_func != 0) {
+        float pm = -INFINITY;
+        for (int c = g; c < nc && acc_ok; c += kRTGroups) {
+            uint32_t v[16];
+            tmem_ld16(tl + 16u * c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (16 * c + j < E) pm = fmaxf(pm, __uint_as_float(v[j]) + ctl->lb[16 * c + j]);
+        }
+        red[g * 128 + row] = pm;
+        __syncthreads();
+        m = red[row];
+        for (int gg = 1; gg < kRTGroups; ++gg) m = fmaxf(m, red[gg * 128 + row]);
+        __syncthreads();
+        float psum = 0.f;
+        for (int c = g; c < nc && acc_ok; c += kRTGroups) {
+            uint32_t v[16];
+            tmem_ld16(tl + 16u * c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (16 * c + j < E) psum += expf(__uint_as_float(v[j]) + ctl->lb[16 * c + j] - m);
+        }
+        red[g * 128 + row] = psum;
+        __syncthreads();
+        sum = 0.f;
+        for (int gg = 0; gg < kRTGroups; ++gg) sum += red[gg * 128 + row];
+    }
+    // the top kMaxTopK under (key descending, index ascending); a fixed length
+    // keeps the list in registers, the first K entries are the top K
+    float lk[kMaxTopK], ls[kMaxTopK];
+    int li[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        lk[j] = -INFINITY;
+        ls[j] = 0.f;
+        li[j] = INT_MAX;
+    }
+    float thr_k = -INFINITY;   // the list's last entry: a candidate must beat it
+    int thr_i = INT_MAX;
+    auto insert = [&](float key, int e, float sc) {
+        if (key > thr_k || (key == thr_k && e < thr_i)) {
+            // carry the candidate down the sorted list: each entry it beats
+            // moves one place down
+            float ck = key, cs = sc;
+            int ci = e;
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                const bool b = ck > lk[j] || (ck == lk[j] && ci < li[j]);
+                const float tk = b ? lk[j] : ck, ts = b ? ls[j] : cs;
+                const int ti = b ? li[j] : ci;
+                lk[j] = b ? ck : lk[j];
+                ls[j] = b ? cs : ls[j];
+                li[j] = b ? ci : li[j];
+                ck = tk;
+                cs = ts;
+                ci = ti;
+            }
+            thr_k = lk[kMaxTopK - 1];
+            thr_i = li[kMaxTopK - 1];
+        }
+    };
+    if (acc_ok) {
+#pragma unroll 1
+        for (int c = g; c < nc; c += kRTGroups) {
+            uint32_t v[16];
+            tmem_ld16(tl + 16u * c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int e = 16 * c + j;
+                if (e < E) {
+                    const float l = __uint_as_float(v[j]) + ctl->lb[e];
+                    if (live) logits[(size_t)t * E + e] = l;
+                    const float sc = score_func == 0 ? 1.0f / (1.0f + expf(-l)) : expf(l - m) / sum;
+                    const float kv = sc + ctl->cb[e];
+                    insert(isnan(kv) ? -INFINITY : kv, e, sc);
+                }
+            }
+        }
+    }
+    __syncthreads();   // every group has read its maxima / sums
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        const int o = (row * kRTGroups + g) * kMaxTopK + j;
+        pk[o] = lk[j];
+        ps[o] = ls[j];
+        pi[o] = li[j];
+    }
+    __syncthreads();
+    if (g == 0) {
+        // merge the four partial lists of this thread's token
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            lk[j] = -INFINITY;
+            ls[j] = 0.f;
+            li[j] = INT_MAX;
+        }
+        thr_k = -INFINITY;
+        thr_i = INT_MAX;
+        for (int gg = 0; gg < kRTGroups; ++gg)
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                const int o = (row * kRTGroups + gg) * kMaxTopK + j;
+                if (pi[o] != INT_MAX) insert(pk[o], pi[o], ps[o]);
+            }
+        if (live) {
+            float ssum = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j)
+                if (j < K) ssum += ls[j];
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j)
+                if (j < K) {
+                    ids[(size_t)t * K + j] = li[j];
+                    gates[(size_t)t * K + j] = ls[j] / ssum;
+                }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, ncols);
+    }
+}
+
 cudaError_t router_set_attributes()
 {
-    return cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_router_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, kRTSmemBytes);
+    return e;
+}
+
+bool router_fused(int T, int E) { return T >= kRouterFusedMinT && E <= kMaxExperts; }
+
+cudaError_t launch_router_topk(const DevState& s, const CUtensorMap& tmX, int T, cudaStream_t st)
+{
+    const int smem = rt_stages(s.E) * rt_stage_bytes(s.E) + (int)sizeof(RouterTopkCtl) + 1024;
+    return launch_kernel(k_router_topk, dim3((T + 127) / 128), dim3(kRTThreads), smem, st, s.pdl, tmX, s.tm_wr128, s.lb,
+                         s.cb, s.logits, s.ids, s.gates, T, s.E, s.K, s.H / 64, s.score_func, s.err);
 }
 
 int router_tile_n(int T) { return T <= 512 ? 64 : 128; }

@@ -4,6 +4,7 @@ size on sampled tokens plus full routing/dispatch."""
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from parity import full_check, make_layer, run_layer
 
@@ -174,3 +175,25 @@ def test_pipelined_host_calls_match_device_forwards():
         torch.cuda.synchronize()
         assert np.array_equal(py.numpy().view(np.uint16), ref.view(torch.int16).cpu().numpy().view(np.uint16))
     layer.check_device_error()
+
+@pytest.mark.parametrize("shape", [
+    # T, H, E, I, k, bias, score: batches of at least 4096 tokens select their
+    # top-k in the router's epilogue (one CTA per 128 tokens, all experts)
+    (4100, 256, 40, 128, 6, "zipf:1.1", 0),       # one expert chunk (N = 48), ragged last token tile
+    (4160, 1024, 260, 128, 4, "normal:1.0", 0),   # a 16-wide second chunk, 16 K-steps
+    (4096, 256, 384, 128, 8, "normal:0.5", 0),    # chunks of 256 + 128, three ring stages
+    (4200, 256, 512, 128, 8, "none", 1),          # E at its maximum, softmax, two stages (the ring wraps)
+])
+def test_fused_router_shapes(shape):
+    T, H, E, I, k, bias, score = shape
+    inp = synth.custom_inputs(T, H, E, I, k, seed=900 + E, bias=bias, score_func=score)
+    layer = make_layer(inp)
+    rng = np.random.default_rng(E)
+    tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 30, replace=False)]))
+    # routing, gates, dispatch and Q1 on every token; the rest on the sample
+    stats, _, _ = full_check(layer, inp, tokens=tokens)
+    logits = layer.logits()
+    r = oracle.route(inp.x, inp.router_w, k, score, inp.logit_bias, inp.sel_bias)
+    err = np.abs(logits.astype(np.float64) - r.logits).max() / np.abs(r.logits).max()
+    print(shape, stats, "logit max rel err", err)
+    assert err <= 1e-5
