@@ -440,16 +440,38 @@ __global__ void __launch_bounds__(kRTThreads, 1)
             uint32_t v[16];
             tmem_ld16(tl + 16u * c, v);
             tmem_ld_wait();
+            // the chunk's keys first; then its candidates that beat the list's
+            // last entry go in best first, so a lane loops only as often as it
+            // inserts (the lanes are different tokens: inserting element by
+            // element would run the insertion for almost every element)
+            float kk[16], ss[16];
+            uint32_t pend = 0;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int e = 16 * c + j;
-                if (e < E) {
-                    const float l = __uint_as_float(v[j]) + ctl->lb[e];
-                    if (live) logits[(size_t)t * E + e] = l;
-                    const float sc = score_func == 0 ? 1.0f / (1.0f + expf(-l)) : expf(l - m) / sum;
-                    const float kv = sc + ctl->cb[e];
-                    insert(isnan(kv) ? -INFINITY : kv, e, sc);
-                }
+                const float l = __uint_as_float(v[j]) + (e < E ? ctl->lb[e] : 0.f);
+                if (live && e < E) logits[(size_t)t * E + e] = l;
+                const float sc = score_func == 0 ? 1.0f / (1.0f + expf(-l)) : expf(l - m) / sum;
+                const float kv = sc + (e < E ? ctl->cb[e] : 0.f);
+                kk[j] = isnan(kv) ? -INFINITY : kv;
+                ss[j] = sc;
+                pend |= (e < E ? 1u : 0u) << j;
+            }
+            while (pend) {
+                // the best pending candidate (key descending, index ascending)
+                float ck = -INFINITY, cs = 0.f;
+                int cj = -1;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (((pend >> j) & 1u) && (cj < 0 || kk[j] > ck)) {
+                        ck = kk[j];
+                        cs = ss[j];
+                        cj = j;
+                    }
+                const int ce = 16 * c + cj;
+                if (!(ck > thr_k || (ck == thr_k && ce < thr_i))) break;   // nothing left beats the list
+                pend &= ~(1u << cj);
+                insert(ck, ce, cs);
             }
         }
     }
@@ -463,21 +485,36 @@ __global__ void __launch_bounds__(kRTThreads, 1)
     }
     __syncthreads();
     if (g == 0) {
-        // merge the four partial lists of this thread's token
+        // merge the four partial lists of this thread's token: each is sorted
+        // under the same order and they hold distinct experts, so the list
+        // takes the best of the four heads kMaxTopK times
+        int hd[kRTGroups];
+#pragma unroll
+        for (int gg = 0; gg < kRTGroups; ++gg) hd[gg] = 0;
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j) {
-            lk[j] = -INFINITY;
-            ls[j] = 0.f;
-            li[j] = INT_MAX;
-        }
-        thr_k = -INFINITY;
-        thr_i = INT_MAX;
-        for (int gg = 0; gg < kRTGroups; ++gg)
+            float bk = -INFINITY, bs = 0.f;
+            int bi = INT_MAX, bg = 0;
 #pragma unroll
-            for (int j = 0; j < kMaxTopK; ++j) {
-                const int o = (row * kRTGroups + gg) * kMaxTopK + j;
-                if (pi[o] != INT_MAX) insert(pk[o], pi[o], ps[o]);
+            for (int gg = 0; gg < kRTGroups; ++gg) {
+                if (hd[gg] < kMaxTopK) {
+                    const int o = (row * kRTGroups + gg) * kMaxTopK + hd[gg];
+                    const float k2 = pk[o];
+                    const int i2 = pi[o];
+                    if (k2 > bk || (k2 == bk && i2 < bi)) {
+                        bk = k2;
+                        bi = i2;
+                        bs = ps[o];
+                        bg = gg;
+                    }
+                }
             }
+#pragma unroll
+            for (int gg = 0; gg < kRTGroups; ++gg) hd[gg] += gg == bg ? 1 : 0;
+            lk[j] = bk;
+            ls[j] = bs;
+            li[j] = bi;
+        }
         if (live) {
             float ssum = 0.f;
 #pragma unroll
