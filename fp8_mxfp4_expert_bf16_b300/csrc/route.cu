@@ -383,28 +383,44 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
 
 __device__ __forceinline__ float pow2_neg(int e) { return __int_as_float((127 - e) << 23); }
 
+// One warp per token and group of kQBlocks 1 x 128 blocks: the token's k
+// destination rows are read once, the group's loads are all in flight before
+// the first block is quantised, and each block's codes go to every
+// destination row (each store fills 128 contiguous bytes).
+constexpr int kQBlocks = 4;
+
 __global__ void __launch_bounds__(256) k_quant_scatter(const uint16_t* __restrict__ x, const int32_t* __restrict__ prow,
                                                        uint8_t* __restrict__ aq, uint32_t* __restrict__ asf, int T,
                                                        int H, int K)
 {
     griddep_wait();
     griddep_launch_dependents();
-    const int KB = H / 128, lane = threadIdx.x & 31;
+    const int KB = H / 128, NG = (KB + kQBlocks - 1) / kQBlocks, lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (gw >= (long long)T * KB) return;
-    const int t = (int)(gw / KB), b = (int)(gw - (long long)t * KB);
+    if (gw >= (long long)T * NG) return;
+    const int t = (int)(gw / NG), b0 = (int)(gw - (long long)t * NG) * kQBlocks;
     const int my_row = lane < K ? prow[(size_t)t * K + lane] : 0;
-    const uint2 v = *reinterpret_cast<const uint2*>(x + (size_t)t * H + b * 128 + lane * 4);
-    const float f0 = bf16_lo(v.x), f1 = bf16_hi(v.x), f2 = bf16_lo(v.y), f3 = bf16_hi(v.y);
-    const float amax = warp_max(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
-    const int ex = act_block_exponent(amax);
-    const float inv = pow2_neg(ex);
-    const uint32_t word = e4m3x4(f0 * inv, f1 * inv, f2 * inv, f3 * inv);
-    for (int j = 0; j < K; ++j) {
-        const int row = __shfl_sync(0xffffffffu, my_row, j);
-        *reinterpret_cast<uint32_t*>(aq + (size_t)row * H + b * 128 + lane * 4) = word;
+    uint2 v[kQBlocks];
+#pragma unroll
+    for (int i = 0; i < kQBlocks; ++i)
+        if (b0 + i < KB) v[i] = *reinterpret_cast<const uint2*>(x + (size_t)t * H + (b0 + i) * 128 + lane * 4);
+    int rows[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) rows[j] = __shfl_sync(0xffffffffu, my_row, j);
+#pragma unroll
+    for (int i = 0; i < kQBlocks; ++i) {
+        const int b = b0 + i;
+        if (b >= KB) break;
+        const float f0 = bf16_lo(v[i].x), f1 = bf16_hi(v[i].x), f2 = bf16_lo(v[i].y), f3 = bf16_hi(v[i].y);
+        const float amax = warp_max(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+        const int ex = act_block_exponent(amax);
+        const float inv = pow2_neg(ex);
+        const uint32_t word = e4m3x4(f0 * inv, f1 * inv, f2 * inv, f3 * inv);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < K) *reinterpret_cast<uint32_t*>(aq + (size_t)rows[j] * H + b * 128 + lane * 4) = word;
+        if (lane < K) asf[sf_word_index(my_row >> 7, b, KB, my_row & 127)] = (uint32_t)(ex + 127) * 0x01010101u;
     }
-    if (lane < K) asf[sf_word_index(my_row >> 7, b, KB, my_row & 127)] = (uint32_t)(ex + 127) * 0x01010101u;
 }
 
 // The fp32-scale variant: s = amax / 448 and codes e4m3(v / s), both fp32
@@ -416,23 +432,33 @@ __global__ void __launch_bounds__(256) k_quant_scatter_f32s(const uint16_t* __re
 {
     griddep_wait();
     griddep_launch_dependents();
-    const int KB = H / 128, lane = threadIdx.x & 31;
+    const int KB = H / 128, NG = (KB + kQBlocks - 1) / kQBlocks, lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (gw >= (long long)T * KB) return;
-    const int t = (int)(gw / KB), b = (int)(gw - (long long)t * KB);
+    if (gw >= (long long)T * NG) return;
+    const int t = (int)(gw / NG), b0 = (int)(gw - (long long)t * NG) * kQBlocks;
     const int my_row = lane < K ? prow[(size_t)t * K + lane] : 0;
-    const uint2 v = *reinterpret_cast<const uint2*>(x + (size_t)t * H + b * 128 + lane * 4);
-    const float f0 = bf16_lo(v.x), f1 = bf16_hi(v.x), f2 = bf16_lo(v.y), f3 = bf16_hi(v.y);
-    const float amax = warp_max(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
-    const float sc = __fdiv_rn(amax, 448.0f);
-    const uint32_t word = amax > 0.0f ? e4m3x4(__fdiv_rn(f0, sc), __fdiv_rn(f1, sc), __fdiv_rn(f2, sc),
-                                               __fdiv_rn(f3, sc))
-                                      : 0u;
-    for (int j = 0; j < K; ++j) {
-        const int row = __shfl_sync(0xffffffffu, my_row, j);
-        *reinterpret_cast<uint32_t*>(aq + (size_t)row * H + b * 128 + lane * 4) = word;
+    uint2 v[kQBlocks];
+#pragma unroll
+    for (int i = 0; i < kQBlocks; ++i)
+        if (b0 + i < KB) v[i] = *reinterpret_cast<const uint2*>(x + (size_t)t * H + (b0 + i) * 128 + lane * 4);
+    int rows[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) rows[j] = __shfl_sync(0xffffffffu, my_row, j);
+#pragma unroll
+    for (int i = 0; i < kQBlocks; ++i) {
+        const int b = b0 + i;
+        if (b >= KB) break;
+        const float f0 = bf16_lo(v[i].x), f1 = bf16_hi(v[i].x), f2 = bf16_lo(v[i].y), f3 = bf16_hi(v[i].y);
+        const float amax = warp_max(fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))));
+        const float sc = __fdiv_rn(amax, 448.0f);
+        const uint32_t word = amax > 0.0f ? e4m3x4(__fdiv_rn(f0, sc), __fdiv_rn(f1, sc), __fdiv_rn(f2, sc),
+                                                   __fdiv_rn(f3, sc))
+                                          : 0u;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < K) *reinterpret_cast<uint32_t*>(aq + (size_t)rows[j] * H + b * 128 + lane * 4) = word;
+        if (lane < K) asf32[(size_t)my_row * KB + b] = sc;
     }
-    if (lane < K) asf32[(size_t)my_row * KB + b] = sc;
 }
 
 // Small batches (T <= 256, one dispatch chunk): one block builds the expert
@@ -523,7 +549,7 @@ cudaError_t launch_dispatch_small(const DevState& s, int T, cudaStream_t st)
 
 cudaError_t launch_quant_scatter(const DevState& s, const uint16_t* x, int T, cudaStream_t st)
 {
-    const long long warps = (long long)T * (s.H / 128);
+    const long long warps = (long long)T * ((s.H / 128 + kQBlocks - 1) / kQBlocks);
     if (s.act_f32)
         return launch_kernel(k_quant_scatter_f32s, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, st, s.pdl, x,
                              (const int32_t*)s.prow, s.aq, s.asf32, T, s.H, s.K);
