@@ -222,7 +222,10 @@ moe_status moe_get_expert_out(moe_handle* h, float* out);
  * moe_get_stage_times waits for the last recorded forward and writes, for
  * each of min(n, moe_stage_count()) stages, its average milliseconds over
  * the forwards recorded since profiling was enabled or the times were last
- * read (at most the last 64); then it starts a new recording window. */
+ * read (at most the last 64); then it starts a new recording window.  The
+ * stages (moe_stage_name): router, topk, dispatch, gemm1_gate_up,
+ * gemm2_down, combine.  For batches of at least 4,096 tokens the top-k runs
+ * in the router kernel's epilogue and the topk stage times nothing. */
 moe_status moe_set_profiling(moe_handle* h, int enable);
 moe_status moe_get_stage_times(moe_handle* h, float* ms, int n);
 int moe_stage_count(void);
