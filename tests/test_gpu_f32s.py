@@ -49,6 +49,17 @@ def test_flash_decode_sampled_f32_scales():
     print("flash-decode f32s", stats)
 
 
+def test_flash_prefill_sampled_f32_scales():
+    """Prefill-sized batch: the fused router's selection, every m-tile in the
+    heavy ring (three 128-column half-step partials); routing, dispatch and
+    Q1 on every token, the rest on 16 sampled tokens."""
+    inp = synth.make_inputs("flash-prefill")
+    layer = make_layer(inp, act_scale_mode=F32)
+    toks = np.random.default_rng(7).choice(inp.x.shape[0], 16, replace=False)
+    stats, _, _ = full_check(layer, inp, tokens=np.sort(toks))
+    print("flash-prefill f32s", stats)
+
+
 def test_scale_getters():
     import fp8_mxfp4_expert_bf16_b300 as moe
     from parity import run_layer

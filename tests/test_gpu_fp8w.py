@@ -49,6 +49,17 @@ def test_flash_decode_sampled_fp8_weights():
     print("flash-decode fp8", stats)
 
 
+def test_flash_prefill_sampled_fp8_weights():
+    """Prefill-sized batch with fp8 experts: the fused router's selection and
+    the heavy promotion ring; routing, dispatch and Q1 on every token, the
+    rest on 16 sampled tokens."""
+    inp = synth.make_inputs("flash-prefill", weights="fp8")
+    layer = make_layer(inp)
+    toks = np.random.default_rng(8).choice(inp.x.shape[0], 16, replace=False)
+    stats, _, _ = full_check(layer, inp, tokens=np.sort(toks))
+    print("flash-prefill fp8", stats)
+
+
 def test_invalid_fp8_weights_are_rejected():
     import fp8_mxfp4_expert_bf16_b300 as moe
     inp = synth.make_inputs("toy", weights="fp8")
