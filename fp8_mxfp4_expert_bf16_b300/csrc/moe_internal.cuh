@@ -98,10 +98,10 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
-// Prefill-sized batches (on average at least 32 rows per expert): every
+// Prefill-sized batches (on average at least 32 rows per expert): every heavy
 // m-tile of the grouped GEMMs is loaded as a full 128-row activation box (its
 // padding rows are zero in HBM, so the MMAs on them spend little energy; the
-// GEMMs are bound by the power cap there) and there is no light phase.
+// GEMMs are bound by the power cap there).
 __host__ __forceinline__ bool prefill_mode(const DevState& s, int T) { return (long long)T * s.K >= 32LL * s.E; }
 
 // Word index of row r of m-tile mt, K-block kb, in a scale-factor buffer laid

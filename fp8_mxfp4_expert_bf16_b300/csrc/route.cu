@@ -535,10 +535,17 @@ __global__ void __launch_bounds__(kMaxExperts) k_dispatch_small(
     }
 }
 
-// m-tiles with at most this many valid rows run in the GEMMs' light phase:
-// kLightRows for decode-sized batches, none for prefill-sized ones (there
-// every m-tile is loaded as a full 128-row box, see prefill_mode)
-static int light_rows(const DevState& s, int T) { return prefill_mode(s, T) ? 0 : kLightRows; }
+// m-tiles with at most this many valid rows run in the GEMMs' light phase,
+// at every batch size: with the tokens on the MMA's N side they cost a
+// fraction of a full 128-row tile's multiply-adds (with skewed routing many
+// experts' last m-tiles hold a few rows: Pro prefill 2.5% faster, at higher
+// clocks under the power cap; Flash prefill unchanged)
+static int light_rows(const DevState& s, int T)
+{
+    (void)s;
+    (void)T;
+    return kLightRows;
+}
 
 cudaError_t launch_dispatch_small(const DevState& s, int T, cudaStream_t st)
 {
