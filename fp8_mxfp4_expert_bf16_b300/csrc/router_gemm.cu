@@ -193,12 +193,12 @@ __global__ void __launch_bounds__(128, 1)
 // chunk): logits (+ logit bias, also stored for the getters), scores
 // (sigmoid, or softmax over the experts, its row maximum and sum combined
 // across the groups through shared memory), keys = scores + correction
-// bias, and each thread's partial top 8 by insertion under the order key
-// descending, ties to the lower expert index, a NaN key ranking last.  One
-// thread per token then merges its four partial lists (the ring's shared
-// memory is free once the MMAs are done) under the same order -- the
-// selection of the separate top-k kernel; gates = the selected scores /
-// their sum, summed in selection order.
+// bias, and each thread's partial top 8 under the order key descending,
+// ties to the lower expert index, a NaN key ranking last (a chunk's
+// candidates enter best first).  One thread per token then merges its four
+// sorted partial lists by their heads (the ring's shared memory is free once
+// the MMAs are done) -- the selection of the separate top-k kernel; gates =
+// the selected scores / their sum, summed in selection order.
 constexpr int kRTMaxStages = 4;
 constexpr int kRTGroups = 4;                             // epilogue warps per TMEM lane quarter (column groups)
 constexpr int kRTThreads = 32 * 4 * kRTGroups;
