@@ -535,23 +535,17 @@ __global__ void __launch_bounds__(kMaxExperts) k_dispatch_small(
     }
 }
 
-// m-tiles with at most this many valid rows run in the GEMMs' light phase,
-// at every batch size: with the tokens on the MMA's N side they cost a
-// fraction of a full 128-row tile's multiply-adds (with skewed routing many
-// experts' last m-tiles hold a few rows: Pro prefill 2.5% faster, at higher
-// clocks under the power cap; Flash prefill unchanged)
-static int light_rows(const DevState& s, int T)
-{
-    (void)s;
-    (void)T;
-    return kLightRows;
-}
+// m-tiles with at most kLightRows valid rows run in the GEMMs' light phase at
+// every batch size: with the tokens on the MMA's N side they cost a fraction
+// of a full 128-row tile's multiply-adds (with skewed routing many experts'
+// last m-tiles hold a few rows: Pro prefill 2.5% faster, at higher clocks
+// under the power cap; Flash prefill unchanged).
 
 cudaError_t launch_dispatch_small(const DevState& s, int T, cudaStream_t st)
 {
     return launch_kernel(k_dispatch_small, dim3(1), dim3(kMaxExperts), 0, st, s.pdl, (const int32_t*)s.ids, s.counts,
                          s.offsets, s.mtile_off, s.mtile_expert, s.mtile_rows, s.n_mtiles, s.light_list, s.heavy_list,
-                         s.prow, T, s.E, s.K, light_rows(s, T));
+                         s.prow, T, s.E, s.K, kLightRows);
 }
 
 cudaError_t launch_quant_scatter(const DevState& s, const uint16_t* x, int T, cudaStream_t st)
@@ -572,7 +566,7 @@ cudaError_t launch_dispatch(const DevState& s, const uint16_t* x, int T, cudaStr
     if (e == cudaSuccess)
         e = launch_kernel(k_scan, dim3(1), dim3(kMaxExperts), 0, st, s.pdl, (const int32_t*)s.chunk_hist, s.chunk_base,
                           s.counts, s.offsets, s.mtile_off, s.mtile_expert, s.mtile_rows, s.n_mtiles, s.light_list,
-                          s.heavy_list, nchunk, s.E, light_rows(s, T));
+                          s.heavy_list, nchunk, s.E, kLightRows);
     if (e == cudaSuccess)
         e = launch_kernel(k_scatter_rows, dim3(nchunk), dim3(kChunk), 0, st, s.pdl, (const int32_t*)s.ids,
                           (const int32_t*)s.chunk_base, (const int32_t*)s.mtile_off, s.prow, T, s.E, s.K);
